@@ -28,8 +28,8 @@
  * Precision (the pages leave it open; this is the reading taken): min/max are
  * exact fp16 comparisons, the scale is computed in fp32 then rounded to fp16,
  * the code is computed in fp32 with IEEE division and round-half-to-even,
- * a zero (or fp16-underflowing) scale gives code 0, a -0.0 minimum is stored as
- * +0.0.  Dequantization and attention use fp64.
+ * a zero (or fp16-underflowing) scale gives code 0, a -0.0 minimum (or maximum)
+ * is taken as +0.0, so the stored min and scale never carry a negative zero.  Dequantization and attention use fp64.
  *
  * Build: cc -O2 -fno-fast-math -ffp-contract=off -shared -fPIC.
  */
@@ -101,6 +101,8 @@ void kvq_or_quant_group(const uint16_t *x, long stride, int n, int max_int,
     }
     if (mn == 0.0f)
         mn = 0.0f;                      /* store -0.0 as +0.0 */
+    if (mx == 0.0f)
+        mx = 0.0f;                      /* so an all-zero group has scale +0.0 */
     float range = mx - mn;              /* fp32, round to nearest */
     float s32 = range / (float)max_int; /* fp32 IEEE division */
     uint16_t s16 = kvq_or_f2h(s32);     /* scale kept in fp16 */

@@ -455,3 +455,12 @@ def test_packed_sizes_match_accounting():
         n = B * H * 4 * G * D
         assert ck.nbytes == cv.nbytes == n * bits // 8
         assert mk.nbytes == mv.nbytes == n // G * 4
+
+
+def test_signed_zero_groups_store_positive_zero():
+    """Groups of +0/-0 in any order: scale and min are +0.0 (no sign from the order)."""
+    for vals in ([0.0, -0.0], [-0.0, 0.0], [-0.0, -0.0, 0.0], [-0.0]):
+        s, mn, c = oracle.quant_group(np.array(vals, np.float16), 2)
+        assert np.float16(s).view(np.uint16) == 0 and np.float16(mn).view(np.uint16) == 0
+    s, mn, c = oracle.quant_group(np.array([-1.0, -0.0], np.float16), 2)
+    assert float(mn) == -1.0 and c.tolist() == [0, 3]
