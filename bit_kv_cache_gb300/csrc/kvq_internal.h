@@ -1,0 +1,96 @@
+// kvq_internal.h -- kernel parameter blocks and launchers shared by the libkvq
+// translation units (not part of the public ABI; see include/kvq.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+struct QuantKParams {
+    const uint16_t *src;   // fp16 [U][*][D]
+    int64_t src_ustride;   // elements between sequences
+    int64_t src_t0;        // first source row
+    int64_t n_pages;       // pages of G tokens to quantize
+    int64_t pg0;           // destination page index of the first one
+    int64_t max_T;
+    int U, D, G, n_boost, slices;
+    int32_t *k_codes, *k_hi;
+    uint8_t *k_bidx;
+    uint16_t *k_meta;
+};
+
+struct QuantVParams {
+    const uint16_t *src;
+    int64_t src_ustride, src_t0;
+    int64_t n_tok;         // tokens to quantize (multiple of G)
+    int64_t tok0;          // destination packed-token index of the first one
+    int64_t max_T;
+    int U, D, G, Gv;
+    int32_t *v_codes;
+    uint16_t *v_meta;
+};
+
+struct CopyRowsParams {
+    const uint16_t *src;
+    uint16_t *dst;
+    int64_t src_rows, src_r0, dst_rows, dst_r0, n_rows;
+    int U, D;
+};
+
+struct AppendParams {
+    const uint16_t *k_new, *v_new;
+    uint16_t *k_dst, *v_dst, *v_evict;
+    int64_t k_rows, k_row, v_rows, v_row, evict_rows, evict_row;  // evict_row < 0: none
+    int U, D;
+};
+
+// Decode attention schedule.  Fast items are tiles of TOK tokens whose keys and
+// values are both packed (tensor-core path); the flattened list of all sequences'
+// tiles (sequence-major, N_f = U * n_fast) is cut into W_f = 8 * C_f equal warp
+// ranges, each of length <= n_fast, so a warp touches at most two sequences.
+// Generic items are chunks of gen_chunk tokens of the rest of each sequence (sink,
+// fp16 buffers, packed tokens outside the tiles; CUDA-core path), one chunk per
+// warp, n_gc chunks per sequence.  CTAs [0, C_f) run fast warps, CTAs
+// [C_f, C_f + C_g) generic warps.  A CTA merges its warps' partial softmax states
+// per sequence into one slot; the last CTA of a sequence (ticket) combines.
+struct DecodeParams {
+    // shape
+    int B, H_kv, g, D, G, bits, Gv, n_boost, kitty;
+    int S_cap, cap_k, cap_v, R_local;
+    int64_t max_T;
+    // lengths
+    int64_t n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head, L;
+    // buffers
+    const int32_t *k_codes, *k_hi;
+    const uint8_t *k_bidx;
+    const uint16_t *k_meta;
+    const int32_t *v_codes;
+    const uint16_t *v_meta;
+    const uint16_t *k_sink, *v_sink, *k_res, *v_res, *v_local;
+    const uint16_t *q;
+    uint16_t *out;
+    float *partials;       // [U][max_slots][g][D + 2]
+    float *scratch;        // [8 * C_f][8][D + 2] first-segment partials of fast warps
+    int32_t *tickets;      // [U]
+    int32_t *status;       // workspace status word
+    // schedule
+    int U, C_f, C_g, n_gc, max_slots;
+    int64_t n_fast;        // fast tiles per sequence
+    int64_t N_f;           // U * n_fast
+    int64_t n_gen;         // generic tokens per sequence
+    int64_t gen_chunk;     // tokens per generic chunk (multiple of 32)
+};
+
+constexpr int kWarps = 8;
+constexpr int kStages = 2;
+
+cudaError_t launch_quant_k(const QuantKParams &p, int bits, bool kitty, cudaStream_t st);
+cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
+cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
+size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D);
+int decode_max_ctas_per_sm(int bits, bool kitty, int n_boost, int D, bool fast);
+
+}  // namespace kvq

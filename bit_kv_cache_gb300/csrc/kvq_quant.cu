@@ -1,0 +1,373 @@
+// kvq_quant.cu -- quantize/pack kernels (keys per channel, values per token, Kitty
+// key pages), plus the row-copy and token-append kernels of the cache.
+//
+// The quantizer is the min-max asymmetric one of the KIVI notes (Step 1):
+//   scale = fp16( (max - min) / (2^b - 1) ),  code = clamp(rint((x - min) / scale))
+// with min/max exact in fp16, the scale computed in fp32 (IEEE division) and
+// rounded to fp16, the code computed in fp32 with IEEE division and
+// round-half-to-even, a zero scale giving code 0, and signed zeros of min/max
+// taken as +0.  Codes are packed 32/b per int32, element j at bit b*j (KIVI
+// notes, Step 2, pack_tensor).
+//
+// Division without a divide per element: r = (x - min) * rcp(scale) differs from
+// the correctly rounded quotient q = fl(d / scale) by at most 3 ulp-relative
+// (|r - q| <= 2^-22 * |q|), so rint(r) == rint(q) whenever r is farther than
+// 2^-11 from a half-integer (for |q| <= 2^10; larger quotients clamp to max_int on
+// both sides).  Only those near-tie elements redo the IEEE division (__fdiv_rn),
+// which makes every code identical to the one the plain definition gives.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// Group parameters from exact fp16 min/max (as fp32 values).
+struct GroupQ {
+    float mn, s, inv, maxf;
+    uint16_t s16, mn16;
+    bool zero;
+};
+
+__device__ __forceinline__ GroupQ make_group(float mn, float mx, int max_int) {
+    GroupQ g;
+    if (mn == 0.0f) mn = 0.0f;  // -0 -> +0
+    if (mx == 0.0f) mx = 0.0f;
+    float range = __fsub_rn(mx, mn);
+    float s32 = __fdiv_rn(range, (float)max_int);
+    __half sh = __float2half_rn(s32);
+    g.s16 = __half_as_ushort(sh);
+    g.mn16 = __half_as_ushort(__float2half_rn(mn));  // exact: mn is an fp16 value
+    g.mn = mn;
+    g.s = __half2float(sh);
+    g.zero = (g.s == 0.0f);
+    g.inv = g.zero ? 0.0f : __frcp_rn(g.s);
+    g.maxf = (float)max_int;
+    return g;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float x, const GroupQ &g) {
+    float d = __fsub_rn(x, g.mn);  // >= 0
+    float r = __fmul_rn(d, g.inv);
+    float k = rintf(r);
+    if (fabsf(__fsub_rn(r, k)) > 0.5f - 0x1p-11f) k = rintf(__fdiv_rn(d, g.s));
+    k = fminf(k, g.maxf);
+    return g.zero ? 0u : (uint32_t)k;
+}
+
+// |x| * 2^24 of an fp16 value as an exact integer.
+__device__ __forceinline__ unsigned long long abs_units(uint32_t h) {
+    uint32_t e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+    if (e == 0) return m;
+    return (unsigned long long)(m | 0x400u) << (e - 1);
+}
+
+// ------------------------------------------------------------------------------
+// Keys: one CTA per page of G tokens.  Thread (pair pr, slice sl) holds channels
+// 2pr, 2pr+1 for TPS consecutive tokens in registers; min/max (and, for Kitty, the
+// channel scores) are combined across slices in shared memory.
+// ------------------------------------------------------------------------------
+template <int BITS, bool KITTY, int TPS>
+__global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
+    constexpr int FPI = KITTY ? 16 : 32 / BITS;  // codes per word of the (low) plane
+    constexpr int CB = KITTY ? 2 : BITS;          // bits per code in that plane
+    constexpr int NW = TPS / FPI;                 // words per channel per thread
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int D = p.D, pairs = D >> 1, S = p.slices;
+    float *s_min = reinterpret_cast<float *>(smem);           // [S][D]
+    float *s_max = s_min + S * D;                             // [S][D]
+    unsigned long long *s_score =
+        reinterpret_cast<unsigned long long *>(s_max + S * D);  // [S][D] (Kitty)
+    int *s_slot = reinterpret_cast<int *>(s_score + (KITTY ? S * D : 0));  // [D]
+
+    const int tid = threadIdx.x, pr = tid % pairs, sl = tid / pairs;
+    const bool active = sl < S;
+    const int u = blockIdx.y;
+    const int64_t pg = blockIdx.x;
+    const int d0 = 2 * pr;
+
+    uint32_t x[TPS];
+    if (active) {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(
+            p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + pg * p.G + sl * TPS) * D) + pr;
+#pragma unroll
+        for (int i = 0; i < TPS; i++) x[i] = __ldg(src + (size_t)i * pairs);
+        __half2 lo = *reinterpret_cast<__half2 *>(&x[0]), hi = lo;
+#pragma unroll
+        for (int i = 1; i < TPS; i++) {
+            __half2 v = *reinterpret_cast<__half2 *>(&x[i]);
+            lo = __hmin2(lo, v);
+            hi = __hmax2(hi, v);
+        }
+        float2 fl = __half22float2(lo), fh = __half22float2(hi);
+        s_min[sl * D + d0] = fl.x;
+        s_min[sl * D + d0 + 1] = fl.y;
+        s_max[sl * D + d0] = fh.x;
+        s_max[sl * D + d0 + 1] = fh.y;
+        if (KITTY) {
+            unsigned long long a0 = 0, a1 = 0;
+#pragma unroll
+            for (int i = 0; i < TPS; i++) {
+                a0 += abs_units(x[i] & 0xffffu);
+                a1 += abs_units(x[i] >> 16);
+            }
+            s_score[sl * D + d0] = a0;
+            s_score[sl * D + d0 + 1] = a1;
+        }
+    }
+    __syncthreads();
+    if (KITTY) {
+        // Boost selection (Kitty, Sec. 3.2): the n_boost channels with the largest
+        // sum |k| over the page; equal scores go to the lower channel index; slots in
+        // ascending channel order, sentinel n_boost+1 otherwise.
+        if (tid < D) {
+            unsigned long long sc = 0;
+            for (int s = 0; s < S; s++) sc += s_score[s * D + tid];
+            s_score[tid] = sc;  // slice 0 row now holds the page score
+        }
+        __syncthreads();
+        bool boosted = false;
+        if (tid < D) {
+            unsigned long long sc = s_score[tid];
+            int rank = 0;
+            for (int e = 0; e < D; e++) {
+                unsigned long long o = s_score[e];
+                rank += (o > sc) || (o == sc && e < tid);
+            }
+            boosted = rank < p.n_boost;
+            s_slot[tid] = boosted ? 1 : 0;
+        }
+        __syncthreads();
+        int slot = 0;
+        if (tid < D) {
+            for (int e = 0; e < tid; e++) slot += s_slot[e];
+        }
+        __syncthreads();
+        if (tid < D) s_slot[tid] = boosted ? slot : p.n_boost + 1;
+        __syncthreads();
+    }
+    if (!active) return;
+
+    GroupQ gq[2];
+    int slot[2] = {0, 0};
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        float mn = s_min[d0 + c], mx = s_max[d0 + c];
+        for (int s = 1; s < S; s++) {
+            mn = fminf(mn, s_min[s * D + d0 + c]);
+            mx = fmaxf(mx, s_max[s * D + d0 + c]);
+        }
+        int max_int = (1 << BITS) - 1;
+        if (KITTY) {
+            slot[c] = s_slot[d0 + c];
+            max_int = slot[c] < p.n_boost ? 15 : 3;
+        }
+        gq[c] = make_group(mn, mx, max_int);
+    }
+
+    const int64_t page = p.pg0 + pg;
+    const int64_t wrow0 = page * (p.G / FPI) + sl * NW;  // first word row of this thread
+    uint2 *dst = reinterpret_cast<uint2 *>(p.k_codes + (size_t)u * (p.max_T / FPI) * D) + pr;
+#pragma unroll
+    for (int wi = 0; wi < NW; wi++) {
+        uint32_t w0 = 0, w1 = 0, h0 = 0, h1 = 0;
+#pragma unroll
+        for (int j = 0; j < FPI; j++) {
+            __half2 v = *reinterpret_cast<__half2 *>(&x[wi * FPI + j]);
+            float2 f = __half22float2(v);
+            uint32_t c0 = quant_code(f.x, gq[0]), c1 = quant_code(f.y, gq[1]);
+            w0 |= (c0 & ((1u << CB) - 1)) << (CB * j);
+            w1 |= (c1 & ((1u << CB) - 1)) << (CB * j);
+            if (KITTY) {
+                h0 |= (c0 >> 2) << (2 * j);
+                h1 |= (c1 >> 2) << (2 * j);
+            }
+        }
+        dst[(size_t)(wrow0 + wi) * pairs] = make_uint2(w0, w1);
+        if (KITTY) {
+            int32_t *hp = p.k_hi + ((size_t)u * (p.max_T / 16) + wrow0 + wi) * p.n_boost;
+            if (slot[0] < p.n_boost) hp[slot[0]] = (int32_t)h0;
+            if (slot[1] < p.n_boost) hp[slot[1]] = (int32_t)h1;
+        }
+    }
+    if (sl == 0) {
+        uint2 m;
+        m.x = (uint32_t)gq[0].s16 | ((uint32_t)gq[0].mn16 << 16);
+        m.y = (uint32_t)gq[1].s16 | ((uint32_t)gq[1].mn16 << 16);
+        reinterpret_cast<uint2 *>(p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * D * 2)[pr] = m;
+        if (KITTY) {
+            uint8_t *bi = p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * D;
+            bi[d0] = (uint8_t)slot[0];
+            bi[d0 + 1] = (uint8_t)slot[1];
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------
+// Values: one thread per token; the whole row (ND x 8 halves) sits in registers.
+// ------------------------------------------------------------------------------
+template <int BITS, int ND, int GV>
+__global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
+    constexpr int FPI = 32 / BITS, D = ND * 8, NWORD = D / FPI;
+    static_assert(GV % FPI == 0 && D % GV == 0, "whole words per value group");
+    const int u = blockIdx.y;
+    const int64_t tl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // token within call
+    if (tl >= p.n_tok) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + tl) * D);
+    uint32_t xw[D / 2];  // the token's row as half2 words
+#pragma unroll
+    for (int i = 0; i < ND; i++) {
+        uint4 v = __ldg(src + i);
+        xw[4 * i] = v.x;
+        xw[4 * i + 1] = v.y;
+        xw[4 * i + 2] = v.z;
+        xw[4 * i + 3] = v.w;
+    }
+    const int64_t tau = p.tok0 + tl;  // index within the packed value region
+    const int64_t page = tau / p.G, tin = tau % p.G;
+    int32_t *vc = p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * NWORD) * p.G + tin;
+    uint32_t *vm = reinterpret_cast<uint32_t *>(p.v_meta) + ((size_t)u * p.max_T + tau) * (D / GV);
+#pragma unroll
+    for (int g0 = 0; g0 < D; g0 += GV) {
+        __half2 lo = *reinterpret_cast<const __half2 *>(&xw[g0 / 2]), hi = lo;
+#pragma unroll
+        for (int i = 1; i < GV / 2; i++) {
+            __half2 v = *reinterpret_cast<const __half2 *>(&xw[g0 / 2 + i]);
+            lo = __hmin2(lo, v);
+            hi = __hmax2(hi, v);
+        }
+        float mn = fminf(__low2float(lo), __high2float(lo));
+        float mx = fmaxf(__low2float(hi), __high2float(hi));
+        GroupQ g = make_group(mn, mx, (1 << BITS) - 1);
+        vm[g0 / GV] = (uint32_t)g.s16 | ((uint32_t)g.mn16 << 16);
+#pragma unroll
+        for (int wi = g0 / FPI; wi < (g0 + GV) / FPI; wi++) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int j = 0; j < FPI; j += 2) {
+                float2 f = unpack_half2(xw[(wi * FPI + j) / 2]);
+                w |= quant_code(f.x, g) << (BITS * j);
+                w |= quant_code(f.y, g) << (BITS * (j + 1));
+            }
+            vc[(size_t)wi * p.G] = (int32_t)w;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------
+// Row copies between [U][*][D] fp16 buffers (prefill split, flush bookkeeping).
+// ------------------------------------------------------------------------------
+__global__ void copy_rows_kernel(CopyRowsParams p) {
+    const int64_t chunks = (int64_t)p.n_rows * (p.D / 8);
+    const int64_t total = chunks * p.U;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t u = i / chunks, r = i % chunks;
+        int64_t row = r / (p.D / 8), c = r % (p.D / 8);
+        const uint4 *s = reinterpret_cast<const uint4 *>(
+            p.src + ((size_t)u * p.src_rows + p.src_r0 + row) * p.D) + c;
+        uint4 *d = reinterpret_cast<uint4 *>(p.dst + ((size_t)u * p.dst_rows + p.dst_r0 + row) * p.D) + c;
+        *d = *s;
+    }
+}
+
+// One new token per sequence: key row -> k_dst[k_row]; value row -> v_dst[v_row],
+// after moving v_dst's old row to v_evict[evict_row] when evict_row >= 0 (Kitty
+// local window full: the oldest value leaves the window for the Q-buffer).
+__global__ void append_kernel(AppendParams p) {
+    const int64_t chunks = p.D / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= chunks * p.U) return;
+    const int64_t u = i / chunks, c = i % chunks;
+    const uint4 *kn = reinterpret_cast<const uint4 *>(p.k_new + (size_t)u * p.D) + c;
+    const uint4 *vn = reinterpret_cast<const uint4 *>(p.v_new + (size_t)u * p.D) + c;
+    uint4 *kd = reinterpret_cast<uint4 *>(p.k_dst + ((size_t)u * p.k_rows + p.k_row) * p.D) + c;
+    uint4 *vd = reinterpret_cast<uint4 *>(p.v_dst + ((size_t)u * p.v_rows + p.v_row) * p.D) + c;
+    *kd = *kn;
+    if (p.evict_row >= 0) {
+        uint4 *ev = reinterpret_cast<uint4 *>(p.v_evict + ((size_t)u * p.evict_rows + p.evict_row) * p.D) + c;
+        *ev = *vd;
+    }
+    *vd = *vn;
+}
+
+// ------------------------------------------------------------------------------
+// Launchers
+// ------------------------------------------------------------------------------
+template <int BITS, bool KITTY>
+static cudaError_t launch_qk_tps(const QuantKParams &p, int tps, size_t smem, cudaStream_t st) {
+    dim3 grid((unsigned)p.n_pages, (unsigned)p.U);
+    switch (tps) {
+#define KVQ_TPS(T)                                                                        \
+    case T:                                                                               \
+        if (smem > 48 * 1024)                                                             \
+            cudaFuncSetAttribute(quant_k_kernel<BITS, KITTY, T>,                          \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        quant_k_kernel<BITS, KITTY, T><<<grid, 256, smem, st>>>(p);                       \
+        return cudaGetLastError();
+        KVQ_TPS(16)
+        KVQ_TPS(32)
+        KVQ_TPS(64)
+#undef KVQ_TPS
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quant_k(const QuantKParams &p_in, int bits, bool kitty, cudaStream_t st) {
+    QuantKParams p = p_in;
+    if (p.n_pages <= 0) return cudaSuccess;
+    const int fpi = kitty ? 16 : 32 / bits;
+    const int pairs = p.D / 2;
+    int smax = 256 / pairs;
+    int nwords = p.G / fpi;  // word rows per page
+    int S = 1;
+    for (int s = 1; s <= smax && s <= nwords; s++)
+        if (nwords % s == 0 && (p.G / s) <= 64) S = s;
+    int tps = p.G / S;
+    if (tps > 64 || (tps != 16 && tps != 32 && tps != 64)) return cudaErrorInvalidValue;
+    p.slices = S;
+    size_t smem = (size_t)S * p.D * 8 + (kitty ? (size_t)S * p.D * 8 + (size_t)p.D * 4 : 0);
+    if (kitty) return launch_qk_tps<2, true>(p, tps, smem, st);
+    if (bits == 2) return launch_qk_tps<2, false>(p, tps, smem, st);
+    if (bits == 4) return launch_qk_tps<4, false>(p, tps, smem, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st) {
+    if (p.n_tok <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((p.n_tok + 127) / 128), (unsigned)p.U);
+#define KVQ_QV(B, N, GVV)                                          \
+    if (bits == B && p.D == N * 8 && p.Gv == GVV) {                \
+        quant_v_kernel<B, N, GVV><<<grid, 128, 0, st>>>(p);        \
+        return cudaGetLastError();                                 \
+    }
+#define KVQ_QV_B(B)                                                        \
+    KVQ_QV(B, 8, 32) KVQ_QV(B, 8, 64)                                      \
+    KVQ_QV(B, 16, 32) KVQ_QV(B, 16, 64) KVQ_QV(B, 16, 128)                 \
+    KVQ_QV(B, 32, 32) KVQ_QV(B, 32, 64) KVQ_QV(B, 32, 128) KVQ_QV(B, 32, 256)
+    KVQ_QV_B(2)
+    KVQ_QV_B(4)
+#undef KVQ_QV_B
+#undef KVQ_QV
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st) {
+    if (p.n_rows <= 0) return cudaSuccess;
+    int64_t total = (int64_t)p.U * p.n_rows * (p.D / 8);
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    copy_rows_kernel<<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
+    int64_t total = (int64_t)p.U * (p.D / 8);
+    append_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,191 @@
+/*
+ * kvq.h -- C ABI of the GB300 low-bit KV-cache library (libkvq.so).
+ *
+ * The library quantizes the key/value cache of one attention layer into 2- or
+ * 4-bit codes and runs single-query (and grouped-query) decode attention
+ * directly on the packed codes.  It follows:
+ *   - KIVI ("KV Cache 量化算子：KIVI"): min-max asymmetric quantization,
+ *     scale = (max-min)/(2^b-1), keys per channel over groups of G tokens,
+ *     values per token, 32/b codes packed per int32 (pack_tensor), an fp16
+ *     residual of recent tokens, decode attention that unpacks in-kernel;
+ *   - Kitty ("Kitty: Accurate and Efficient 2-Bit KV Cache Quantization with
+ *     Dynamic Channel-wise Precision Boost"): fp16 sink tokens, key/value
+ *     Q-buffers of G tokens, a value local window of R tokens, and per page the
+ *     top n_boost key channels kept at INT4 as a low 2-bit plane plus a compact
+ *     high 2-bit plane and a boost index (Sec. 3.2, Sec. 4.1, Algorithm 1);
+ *   - BitDecoding (arXiv 2503.18773): attention softmax(q D(K')^T) D(V') on the
+ *     packed cache, with the query heads of a GQA group processed together as
+ *     one tensor-core tile (Sec. V-A, query transformation).
+ *
+ * Conventions for every entry point:
+ *   - All buffers are caller-owned.  Pointers marked "device" are CUDA device
+ *     memory of the current device, 16-byte aligned.  The library never
+ *     allocates memory.
+ *   - fp16 data is passed as uint16_t (IEEE binary16 bit patterns).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; the host-side lengths in kvq_cache are updated at
+ *     enqueue time.  No entry point synchronizes the stream except
+ *     kvq_read_status.
+ *   - Return value: KVQ_OK or a negative kvq_status.  No entry point aborts or
+ *     throws.  On an argument error nothing is enqueued and the cache is not
+ *     modified.  KVQ_ERR_CUDA means a launch failed (cudaGetLastError).
+ *   - Every sequence (b, h_kv) of a cache has the same length.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = -1,  /* bad shape, pointer, alignment or length       */
+    KVQ_ERR_UNSUPPORTED = -2,  /* valid but not implemented (bits, D, g, ...)    */
+    KVQ_ERR_CAPACITY = -3,     /* packed region or a buffer would overflow       */
+    KVQ_ERR_WORKSPACE = -4,    /* workspace missing or too small                 */
+    KVQ_ERR_CUDA = -5,         /* a CUDA launch or copy failed                    */
+    KVQ_ERR_DEVICE = -6        /* a kernel reported an error in the status word   */
+} kvq_status;
+
+enum { KVQ_MODE_KIVI = 0, KVQ_MODE_KITTY = 1 };
+
+/* Device status bits (see kvq_read_status). */
+enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
+
+/* Shape of one layer's cache.
+ *   B, H_q, H_kv, D : batch, query heads, key/value heads (H_q % H_kv == 0), head dim
+ *   G               : group / page size in tokens (keys are quantized per channel over
+ *                     G tokens; values per token over Gv = min(G, D) channels)
+ *   bits            : 2 or 4 (Kitty: 2; its boosted key channels reach 4 bits)
+ *   S               : fp16 attention-sink tokens kept at the start (0 = none)
+ *   R               : KIVI: fp16 residual capacity, a multiple of G, flushed as R/G
+ *                     groups once full.  Kitty: the value local window.
+ *   n_boost         : Kitty: key channels per page kept at INT4 (0..min(D,254)).
+ *                     Must be 0 in KIVI mode.
+ *   mode            : KVQ_MODE_KIVI or KVQ_MODE_KITTY
+ *   max_T           : packed-token capacity per sequence, a multiple of G       */
+typedef struct {
+    int32_t B, H_q, H_kv, D, G, bits;
+    int32_t S, R, n_boost, mode;
+    int64_t max_T;
+} kvq_config;
+
+/* Caller-owned device buffers and host-side lengths of one layer's cache.
+ * Layouts (U = B*H_kv sequences, fpi = 32/bits codes per int32, element j of a
+ * word at bit bits*j, least significant first):
+ *   k_codes  int32 [U][max_T/fpi][D]     keys packed along tokens: word (w, d) holds
+ *                                        tokens fpi*w .. fpi*w+fpi-1 of channel d.
+ *                                        Kitty: the low 2-bit plane (fpi = 16).
+ *   k_hi     int32 [U][max_T/16][n_boost] Kitty: high 2 bits of the boosted channels,
+ *                                        slot order; NULL if n_boost == 0.
+ *   k_bidx   uint8 [U][max_T/G][D]       Kitty: channel -> slot, n_boost+1 if not
+ *                                        boosted; NULL in KIVI mode.
+ *   k_meta   fp16  [U][max_T/G][D][2]    (scale, min) per channel per group.
+ *   v_codes  int32 [U][max_T/G][D/fpi][G] values packed along channels; within a
+ *                                        page of G tokens, word (m, t) holds channels
+ *                                        fpi*m .. fpi*m+fpi-1 of token t.
+ *   v_meta   fp16  [U][max_T][D/Gv][2]   (scale, min) per token per channel group.
+ *   k_sink, v_sink  fp16 [U][S][D]       (NULL if S == 0)
+ *   k_res    fp16  [U][cap_k][D]         cap_k = R (KIVI residual) or G (Kitty Q-buffer)
+ *   v_res    fp16  [U][cap_v][D]         cap_v = R (KIVI residual) or G (Kitty Q-buffer)
+ *   v_local  fp16  [U][R][D]             Kitty local window (ring, oldest at
+ *                                        local_head); NULL in KIVI mode.
+ *   status   int32 device word that kernels OR error bits into (may be NULL).
+ * Lengths: n_sink sink tokens, T_k / T_v packed key / value tokens, n_kres keys in
+ * k_res, n_vres values in v_res, n_local values in v_local.  A fresh cache has all
+ * lengths 0.  Logical token order: keys [sink | packed | k_res], values
+ * [sink | packed | v_res | v_local (oldest first)]. */
+typedef struct {
+    int32_t *k_codes;
+    int32_t *k_hi;
+    uint8_t *k_bidx;
+    uint16_t *k_meta;
+    int32_t *v_codes;
+    uint16_t *v_meta;
+    uint16_t *k_sink, *v_sink;
+    uint16_t *k_res, *v_res, *v_local;
+    int32_t *status;
+    int64_t n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head;
+} kvq_cache;
+
+/* Text for a kvq_status value (static string). */
+const char *kvq_status_str(int status);
+
+/* Validates a configuration.  KVQ_OK, KVQ_ERR_INVALID_ARG (H_q % H_kv, G % fpi,
+ * D % fpi, Gv | D, R % G (KIVI), n_boost range, max_T % G, non-positive sizes) or
+ * KVQ_ERR_UNSUPPORTED (bits not 2/4, Kitty with bits != 2, D not a multiple of 8). */
+int kvq_config_check(const kvq_config *cfg);
+
+/* Byte size of each cache buffer for cfg: which = 0 k_codes, 1 k_hi, 2 k_bidx,
+ * 3 k_meta, 4 v_codes, 5 v_meta, 6 k_sink (= v_sink), 7 k_res, 8 v_res, 9 v_local.
+ * Returns 0 for a buffer the mode does not use or for an invalid cfg. */
+size_t kvq_buffer_bytes(const kvq_config *cfg, int which);
+
+/* Prefill of the keys (KIVI page, Step 3: after prefill the cache is split into
+ * a low-bit part and an fp16 residual).  k: device fp16 [B][H_kv][L0][D].
+ * The first min(S, L0) tokens go to k_sink; the next floor((L0-n_sink)/G)*G are
+ * quantized per channel in groups of G tokens into k_codes/k_meta (Kitty: the
+ * top n_boost channels of each page by sum |k| at 4 bits, the rest at 2); the
+ * remainder (< G) is copied to k_res.  Requires an empty key cache (T_k == 0,
+ * n_kres == 0) and 1 <= L0.  KVQ_ERR_CAPACITY if the packed part exceeds max_T. */
+int kvq_quant_pack_k(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k,
+                     int64_t L0, void *stream);
+
+/* Prefill of the values.  v: device fp16 [B][H_kv][L0][D].  Sink as for keys.
+ * KIVI: floor((L0-n_sink)/G)*G tokens quantized per token in groups of Gv
+ * channels, the rest copied to v_res.  Kitty: the last min(R, L0-n_sink) tokens go
+ * to the local window; of the older ones floor(./G)*G are quantized and the rest
+ * copied to the value Q-buffer (v_res).  Requires an empty value cache. */
+int kvq_quant_pack_v(const kvq_config *cfg, kvq_cache *cache, const uint16_t *v,
+                     int64_t L0, void *stream);
+
+/* Stage (1) of the Kitty decode pipeline (Sec. 4.3): insert one new token.
+ * k_new, v_new: device fp16 [B][H_kv][D].  While the sink is not full the token
+ * goes to the sink.  Otherwise the key goes to k_res; the value goes to v_res
+ * (KIVI) or to the local window, whose oldest value moves to the value Q-buffer
+ * once the window is full (Kitty).  KVQ_ERR_CAPACITY if a destination buffer is
+ * full (call kvq_flush_group first). */
+int kvq_append_token(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k_new,
+                     const uint16_t *v_new, void *stream);
+
+/* Stage (3): quantize every full buffer.  A key buffer holding cap_k tokens is
+ * packed as cap_k/G new groups at the end of the packed keys and emptied; the same
+ * for the value buffer.  *flushed_k / *flushed_v (may be NULL) receive 1 if that
+ * buffer was flushed, else 0.  KVQ_ERR_CAPACITY if max_T would be exceeded. */
+int kvq_flush_group(const kvq_config *cfg, kvq_cache *cache, int *flushed_k,
+                    int *flushed_v, void *stream);
+
+/* Workspace bytes kvq_decode_attn needs for cfg (split-T partials, one counter per
+ * sequence and the status word).  The workspace must be zero-filled before its
+ * first use (kvq_workspace_init); every call leaves its counters at zero again. */
+size_t kvq_decode_attn_workspace_bytes(const kvq_config *cfg);
+
+/* Zero-fills a workspace (cudaMemsetAsync on stream). */
+int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Stage (2): decode attention for one query token per sequence,
+ *   out[b][h] = softmax_t( q[b][h] . K_t / sqrt(D) ) . V_t
+ * over every cached token (sink, packed, buffers), with packed keys and values
+ * dequantized (code*scale+min) on the fly in registers; query head h reads key /
+ * value head h / (H_q/H_kv).  q: device fp16 [B][H_q][D]; out: device fp16
+ * [B][H_q][D]; ws: device workspace of ws_bytes >= kvq_decode_attn_workspace_bytes.
+ * Accumulation is fp32 (fp16 tensor-core operands for the packed tiles).
+ * KVQ_ERR_INVALID_ARG if the cache is empty or its key and value lengths differ. */
+int kvq_decode_attn(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                    uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronizes `stream`, then returns in *dev_status the OR of the error bits the
+ * kernels wrote into the workspace status word and into cache->status (if cache is
+ * not NULL and its status pointer is set), and clears both.  KVQ_ERR_DEVICE if any
+ * bit was set, else KVQ_OK. */
+int kvq_read_status(const kvq_cache *cache, void *ws, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,113 @@
+"""Shared helpers for the GPU-vs-oracle parity tests."""
+import numpy as np
+
+import kvq_synth
+import oracle
+
+TOL_ABS = 2e-3
+TOL_REL = 2e-3
+
+
+def make_pair(wl, max_T, device):
+    import bit_kv_cache_gb300 as kvq
+    gpu = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
+                       n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=device)
+    ora = oracle.OracleCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
+                             n_boost=wl.n_boost, mode=wl.mode)
+    return gpu, ora
+
+
+def to_dev(a, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def prefill_both(gpu, ora, K, V, device):
+    gpu.prefill(to_dev(K, device), to_dev(V, device))
+    ora.prefill(K, V)
+
+
+def assert_lengths(gpu, ora):
+    got = gpu.lengths
+    want = dict(n_sink=ora.n_sink, T_k=ora.T_k, n_kres=ora.n_kres, T_v=ora.T_v,
+                n_vres=ora.n_vres, n_local=ora.n_local, local_head=ora.local_head)
+    assert got == want, (got, want)
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+def _u16(a):
+    return np.ascontiguousarray(a).view(np.uint16)
+
+
+def assert_state_equal(gpu, ora, units=None):
+    """Bit-exact comparison of every cache buffer (optionally for some (b, h) only)."""
+    assert_lengths(gpu, ora)
+    cfg = gpu.cfg
+    kitty = ora.kitty
+    kfpi = 16 if kitty else 32 // cfg.bits
+    vfpi = 32 // cfg.bits
+
+    def pick(a):
+        if units is None:
+            return a
+        return np.stack([a[b, h] for b, h in units])
+
+    T_k, T_v, G = ora.T_k, ora.T_v, cfg.G
+    kc = _np(gpu.view("k_codes")[:, :, : T_k // kfpi])
+    assert np.array_equal(pick(kc), pick(ora.k_codes)), "key codes differ"
+    km = _u16(_np(gpu.view("k_meta")[:, :, : T_k // G]))
+    assert np.array_equal(pick(km), pick(_u16(ora.k_meta))), "key scale/min differ"
+    vc = _np(gpu.view("v_codes")[:, :, : T_v // G])                 # [B,H,P,D/fpi,G]
+    vc = vc.transpose(0, 1, 2, 4, 3).reshape(cfg.B, cfg.H_kv, T_v, cfg.D // vfpi)
+    assert np.array_equal(pick(vc), pick(ora.v_codes)), "value codes differ"
+    vm = _u16(_np(gpu.view("v_meta")[:, :, :T_v]))
+    assert np.array_equal(pick(vm), pick(_u16(ora.v_meta))), "value scale/min differ"
+    if kitty:
+        bi = _np(gpu.view("k_bidx")[:, :, : T_k // G])
+        assert np.array_equal(pick(bi), pick(ora.k_bidx)), "boost index differs"
+        if cfg.n_boost:
+            hi = _np(gpu.view("k_hi")[:, :, : T_k // 16])
+            assert np.array_equal(pick(hi), pick(ora.k_hi)), "high plane differs"
+        # the whole ring: slots never written are zero on both sides
+        lo = _u16(_np(gpu.view("v_local")))
+        assert np.array_equal(pick(lo), pick(_u16(ora.v_local))), "local window differs"
+    for name, n in (("k_res", ora.n_kres), ("v_res", ora.n_vres), ("k_sink", ora.n_sink),
+                    ("v_sink", ora.n_sink)):
+        if n == 0:
+            continue
+        g = _u16(_np(gpu.view(name)[:, :, :n]))
+        o = _u16(getattr(ora, name)[:, :, :n])
+        assert np.array_equal(pick(g), pick(o)), name + " differs"
+
+
+def assert_close(out, ref, what="attention"):
+    """|out - ref| <= 2e-3 + 2e-3 |ref| for every element the oracle computed."""
+    out = np.asarray(out, np.float64)
+    mask = ~np.isnan(ref)
+    err = np.abs(out - ref)
+    bound = TOL_ABS + TOL_REL * np.abs(ref)
+    bad = mask & ~(err <= bound)
+    assert not bad.any(), "%s: %d elements out of tolerance, max err %.3g (ref %.3g)" % (
+        what, bad.sum(), err[mask].max(), np.abs(ref[mask]).max())
+    return float(err[mask].max()) if mask.any() else 0.0
+
+
+def run_steps(gpu, ora, wl, n_steps, device, check_every=1, units=None):
+    """n decode steps (append, attend, flush) on both sides; compares outputs."""
+    kn, vn = kvq_synth.decode_tokens(wl, n_steps)
+    qs = kvq_synth.queries(wl, n_steps)
+    worst = 0.0
+    for i in range(n_steps):
+        gpu.append_token(to_dev(kn[i], device), to_dev(vn[i], device))
+        ora.append(kn[i], vn[i])
+        if i % check_every == 0 or i == n_steps - 1:
+            out = _np(gpu.decode_attn(to_dev(qs[i], device)).float())
+            ref = ora.attend(qs[i], units=units)
+            worst = max(worst, assert_close(out, ref, what="step %d" % i))
+        fk, fv = gpu.flush_group()
+        ofk, ofv = ora.flush()
+        assert (fk, fv) == (ofk, ofv)
+    return worst
