@@ -4,7 +4,7 @@ Argument marshalling only: every step of quantization, packing, buffer updates
 and attention runs in the library's CUDA kernels, reached through the C ABI in
 ``include/kvq.h``.  PyTorch provides device memory and the current stream.  There
 is no CPU fallback: importing this package fails if ``libkvq.so`` is missing
-(build it with ``python -m bit_kv_cache_gb300.build``).
+(build it with ``python bit_kv_cache_gb300/build.py``).
 """
 from __future__ import annotations
 
@@ -50,7 +50,7 @@ class Cache(ctypes.Structure):
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
-        raise ImportError("libkvq.so not built (%s); run: python -m bit_kv_cache_gb300.build" % path)
+        raise ImportError("libkvq.so not built (%s); run: python bit_kv_cache_gb300/build.py" % path)
     L = ctypes.CDLL(path)
     P, I, I64, Sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     CP, KP = ctypes.POINTER(Config), ctypes.POINTER(Cache)

@@ -1,6 +1,6 @@
 """Builds libkvq.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-    python -m bit_kv_cache_gb300.build [--force]
+    python bit_kv_cache_gb300/build.py [--force]
 
 The translation units compile in parallel and link into
 ``bit_kv_cache_gb300/_build/libkvq.so``.  Nothing is installed outside the tree.

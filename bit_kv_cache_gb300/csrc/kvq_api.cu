@@ -48,7 +48,7 @@ int num_sms() {
 
 bool fast_supported(const kvq_config *c) {
     const int tok = c->bits == 2 ? 128 : 64;
-    if (c->D != 128 || c->H_q / c->H_kv > 8) return false;
+    if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4
     if (c->G % tok != 0 || gv_of(c) != c->D) return false;
     if (kitty(c) && (c->n_boost % 16 != 0 || c->n_boost > kMaxBoostFast)) return false;
     return true;

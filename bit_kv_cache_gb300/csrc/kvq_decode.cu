@@ -12,9 +12,11 @@
 // atomic ticket, no spin-wait) combines the partials with the log-sum-exp rule and
 // writes fp16 out.
 //
-// Tensor-core tiles (all g = H_q/H_kv query heads of a KV head at once, padded to
-// the mma N of 8 -- the BitDecoding query transformation, Sec. V-A):
-//   QK:  S[token][head] += Kcodes[token][ch] * q'[ch][head],  q' = q * scale_k * log2e/sqrt(D)
+// Tensor-core tiles (all g <= 4 query heads of a KV head at once in one mma N=8
+// tile -- the BitDecoding query transformation, Sec. V-A):
+//   QK:  S[token][col] += Kcodes[token][ch] * q'[ch][col],  q' = q * scale_k * log2e/sqrt(D)
+//        split in fp16 hi (column 2h) and lo (column 2h+1) parts of head h, so the
+//        folded query keeps 22 significant bits
 //        plus a per-head constant sum_ch q*min_k (keys are per-channel, so the
 //        scale folds into q and the min into a constant; one page = one group).
 //   PV:  O[ch][head] += Vcodes[ch][token] * p'[token][head],  p' = p * scale_v(token)
@@ -373,14 +375,22 @@ struct FastWarp {
 
     // Tiles [t0, t1) of sequence uu; writes the warp's partial [8][D+2] to `part`.
     // The mbarriers must be initialized (init_bars) and idle (all phases consumed).
+    //
+    // Query heads (g <= 4) and precision: q' = q * scale_k * log2e/sqrt(D) is split
+    // into fp16 hi + lo parts (22 significant bits); mma column 2h carries hi(q'_h),
+    // column 2h+1 carries lo(q'_h), so the lane that owns columns 2t, 2t+1 of the
+    // S tile adds them and owns head t of the softmax.  For PV the p' tile has one
+    // column per head (heads 4..7 zero), so the output lanes own heads 2t, 2t+1.
     __device__ void run(int uu, int64_t t0, int64_t t1, const uint16_t *q_w, float *part) {
         u = uu;
         const int gq = lane >> 2, t = lane & 3;
+        const int hq = gq >> 1;            // head whose q' part feeds mma column gq
+        const bool lo_col = (gq & 1) != 0;
         const float C = kLog2e * rsqrtf((float)T::D);
         const int64_t n = t1 - t0;
         for (int s = 0; s < kStages && s < n; s++) issue(t0 + s, s);
 
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, mn0 = 0.f, mn1 = 0.f;
+        float m = -INFINITY, l = 0.f, mn = 0.f;  // softmax state of head t
         float O[8][4];
 #pragma unroll
         for (int o = 0; o < 8; o++)
@@ -388,7 +398,11 @@ struct FastWarp {
             for (int e = 0; e < 4; e++) O[o][e] = 0.f;
         bool failed = false;
         unsigned char *pbuf = wbase + kStages * sbytes;
+        uint16_t *pb = reinterpret_cast<uint16_t *>(pbuf);
         uint8_t *invb = wbase + fast_qbuf_off<BITS>(KITTY, p.n_boost) + qbuf_bytes(T::D);  // [64]
+        for (int i = lane; i < 4 * T::TOK / 2; i += 32)  // p' rows of heads 4..7 stay zero
+            reinterpret_cast<uint32_t *>(pb + 4 * T::TOK)[i] = 0u;
+        __syncwarp();
 
         for (int64_t i = 0; i < n && !failed; i++) {
             const int s = (int)(i % kStages);
@@ -401,9 +415,14 @@ struct FastWarp {
             unsigned char *st = stage(s);
             const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
 
-            // ---- q' fragments for this page's key scales, and the min constant ----
-            uint32_t bq[8][2];
+            // ---- S = Kcodes . q'  (hi/lo columns), plus the per-head min constant ----
+            float acc[T::NJ][4];
+#pragma unroll
+            for (int j = 0; j < T::NJ; j++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) acc[j][e] = 0.f;
             float cst = 0.f;
+            const uint32_t kb = smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3);
 #pragma unroll
             for (int sl = 0; sl < 8; sl++) {
                 float qp[4];
@@ -411,32 +430,14 @@ struct FastWarp {
                 for (int cc = 0; cc < 4; cc++) {
                     const int ch = 16 * sl + 4 * cc + t;
                     const float2 sm = unpack_half2(km[ch]);
-                    const float qv = h2f(q_w[gq * T::D + ch]);
-                    qp[cc] = qv * sm.x * C;
+                    const float qv = h2f(q_w[hq * T::D + ch]);
+                    qp[cc] = split_part(qv * sm.x * C, lo_col);
                     cst = fmaf(qv, sm.y, cst);
                 }
-                bq[sl][0] = pack_half2(qp[0], qp[1]);
-                bq[sl][1] = pack_half2(qp[2], qp[3]);
-            }
-            cst += __shfl_xor_sync(0xffffffffu, cst, 1);
-            cst += __shfl_xor_sync(0xffffffffu, cst, 2);
-            cst *= C;
-            const float c0 = __shfl_sync(0xffffffffu, cst, (2 * t) * 4);
-            const float c1 = __shfl_sync(0xffffffffu, cst, (2 * t + 1) * 4);
-
-            // ---- S = codes . q' ----
-            float acc[T::NJ][4];
-#pragma unroll
-            for (int j = 0; j < T::NJ; j++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) acc[j][e] = 0.f;
-            const uint32_t kb = smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3);
-#pragma unroll
-            for (int sl = 0; sl < 8; sl++) {
                 uint32_t w[4], x[4], xs[4];
                 ldmatrix_x4(w, kb + 64 * sl);
                 split(w, x, xs);
-                mma_rowsets(acc, x, xs, bq[sl][0], bq[sl][1]);
+                mma_rowsets(acc, x, xs, pack_half2(qp[0], qp[1]), pack_half2(qp[2], qp[3]));
             }
             if (KITTY && p.n_boost > 0) {
                 // Boosted channels: S += hi . (4 q'), slots gathered through the index.
@@ -456,37 +457,35 @@ struct FastWarp {
                     for (int cc = 0; cc < 4; cc++) {
                         const int ch = invb[16 * s2 + 4 * cc + t] & (T::D - 1);
                         const float2 sm = unpack_half2(km[ch]);
-                        qp[cc] = 4.0f * h2f(q_w[gq * T::D + ch]) * sm.x * C;
+                        qp[cc] = split_part(4.0f * h2f(q_w[hq * T::D + ch]) * sm.x * C, lo_col);
                     }
                     uint32_t w[4], x[4], xs[4];
                     ldmatrix_x4(w, hb + 64 * s2);
                     split(w, x, xs);
                     mma_rowsets(acc, x, xs, pack_half2(qp[0], qp[1]), pack_half2(qp[2], qp[3]));
                 }
+                __syncwarp();
             }
+            cst += __shfl_xor_sync(0xffffffffu, cst, 1);
+            cst += __shfl_xor_sync(0xffffffffu, cst, 2);
+            const float ct = __shfl_sync(0xffffffffu, cst, (2 * t) * 4) * C;  // head t
 
-            // ---- online softmax over the tile ----
-            float z[T::NJ][4];
-            float tm0 = -INFINITY, tm1 = -INFINITY;
-            unscale_logits(acc, z, c0, c1);
+            // ---- online softmax over the tile (head t; rows g and g+8 of each row set) ----
+            float z[T::NJ][2];
+            unscale_logits(acc, z, ct);
+            float tm = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < T::NJ; j++) {
-                tm0 = fmaxf(tm0, fmaxf(z[j][0], z[j][2]));
-                tm1 = fmaxf(tm1, fmaxf(z[j][1], z[j][3]));
-            }
+            for (int j = 0; j < T::NJ; j++) tm = fmaxf(tm, fmaxf(z[j][0], z[j][1]));
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-                tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-            }
-            const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
-            const float a0 = exp2f(m0 - nm0), a1 = exp2f(m1 - nm1);
-            m0 = nm0;
-            m1 = nm1;
-            l0 *= a0;
-            l1 *= a1;
-            mn0 *= a0;
-            mn1 *= a1;
+            for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+            const float nm = fmaxf(m, tm);
+            const float a = exp2f(m - nm);
+            m = nm;
+            l *= a;
+            mn *= a;
+            // the output lanes own heads 2t, 2t+1: fetch their rescale factors
+            const float a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
+            const float a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
 #pragma unroll
             for (int o = 0; o < 8; o++) {
                 O[o][0] *= a0;
@@ -494,26 +493,18 @@ struct FastWarp {
                 O[o][1] *= a1;
                 O[o][3] *= a1;
             }
-            // value scale/min of the lane's tokens: 2-bit 16*gq..+15, 4-bit 8*gq..+7
             const uint32_t *vm = reinterpret_cast<const uint32_t *>(st + T::OFF_VM);
-            uint16_t *pb = reinterpret_cast<uint16_t *>(pbuf);
 #pragma unroll
             for (int j = 0; j < T::NJ; j++) {
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int tok = tok_of(j, e);
-                    const float pe = exp2f(z[j][e] - ((e & 1) ? m1 : m0));
+                for (int e = 0; e < 2; e++) {
+                    const int tok = tok_of(j, 2 * e);
+                    const float pe = exp2f(z[j][e] - m);
                     const float2 sm = unpack_half2(vm[tok]);
-                    if (e & 1) {
-                        l1 += pe;
-                        mn1 = fmaf(pe, sm.y, mn1);
-                    } else {
-                        l0 += pe;
-                        mn0 = fmaf(pe, sm.y, mn0);
-                    }
-                    const int head = 2 * t + (e & 1);
+                    l += pe;
+                    mn = fmaf(pe, sm.y, mn);
                     const int r = tok & 15;
-                    pb[head * T::TOK + (tok & ~15) + 4 * (r & 3) + (r >> 2)] =
+                    pb[t * T::TOK + (tok & ~15) + 4 * (r & 3) + (r >> 2)] =
                         __half_as_ushort(__float2half_rn(pe * sm.x));
                 }
             }
@@ -542,22 +533,26 @@ struct FastWarp {
                 if (pending & (1u << s)) mbar_wait(&bars[s], (phase >> s) & 1u, p.status);
             pending = 0;
         }
-        // ---- warp partial: heads 2t, 2t+1; channels of the O row sets ----
+        // ---- warp partial ----
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-            mn0 += __shfl_xor_sync(0xffffffffu, mn0, o);
-            mn1 += __shfl_xor_sync(0xffffffffu, mn1, o);
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+            mn += __shfl_xor_sync(0xffffffffu, mn, o);
         }
+        const float mn0 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t) & 3));
+        const float mn1 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t + 1) & 3));
         __syncwarp();
         store_o(O, part, mn0, mn1);
         if (gq == 0) {
-            part[(2 * t) * (T::D + 2) + T::D] = m0;
-            part[(2 * t) * (T::D + 2) + T::D + 1] = l0;
-            part[(2 * t + 1) * (T::D + 2) + T::D] = m1;
-            part[(2 * t + 1) * (T::D + 2) + T::D + 1] = l1;
+            part[t * (T::D + 2) + T::D] = m;
+            part[t * (T::D + 2) + T::D + 1] = l;
         }
+    }
+
+    // hi part (fp16-rounded) or lo part (remainder, rounded later to fp16) of x.
+    __device__ __forceinline__ static float split_part(float x, bool lo) {
+        const float hi = __half2float(__float2half_rn(x));
+        return lo ? x - hi : hi;
     }
 
     __device__ __forceinline__ static void mma_rowsets(float (&acc)[T::NJ][4], const uint32_t (&x)[4],
@@ -584,15 +579,14 @@ struct FastWarp {
 #undef KVQ_RS
     }
 
-    __device__ __forceinline__ static void unscale_logits(const float (&acc)[T::NJ][4], float (&z)[T::NJ][4],
-                                                          float c0, float c1) {
-#define KVQ_US(J)                                                   \
-    if (J < T::NJ) {                                                \
-        const float f = unscale<J>();                               \
-        z[J % T::NJ][0] = fmaf(acc[J % T::NJ][0], f, c0);           \
-        z[J % T::NJ][1] = fmaf(acc[J % T::NJ][1], f, c1);           \
-        z[J % T::NJ][2] = fmaf(acc[J % T::NJ][2], f, c0);           \
-        z[J % T::NJ][3] = fmaf(acc[J % T::NJ][3], f, c1);           \
+    // z[j][0] (row g) and z[j][1] (row g+8) of head t: hi + lo columns, unscaled, + constant.
+    __device__ __forceinline__ static void unscale_logits(const float (&acc)[T::NJ][4], float (&z)[T::NJ][2],
+                                                          float c) {
+#define KVQ_US(J)                                                                   \
+    if (J < T::NJ) {                                                                \
+        const float f = unscale<J>();                                               \
+        z[J % T::NJ][0] = fmaf(acc[J % T::NJ][0] + acc[J % T::NJ][1], f, c);        \
+        z[J % T::NJ][1] = fmaf(acc[J % T::NJ][2] + acc[J % T::NJ][3], f, c);        \
     }
         KVQ_US(0) KVQ_US(1) KVQ_US(2) KVQ_US(3) KVQ_US(4) KVQ_US(5) KVQ_US(6) KVQ_US(7)
 #undef KVQ_US
