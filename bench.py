@@ -4,8 +4,9 @@ Default workload: the Llama-3-8B-shaped GQA layer (B=4, H_q=32, H_kv=8, D=128,
 T=32768 packed 2-bit tokens, G=R=128).  One step = one decode step of one layer
 in the Kitty pipeline order: append the new token (kvq_append_token), attend
 (kvq_decode_attn), quantize the residual when it is full (kvq_flush_group).  The
-benchmark rotates through four independent layer caches (4 x 77.7 MB > 2 x L2),
-so no step finds its cache in L2.
+benchmark rotates through 16 layer caches (16 x 77.7 MB > 2 x L2), so no step
+finds its cache in L2.  Layer l's prefill is the seeded draw rolled by l*977
+tokens (same distribution, different pages); residual fills are staggered.
 
 value  = effective packed-KV bandwidth: algorithmic bytes of all timed steps
          (codes + fp16 scales/mins + fp16 sink/residual + q + out, summed per step
@@ -35,8 +36,7 @@ import numpy as np  # noqa: E402
 
 import kvq_synth  # noqa: E402
 
-N_LAYERS = 4
-METRIC = None
+N_LAYERS = 16
 
 
 def load_baseline():
@@ -93,47 +93,59 @@ def profiled_traffic(workload: str):
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling; summary() keeps the samples taken inside [t0, t1]."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.p = None
+        self.rows = []
 
-    def __enter__(self):
+    def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
-        return self
+        time.sleep(0.5)
 
-    def __exit__(self, *a):
-        self.rows = []
+    def stop(self):
         if self.p is None:
             return
-        time.sleep(0.15)
+        time.sleep(0.1)
         self.p.terminate()
         out, _ = self.p.communicate(timeout=10)
+        import datetime
         for line in out.strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                self.rows.append(parts)
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            self.rows.append([ts] + parts[1:])
 
-    def summary(self):
-        if not getattr(self, "rows", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+    def summary(self, t0: float, t1: float):
+        rows = [r for r in self.rows if t0 - 0.025 <= r[0] <= t1 + 0.025]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no sample in timed region"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[2]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[3]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
 def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
@@ -166,19 +178,34 @@ def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
     return per * steps / dt / 1e9, dt, steps, desc
 
 
-def reference_arm(args, wl, baseline, rank, world):
-    """--impl reference: the CPU oracle as it stands, on the host cores."""
+def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
+    """--impl reference: the CPU oracle as it stands, on the host cores.
+
+    One step = the oracle's decode attention over the first n tokens of one
+    (b, h_kv) sequence of the workload (all g query heads), with n chosen from a
+    calibration run so that warm-up + timed steps take about budget_s seconds."""
     if rank != 0:
         return 0
     K, W = args.steps, args.warmup
     import oracle
-    L0 = wl.T + 64
     sub = wl.replace(B=1, H_kv=1, H_q=wl.g)
-    Kx, Vx = kvq_synth.prefill_kv(sub, L0)
-    ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S, R=sub.R,
-                             n_boost=sub.n_boost, mode=sub.mode)
-    ora.prefill(Kx, Vx)
+
+    def make(n_tok):
+        Kx, Vx = kvq_synth.prefill_kv(sub, n_tok)
+        ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S,
+                                 R=sub.R, n_boost=sub.n_boost, mode=sub.mode)
+        ora.prefill(Kx, Vx)
+        return ora
+
+    L_full = wl.T + 64
+    probe = make(min(L_full, 8 * wl.G + 64))
     qs = kvq_synth.queries(sub, 4)
+    t0 = time.perf_counter()
+    probe.attend(qs[0])
+    per_tok = (time.perf_counter() - t0) / probe.L
+    n_tok = int(budget_s / (K + W) / max(per_tok, 1e-9))
+    n_tok = max(wl.G + 1, min(L_full, n_tok // wl.G * wl.G + 64))
+    ora = make(n_tok)
     lengths = dict(n_sink=ora.n_sink, T_k=ora.T_k, n_kres=ora.n_kres, T_v=ora.T_v,
                    n_vres=ora.n_vres, n_local=ora.n_local)
     per = decode_bytes(sub, lengths)
@@ -189,8 +216,9 @@ def reference_arm(args, wl, baseline, rank, world):
         ora.attend(qs[i % 4])
     dt = time.perf_counter() - t0
     val = per * K / dt / 1e9
-    sample = ("per step: oracle decode attention over 1 of %d (b,h_kv) sequences (%d tokens, "
-              "fp64, single thread)" % (wl.B * wl.H_kv, L0))
+    sample = ("per step: oracle decode attention (fp64, single thread) over the first %d of "
+              "%d tokens of 1 of %d (b,h_kv) sequences, %d query heads" % (
+                  ora.L, L_full, wl.B * wl.H_kv, wl.g))
     line = {"impl": "reference", "metric": baseline["metric"], "value": val, "unit": "GB/s",
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": dt / K * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -207,12 +235,13 @@ def reference_arm(args, wl, baseline, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="llama3_8b_gqa_b2", choices=sorted(kvq_synth.WORKLOADS))
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     baseline = load_baseline()
@@ -235,18 +264,25 @@ def main():
     __graft_entry__.build()
     import bit_kv_cache_gb300 as kvq
 
-    # ---- N_LAYERS independent layer caches, residual fills staggered ----
+    # ---- N_LAYERS layer caches: one seeded draw, rolled per layer; staggered fills ----
+    extra = (wl.S + wl.R) if wl.mode == "kitty" else 0
+    grow = -(-(args.steps + args.warmup + 256) // N_LAYERS)          # appends per layer
+    max_T = wl.T + wl.G * (grow // wl.G + 3)
+    L0 = wl.T + extra + wl.G - 1
+    K0, V0 = kvq_synth.prefill_kv(wl, L0, replica=rank)
+    K0 = torch.from_numpy(K0).to(dev)
+    V0 = torch.from_numpy(V0).to(dev)
     caches = []
-    L_fill = [64, 96, 0, 32]
     for li in range(N_LAYERS):
-        Kx, Vx = kvq_synth.prefill_kv(wl, wl.T + L_fill[li] + (wl.S if wl.mode == "kitty" else 0)
-                                      + (wl.R if wl.mode == "kitty" else 0), replica=li + 16 * rank)
+        fill = (li * wl.G) // N_LAYERS              # residual fill after prefill
+        Kl = torch.roll(K0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
+        Vl = torch.roll(V0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
         c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                         n_boost=wl.n_boost, mode=wl.mode, max_T=wl.T + 8 * wl.G, device=dev)
-        c.prefill(torch.from_numpy(Kx).to(dev), torch.from_numpy(Vx).to(dev))
-        del Kx, Vx
+                         n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=dev)
+        c.prefill(Kl, Vl)
         caches.append(c)
-    n_tok = args.steps + args.warmup + 8
+        del Kl, Vl
+    del K0, V0
     kn, vn = kvq_synth.decode_tokens(wl, 64, replica=rank)
     qs = kvq_synth.queries(wl, 64, replica=rank)
     kn_d = torch.from_numpy(kn).to(dev)
@@ -279,15 +315,19 @@ def main():
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total_bytes = 0
     flushes = 0
-    with Clocks(local) as clk:
-        torch.cuda.synchronize()
-        t_start.record(stream)
-        for i in range(K):
-            b, f = step(args.warmup + i, evs[i])
-            total_bytes += b
-            flushes += f
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    clk = Clocks(local)
+    clk.start()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        b, f = step(args.warmup + i, evs[i])
+        total_bytes += b
+        flushes += f
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk.stop()
     ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(bb) for a, bb in evs]
     st = sum(c.read_status() for c in caches)
@@ -311,7 +351,7 @@ def main():
     kn_s = torch.empty_like(kn_d[0])
     vn_s = torch.empty_like(vn_d[0])
     q_s = torch.empty_like(q_d[0])
-    Ke = min(K, 200)
+    Ke = max(1, min(K, args.e2e_steps))
     e_bytes = 0
     for i in range(Ke + 3):
         if i == 3:
@@ -354,15 +394,15 @@ def main():
                    "T": wl.T, "G": wl.G, "R": wl.R, "bits": wl.bits, "S": wl.S,
                    "n_boost": wl.n_boost, "mode": wl.mode,
                    "step": "append_token + decode_attn + flush_group (when full), one layer",
-                   "l2": "%d layer caches rotated (%.0f MB each, > 2 x L2)" % (
-                       N_LAYERS, dec_bytes / 1e6),
+                   "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (
+                       N_LAYERS, dec_bytes / 1e6, N_LAYERS * dec_bytes / 1e9),
                    "parallelism": "independent replicas per GPU" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel", "us_per_launch": dec_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": dec_bytes, "traffic": traffic},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(w0, w1),
         "e2e": {"value": e_bytes / e_dt / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_step": e_dt / Ke * 1e6},
     }

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu"]
-HEADERS = ["kvq_device.cuh", "kvq_internal.h"]
+HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode_fast.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -39,10 +39,14 @@ bool key_slices_ok(const kvq_config *c) {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+// SM count of the current device (cached per device; 148 if no device is usable).
 int num_sms() {
+    static int cache[64] = {0};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
     return n;
 }
 
@@ -50,32 +54,50 @@ bool fast_supported(const kvq_config *c) {
     const int tok = c->bits == 2 ? 128 : 64;
     if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4
     if (c->G % tok != 0 || gv_of(c) != c->D) return false;
+    if (c->G & (c->G - 1)) return false;  // pages of a power-of-two size (shift arithmetic)
     if (kitty(c) && (c->n_boost % 16 != 0 || c->n_boost > kMaxBoostFast)) return false;
     return true;
 }
 
-// Partial-slot bound per sequence for a workspace: CTAs of one wave spread over the
-// sequences, plus the two CTAs a range can straddle, for each of the two pools.
-int64_t slot_bound(const kvq_config *c) { return cdiv(4 * (int64_t)num_sms(), units(c)) + 6; }
+// Partial-slot bound per sequence: the CTAs of the pools spread over the sequences,
+// plus the CTAs a range can straddle at both ends, for each pool.
+int64_t slot_bound(const kvq_config *c) { return cdiv(4 * (int64_t)num_sms(), units(c)) + 8; }
+
+// Upper bound of the CTAs of one pool: one wave, or the minimum that keeps every warp
+// range within two sequences (about U / warps-per-CTA).
+int64_t max_pool_ctas(const kvq_config *c) { return std::max<int64_t>(num_sms(), cdiv(units(c), 6)); }
 
 struct WsLayout {
     size_t status, tickets, scratch, partials, total;
 };
 
-// Upper bound of fast CTAs in one launch: at most nsm, or the minimum that keeps
-// every warp range within two sequences (ceil(U / kWarps) when n_fast >= 1).
-int64_t max_fast_ctas(const kvq_config *c) { return std::max<int64_t>(num_sms(), cdiv(units(c), kWarps)); }
-
 WsLayout ws_layout(const kvq_config *c) {
     WsLayout w;
     const int64_t U = units(c), g = c->H_q / c->H_kv;
-    const int64_t max_cf = max_fast_ctas(c);
     w.status = 0;
     w.tickets = 256;
     w.scratch = w.tickets + (size_t)cdiv(U * 4, 256) * 256;
-    w.partials = w.scratch + (size_t)max_cf * kWarps * 8 * (c->D + 2) * 4;
-    w.total = w.partials + (size_t)U * slot_bound(c) * g * (c->D + 2) * 4;
+    w.partials = w.scratch + (size_t)2 * max_pool_ctas(c) * kMaxWarps * 8 * (c->D + 4) * 4;
+    w.total = w.partials + (size_t)U * slot_bound(c) * g * (c->D + 4) * 4;
     return w;
+}
+
+// Warps per pool CTA count for N items (n per sequence): every warp owns >= 1 item
+// (so all CTAs between a sequence's first and last hold some of its items) and no
+// warp range exceeds n + 1 items (so it touches at most two sequences).
+int64_t clamp_pool(int64_t want, int64_t N, int64_t n, int wpc) {
+    if (N == 0) return 0;
+    const int64_t lo = std::max<int64_t>(1, cdiv(N, (int64_t)wpc * (n + 1)));
+    const int64_t hi = std::max<int64_t>(1, N / wpc);
+    return std::min(hi, std::max(lo, want));
+}
+
+// CTAs of a pool (C CTAs, wpc warps each, N items, n per sequence) holding items of u.
+int64_t pool_ctas_host(int64_t C, int wpc, int64_t N, int64_t n, int64_t u) {
+    if (n == 0 || C == 0) return 0;
+    const int64_t W = C * wpc;
+    auto warp_of = [&](int64_t x) { return std::min(W - 1, ((x + 1) * W - 1) / N); };
+    return warp_of((u + 1) * n - 1) / wpc - warp_of(u * n) / wpc + 1;
 }
 
 int check_cache_ptrs(const kvq_config *c, const kvq_cache *k) {
@@ -387,57 +409,141 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     if (!ws || !aligned16(ws) || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE;
 
     const int U = (int)units(c), g = c->H_q / c->H_kv, nsm = num_sms();
-    const bool fast = fast_supported(c);
     const int tok = c->bits == 2 ? 128 : 64;
-    const int64_t n_fast = fast ? std::min(k->T_k, k->T_v) / tok : 0;
-    const int64_t n_gen = L - n_fast * tok;
-    const int64_t N_f = (int64_t)U * n_fast;
-
-    // Schedule: split the GPU between fast CTAs (tiles) and generic CTAs (chunks of
-    // the remaining tokens) so that the longest warp is as short as possible.
-    // Cost unit: one fast tile; a generic token costs about kGen of a tile.
-    const double kGen = fast ? 5.0 / tok : 1.0 / 32.0;
-    int best_cf = 0, best_cg = 0, best_ngc = 0;
-    int64_t best_chunk = 0;
-    double best = 1e300;
-    const int64_t gmax = std::max<int64_t>(32, cdiv(n_gen, 32) * 32);
-    int64_t cands[40];
-    int nc = 0;
-    for (int64_t ch = 32; ch <= 256 && ch < gmax; ch += 32) cands[nc++] = ch;
-    for (int64_t ch = 512; ch < gmax && nc < 39; ch *= 2) cands[nc++] = ch;
-    cands[nc++] = gmax;  // the whole generic part of a sequence in one chunk
-    for (int ci = 0; ci < nc; ci++) {
-        const int64_t chunk = cands[ci];
-        const int64_t ngc = n_gen > 0 ? cdiv(n_gen, chunk) : 0;
-        const int64_t cg = cdiv((int64_t)U * ngc, kWarps);
-        if (cg > 4 * (int64_t)nsm && chunk < gmax) continue;  // too many generic CTAs
-        // Fast CTAs: every warp must own >= 1 tile (W_f <= N_f, so the CTAs between the
-        // first and last CTA of a sequence all hold some of its tiles) and no warp range
-        // may exceed n_fast + 1 tiles (so a warp touches at most two sequences).
-        int64_t cf = 0;
-        if (N_f > 0) {
-            const int64_t lo = std::max<int64_t>(1, cdiv(N_f, (int64_t)kWarps * (n_fast + 1)));
-            const int64_t hi = std::max<int64_t>(1, N_f / kWarps);
-            cf = std::min(hi, std::max(lo, (int64_t)nsm - cg));
-        }
-        const double tf = N_f > 0 ? (double)cdiv(N_f, cf * kWarps) : 0.0;
-        const double tg = ngc > 0 ? (double)std::min(chunk, n_gen) * kGen : 0.0;
-        const int64_t waves = cdiv(cf + cg, nsm);
-        const double est = (double)waves * std::max(tf, tg) + 0.02 * (double)(cf + cg) / U;
-        if (est < best) {
-            best = est;
-            best_cf = (int)cf;
-            best_cg = (int)cg;
-            best_ngc = (int)ngc;
-            best_chunk = chunk;
-        }
-    }
+    // The tile paths cover: D = 128, g <= 4, pages of whole tiles, one value group per
+    // token, packed values never ahead of packed keys, mixed key blocks only at 2 bits.
+    bool fast = fast_supported(c) && k->T_v <= k->T_k && k->T_v % tok == 0 &&
+                (k->T_k == k->T_v || (kitty(c) && (k->T_k - k->T_v) % 16 == 0));
+    const int wpc = decode_warps_per_cta(c->bits, kitty(c), kitty(c) ? c->n_boost : 0, fast);
 
     DecodeParams p;
     memset(&p, 0, sizeof(p));
+    p.U = U;
+    p.wpc = wpc;
+    // The schedule depends only on these numbers; decode steps repeat them for 16
+    // tokens at a time, so the last one is kept.
+    struct SchedKey {
+        int64_t U, wpc, nsm, fast, T_k, T_v, n_sink, n_kres, L, tok;
+        bool operator==(const SchedKey &o) const { return memcmp(this, &o, sizeof(*this)) == 0; }
+    };
+    struct SchedVal {
+        int C_f, C_m, C_g, n_gc, max_slots;
+        int64_t n_fast, n_mini, N_f, N_m, n_gen, gen_chunk;
+    };
+    static thread_local SchedKey last_key;
+    static thread_local SchedVal last_val;
+    static thread_local bool have_last = false;
+    SchedKey key;
+    memset(&key, 0, sizeof(key));
+    key.U = U;
+    key.wpc = wpc;
+    key.nsm = nsm;
+    key.fast = fast;
+    key.T_k = k->T_k;
+    key.T_v = k->T_v;
+    key.n_sink = k->n_sink;
+    key.n_kres = k->n_kres;
+    key.L = L;
+    key.tok = tok;
+    if (have_last && key == last_key) {
+        const SchedVal &v = last_val;
+        p.C_f = v.C_f;
+        p.C_m = v.C_m;
+        p.C_g = v.C_g;
+        p.n_gc = v.n_gc;
+        p.max_slots = v.max_slots;
+        p.n_fast = v.n_fast;
+        p.n_mini = v.n_mini;
+        p.N_f = v.N_f;
+        p.N_m = v.N_m;
+        p.n_gen = v.n_gen;
+        p.gen_chunk = v.gen_chunk;
+    } else if (fast) {
+        // fast tiles: keys and values packed; mini tiles: the rest in 16-token tiles
+        p.n_fast = k->T_v / tok;
+        p.n_mini = cdiv(k->n_sink, 16) + (k->T_k - p.n_fast * tok) / 16 + cdiv(k->n_kres, 16);
+        p.N_f = (int64_t)U * p.n_fast;
+        p.N_m = (int64_t)U * p.n_mini;
+        // cost of a mini tile relative to a fast tile (bytes of 16 fp16 tokens vs a packed
+        // tile, lighter arithmetic)
+        const double kMini = 0.6;
+        double best = 1e300;
+        int64_t bf = 0, bm = 0;
+        const int64_t cm_max = p.N_m > 0 ? nsm : 0;
+        for (int64_t cm0 = (p.N_m > 0 ? 1 : 0); cm0 <= cm_max; cm0++) {
+            const int64_t cm = clamp_pool(cm0, p.N_m, p.n_mini, wpc);
+            const int64_t cf = clamp_pool(std::max<int64_t>(1, nsm - cm), p.N_f, p.n_fast, wpc);
+            const double tf = cf ? (double)cdiv(p.N_f, cf * wpc) : 0.0;
+            const double tm = cm ? (double)cdiv(p.N_m, cm * wpc) * kMini : 0.0;
+            const double est = (double)cdiv(cf + cm, nsm) * std::max(tf, tm) + 1e-3 * (double)(cf + cm);
+            if (est < best) {
+                best = est;
+                bf = cf;
+                bm = cm;
+            }
+            if (p.N_f == 0 && cm0 > 0 && cm >= clamp_pool(nsm, p.N_m, p.n_mini, wpc)) break;
+        }
+        p.C_f = (int)bf;
+        p.C_m = (int)bm;
+    } else {
+        // generic chunks of the whole sequence (CUDA cores)
+        p.n_gen = L;
+        const double kGen = 1.0;
+        double best = 1e300;
+        const int64_t gmax = std::max<int64_t>(32, cdiv(L, 32) * 32);
+        int64_t cands[40];
+        int nc = 0;
+        for (int64_t ch = 32; ch <= 256 && ch < gmax; ch += 32) cands[nc++] = ch;
+        for (int64_t ch = 512; ch < gmax && nc < 39; ch *= 2) cands[nc++] = ch;
+        cands[nc++] = gmax;
+        for (int ci = 0; ci < nc; ci++) {
+            const int64_t chunk = cands[ci];
+            const int64_t ngc = cdiv(L, chunk);
+            const int64_t cg = cdiv((int64_t)U * ngc, wpc);
+            if (cg > 4 * (int64_t)nsm && chunk < gmax) continue;
+            const double est = (double)cdiv(cg, nsm) * (double)std::min(chunk, L) * kGen + 1e-3 * cg;
+            if (est < best) {
+                best = est;
+                p.C_g = (int)cg;
+                p.n_gc = (int)ngc;
+                p.gen_chunk = chunk;
+            }
+        }
+    }
+    if (!(have_last && key == last_key)) {
+        // slots per sequence
+        int64_t max_slots = 0;
+        for (int64_t u = 0; u < U; u++) {
+            int64_t sl = pool_ctas_host(p.C_f, wpc, p.N_f, p.n_fast, u) +
+                         pool_ctas_host(p.C_m, wpc, p.N_m, p.n_mini, u);
+            if (p.n_gc > 0) sl += ((u + 1) * p.n_gc - 1) / wpc - (u * p.n_gc) / wpc + 1;
+            max_slots = std::max(max_slots, sl);
+        }
+        // merge / combine weight tables must fit the kernel's free shared memory
+        const int64_t tab = decode_table_floats(c->bits, kitty(c), kitty(c) ? c->n_boost : 0, c->D, fast);
+        const int64_t nu_max = std::min<int64_t>(24, U);
+        const bool tab_ok = 24 * g * (2 * wpc + 2) <= tab && nu_max * g * max_slots <= tab;
+        if (max_slots < 1 || max_slots > slot_bound(c) || p.C_f > max_pool_ctas(c) || p.C_m > max_pool_ctas(c) ||
+            p.C_g > 4 * (int64_t)max_pool_ctas(c) || !tab_ok)
+            return KVQ_ERR_UNSUPPORTED;
+        p.max_slots = (int)max_slots;
+        last_key = key;
+        last_val = SchedVal{p.C_f, p.C_m, p.C_g, p.n_gc, p.max_slots, p.n_fast,
+                            p.n_mini, p.N_f, p.N_m, p.n_gen, p.gen_chunk};
+        have_last = true;
+    }
+
     p.B = c->B;
     p.H_kv = c->H_kv;
     p.g = g;
+    if (fast) {
+        int sh = 0;
+        while ((tok << sh) < c->G) sh++;
+        p.tpp_shift = sh;
+        sh = 0;
+        while ((1 << sh) < c->G) sh++;
+        p.g_shift = sh;
+    }
     p.D = c->D;
     p.G = c->G;
     p.bits = c->bits;
@@ -475,27 +581,6 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.tickets = reinterpret_cast<int32_t *>(w + wl.tickets);
     p.scratch = reinterpret_cast<float *>(w + wl.scratch);
     p.partials = reinterpret_cast<float *>(w + wl.partials);
-    p.U = U;
-    p.C_f = best_cf;
-    p.C_g = best_cg;
-    p.n_gc = best_ngc;
-    p.n_fast = n_fast;
-    p.N_f = N_f;
-    p.n_gen = n_gen;
-    p.gen_chunk = best_chunk;
-    // slots per sequence: fast CTAs touching it + generic CTAs touching it
-    int64_t max_slots = 0;
-    const int64_t Wf = (int64_t)best_cf * kWarps;
-    auto warp_of = [&](int64_t x) { return std::min(Wf - 1, ((x + 1) * Wf - 1) / N_f); };
-    for (int64_t u = 0; u < U; u++) {
-        int64_t s = 0;
-        if (n_fast > 0) s += warp_of((u + 1) * n_fast - 1) / kWarps - warp_of(u * n_fast) / kWarps + 1;
-        if (best_ngc > 0) s += ((u + 1) * best_ngc - 1) / kWarps - (u * best_ngc) / kWarps + 1;
-        max_slots = std::max(max_slots, s);
-    }
-    if (best == 1e300 || max_slots > slot_bound(c) || (int64_t)best_cf > max_fast_ctas(c))
-        return KVQ_ERR_UNSUPPORTED;
-    p.max_slots = (int)max_slots;
     return status_of(launch_decode(p, fast, (cudaStream_t)stream));
 }
 

@@ -40,63 +40,17 @@
 #include "kvq_internal.h"
 
 namespace kvq {
+__host__ __device__ __forceinline__ int64_t kvq_min64(int64_t a, int64_t b) { return a < b ? a : b; }
+}  // namespace kvq
 
-constexpr float kLog2e = 1.4426950408889634f;
+#include "kvq_decode_fast.cuh"
+
+namespace kvq {
+
 constexpr int KVQ_DEV_BAD_STATE_BIT = 2;
 
-__host__ __device__ __forceinline__ int64_t kvq_min64(int64_t a, int64_t b) { return a < b ? a : b; }
-
-template <int BITS>
-struct Tile {
-    static constexpr int D = 128;
-    static constexpr int FPI = 32 / BITS;
-    static constexpr int TOK = BITS == 2 ? 128 : 64;     // tokens per tile (8 words of keys)
-    static constexpr int K_STRIDE = D * 4 + 16;          // padded key row (conflict-free ldmatrix)
-    static constexpr int V_ROWS = D / FPI;               // channel blocks: 8 or 16
-    static constexpr int V_STRIDE = TOK * 4 + 16;
-    static constexpr int NJ = FPI / 2;                   // row sets per word: 8 or 4
-    static constexpr int NSET = V_ROWS / 8;              // 1 or 2
-    static constexpr int TSLABS = TOK / 16;              // 16-token slabs for PV
-    static constexpr int JDIRECT = BITS == 2 ? 5 : 2;    // row sets readable without a shift
-    static constexpr int SH = BITS == 2 ? 6 : 8;         // pre-shift for the others
-    static constexpr uint32_t MASK0 = BITS == 2 ? 0x00030003u : 0x000F000Fu;
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + 8 * K_STRIDE;
-    static constexpr int OFF_KM = OFF_V + V_ROWS * V_STRIDE;
-    static constexpr int OFF_VM = OFF_KM + D * 4;
-    static constexpr int OFF_HI = OFF_VM + TOK * 4;
-    static constexpr int PBUF = 8 * TOK * 2;
-};
-
-__host__ __device__ inline int hi_stride(int nb) { return nb * 4 + 16; }
-
-template <int BITS>
-__host__ __device__ inline int stage_bytes(bool kitty, int nb) {
-    int s = Tile<BITS>::OFF_HI + (kitty ? 8 * hi_stride(nb) + 128 : 0);
-    return (s + 127) & ~127;
-}
-
-__host__ __device__ inline int part_bytes(int D) { return 8 * (D + 2) * 4; }
-__host__ __device__ inline int qbuf_bytes(int D) { return 8 * D * 2; }
-
-// Per-warp shared memory, fast kernel:
-//   [stage 0 .. kStages-1][p' buffer][q buffer fp16 [8][D]][slot index 64 B][mbarriers]
-// The warp's final partial is written over its stage 0 after its last tile.
-template <int BITS>
-__host__ __device__ inline int fast_warp_bytes(bool kitty, int nb) {
-    int s = kStages * stage_bytes<BITS>(kitty, nb) + Tile<BITS>::PBUF + qbuf_bytes(Tile<BITS>::D) + 64 +
-            8 * kStages;
-    return (s + 127) & ~127;
-}
-template <int BITS>
-__host__ __device__ inline int fast_qbuf_off(bool kitty, int nb) {
-    return kStages * stage_bytes<BITS>(kitty, nb) + Tile<BITS>::PBUF;
-}
-
-// Per-warp shared memory, generic-only kernel: [partial][q buffer].
-__host__ __device__ inline int gen_warp_bytes(int D) {
-    return (part_bytes(D) + qbuf_bytes(D) + 127) & ~127;
-}
+// Per-warp shared memory of the generic-only kernel: [partial][q buffer fp16 [8][D]].
+__host__ __device__ inline int gen_warp_bytes(int D) { return (part_bytes(D) + 8 * D * 2 + 127) & ~127; }
 
 // ---------------------------------------------------------------------------------
 // Generic path: one token per lane for QK, one token per step for PV (CUDA cores,
@@ -265,385 +219,54 @@ __device__ void generic_store(const DecodeParams &p, const GenState<DPL> &st, fl
 #pragma unroll
         for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-        for (int i = 0; i < DPL; i++) part[h * (D + 2) + lane * DPL + i] = st.o[h][i];
+        for (int i = 0; i < DPL; i++) part[h * prow(D) + lane * DPL + i] = st.o[h][i];
         if (lane == 0) {
-            part[h * (D + 2) + D] = st.m[h];
-            part[h * (D + 2) + D + 1] = l;
+            part[h * prow(D) + D] = st.m[h];
+            part[h * prow(D) + D + 1] = l;
         }
     }
 }
 
 // ---------------------------------------------------------------------------------
-// Fast path: packed tiles on the tensor cores.
+// Schedule arithmetic (closed forms, identical on host and device).
+// A pool of W = wpc * C warps cuts the sequence-major list of N = U * n items into
+// ranges [a_k, a_{k+1}), a_k = floor(k * N / W).
 // ---------------------------------------------------------------------------------
-template <int BITS, bool KITTY>
-struct FastWarp {
-    using T = Tile<BITS>;
-    const DecodeParams &p;
-    unsigned char *wbase;
-    int u, lane;
-    int sbytes;
-    uint64_t *bars;
-    uint32_t phase = 0;    // bit s: parity of the next completion of stage s
-    uint32_t pending = 0;  // bit s: stage s has copies in flight
-
-    __device__ void init_bars() {
-        if (lane == 0) {
-            for (int s = 0; s < kStages; s++) mbar_init(&bars[s], 1);
-            fence_barrier_init();
-        }
-        __syncwarp();
-    }
-
-    __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
-        : p(pp), wbase(wb), u(0), lane(threadIdx.x & 31) {
-        sbytes = stage_bytes<BITS>(KITTY, p.n_boost);
-        bars = reinterpret_cast<uint64_t *>(wbase + fast_qbuf_off<BITS>(KITTY, p.n_boost) + qbuf_bytes(T::D) + 64);
-    }
-
-    __device__ unsigned char *stage(int s) const { return wbase + s * sbytes; }
-
-    __device__ uint32_t tile_bytes() const {
-        uint32_t b = 8 * T::D * 4 + T::V_ROWS * T::TOK * 4 + T::D * 4 + T::TOK * 4;
-        if (KITTY) b += 8 * p.n_boost * 4 + T::D;
-        return b;
-    }
-
-    // Enqueue the bulk copies of tile ti into stage s (whole warp).
-    __device__ void issue(int64_t ti, int s) {
-        pending |= 1u << s;
-        unsigned char *st = stage(s);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], tile_bytes());
-        __syncwarp();
-        const int64_t tok0 = ti * T::TOK;                  // packed-token index
-        const int64_t page = tok0 / p.G, off = tok0 % p.G;
-        const int nk = 8, nv = T::V_ROWS;
-        const int i = lane;
-        if (i < nk) {
-            const int32_t *src = p.k_codes + ((size_t)u * (p.max_T / T::FPI) + ti * 8 + i) * T::D;
-            bulk_g2s(st + T::OFF_K + i * T::K_STRIDE, src, T::D * 4, &bars[s]);
-        } else if (i < nk + nv) {
-            const int m = i - nk;
-            const int32_t *src = p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * T::V_ROWS + m) * p.G + off;
-            bulk_g2s(st + T::OFF_V + m * T::V_STRIDE, src, T::TOK * 4, &bars[s]);
-        } else if (i == nk + nv) {
-            const uint16_t *src = p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2;
-            bulk_g2s(st + T::OFF_KM, src, T::D * 4, &bars[s]);
-        } else if (i == nk + nv + 1) {
-            const uint16_t *src = p.v_meta + ((size_t)u * p.max_T + tok0) * 2;
-            bulk_g2s(st + T::OFF_VM, src, T::TOK * 4, &bars[s]);
-        } else if (KITTY && i < nk + nv + 2 + 8) {
-            const int r = i - (nk + nv + 2);
-            const int32_t *src = p.k_hi + ((size_t)u * (p.max_T / 16) + ti * 8 + r) * p.n_boost;
-            bulk_g2s(st + T::OFF_HI + r * hi_stride(p.n_boost), src, p.n_boost * 4, &bars[s]);
-        } else if (KITTY && i == nk + nv + 2 + 8) {
-            const uint8_t *src = p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * T::D;
-            bulk_g2s(st + T::OFF_HI + 8 * hi_stride(p.n_boost), src, T::D, &bars[s]);
-        }
-    }
-
-    // The 4 A-operand registers of row set j from the 4 ldmatrix words (see header).
-    template <int J>
-    __device__ __forceinline__ static void frag(const uint32_t (&x)[4], const uint32_t (&xs)[4],
-                                                uint32_t (&a)[4]) {
-        constexpr int JJ = J < T::JDIRECT ? J : J - (T::SH / BITS);
-        constexpr uint32_t M = T::MASK0 << (BITS * JJ);
-#pragma unroll
-        for (int r = 0; r < 4; r++) a[r] = (J < T::JDIRECT ? x[r] : xs[r]) & M;
-    }
-    template <int J>
-    __device__ __forceinline__ static float unscale() {
-        constexpr int JJ = J < T::JDIRECT ? J : J - (T::SH / BITS);
-        return (float)(1u << (24 - BITS * JJ));
-    }
-
-    __device__ __forceinline__ static void split(const uint32_t (&w)[4], uint32_t (&x)[4], uint32_t (&xs)[4]) {
-        x[0] = prmt(w[0], w[1], 0x5410);  // rows g   (low halves),  k = 2t, 2t+1
-        x[1] = prmt(w[0], w[1], 0x7632);  // rows g+8 (high halves)
-        x[2] = prmt(w[2], w[3], 0x5410);  // rows g,   k = 2t+8, 2t+9
-        x[3] = prmt(w[2], w[3], 0x7632);
-#pragma unroll
-        for (int r = 0; r < 4; r++) xs[r] = x[r] >> T::SH;
-    }
-
-    // Token (within tile) of accumulator element e of row set j for this lane.
-    __device__ __forceinline__ int tok_of(int j, int e) const {
-        const int gq = lane >> 2;
-        if (BITS == 2) return 16 * gq + j + ((e >> 1) ? 8 : 0);
-        return 8 * gq + j + ((e >> 1) ? 4 : 0);
-    }
-
-    // Tiles [t0, t1) of sequence uu; writes the warp's partial [8][D+2] to `part`.
-    // The mbarriers must be initialized (init_bars) and idle (all phases consumed).
-    //
-    // Query heads (g <= 4) and precision: q' = q * scale_k * log2e/sqrt(D) is split
-    // into fp16 hi + lo parts (22 significant bits); mma column 2h carries hi(q'_h),
-    // column 2h+1 carries lo(q'_h), so the lane that owns columns 2t, 2t+1 of the
-    // S tile adds them and owns head t of the softmax.  For PV the p' tile has one
-    // column per head (heads 4..7 zero), so the output lanes own heads 2t, 2t+1.
-    __device__ void run(int uu, int64_t t0, int64_t t1, const uint16_t *q_w, float *part) {
-        u = uu;
-        const int gq = lane >> 2, t = lane & 3;
-        const int hq = gq >> 1;            // head whose q' part feeds mma column gq
-        const bool lo_col = (gq & 1) != 0;
-        const float C = kLog2e * rsqrtf((float)T::D);
-        const int64_t n = t1 - t0;
-        for (int s = 0; s < kStages && s < n; s++) issue(t0 + s, s);
-
-        float m = -INFINITY, l = 0.f, mn = 0.f;  // softmax state of head t
-        float O[8][4];
-#pragma unroll
-        for (int o = 0; o < 8; o++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) O[o][e] = 0.f;
-        bool failed = false;
-        unsigned char *pbuf = wbase + kStages * sbytes;
-        uint16_t *pb = reinterpret_cast<uint16_t *>(pbuf);
-        uint8_t *invb = wbase + fast_qbuf_off<BITS>(KITTY, p.n_boost) + qbuf_bytes(T::D);  // [64]
-        for (int i = lane; i < 4 * T::TOK / 2; i += 32)  // p' rows of heads 4..7 stay zero
-            reinterpret_cast<uint32_t *>(pb + 4 * T::TOK)[i] = 0u;
-        __syncwarp();
-
-        for (int64_t i = 0; i < n && !failed; i++) {
-            const int s = (int)(i % kStages);
-            if (!mbar_wait(&bars[s], (phase >> s) & 1u, p.status)) {
-                failed = true;
-                break;
-            }
-            phase ^= 1u << s;
-            pending &= ~(1u << s);
-            unsigned char *st = stage(s);
-            const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
-
-            // ---- S = Kcodes . q'  (hi/lo columns), plus the per-head min constant ----
-            float acc[T::NJ][4];
-#pragma unroll
-            for (int j = 0; j < T::NJ; j++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) acc[j][e] = 0.f;
-            float cst = 0.f;
-            const uint32_t kb = smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3);
-#pragma unroll
-            for (int sl = 0; sl < 8; sl++) {
-                float qp[4];
-#pragma unroll
-                for (int cc = 0; cc < 4; cc++) {
-                    const int ch = 16 * sl + 4 * cc + t;
-                    const float2 sm = unpack_half2(km[ch]);
-                    const float qv = h2f(q_w[hq * T::D + ch]);
-                    qp[cc] = split_part(qv * sm.x * C, lo_col);
-                    cst = fmaf(qv, sm.y, cst);
-                }
-                uint32_t w[4], x[4], xs[4];
-                ldmatrix_x4(w, kb + 64 * sl);
-                split(w, x, xs);
-                mma_rowsets(acc, x, xs, pack_half2(qp[0], qp[1]), pack_half2(qp[2], qp[3]));
-            }
-            if (KITTY && p.n_boost > 0) {
-                // Boosted channels: S += hi . (4 q'), slots gathered through the index.
-                const uint8_t *bi = st + T::OFF_HI + 8 * hi_stride(p.n_boost);
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const int ch = lane * 4 + r;
-                    const int sl = bi[ch];
-                    if (sl < p.n_boost) invb[sl] = (uint8_t)ch;
-                }
-                __syncwarp();
-                const int nsl = p.n_boost / 16;
-                const uint32_t hb = smem_u32(st + T::OFF_HI) + (lane & 7) * hi_stride(p.n_boost) + 16 * (lane >> 3);
-                for (int s2 = 0; s2 < nsl; s2++) {
-                    float qp[4];
-#pragma unroll
-                    for (int cc = 0; cc < 4; cc++) {
-                        const int ch = invb[16 * s2 + 4 * cc + t] & (T::D - 1);
-                        const float2 sm = unpack_half2(km[ch]);
-                        qp[cc] = split_part(4.0f * h2f(q_w[hq * T::D + ch]) * sm.x * C, lo_col);
-                    }
-                    uint32_t w[4], x[4], xs[4];
-                    ldmatrix_x4(w, hb + 64 * s2);
-                    split(w, x, xs);
-                    mma_rowsets(acc, x, xs, pack_half2(qp[0], qp[1]), pack_half2(qp[2], qp[3]));
-                }
-                __syncwarp();
-            }
-            cst += __shfl_xor_sync(0xffffffffu, cst, 1);
-            cst += __shfl_xor_sync(0xffffffffu, cst, 2);
-            const float ct = __shfl_sync(0xffffffffu, cst, (2 * t) * 4) * C;  // head t
-
-            // ---- online softmax over the tile (head t; rows g and g+8 of each row set) ----
-            float z[T::NJ][2];
-            unscale_logits(acc, z, ct);
-            float tm = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < T::NJ; j++) tm = fmaxf(tm, fmaxf(z[j][0], z[j][1]));
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-            const float nm = fmaxf(m, tm);
-            const float a = exp2f(m - nm);
-            m = nm;
-            l *= a;
-            mn *= a;
-            // the output lanes own heads 2t, 2t+1: fetch their rescale factors
-            const float a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
-            const float a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
-#pragma unroll
-            for (int o = 0; o < 8; o++) {
-                O[o][0] *= a0;
-                O[o][2] *= a0;
-                O[o][1] *= a1;
-                O[o][3] *= a1;
-            }
-            const uint32_t *vm = reinterpret_cast<const uint32_t *>(st + T::OFF_VM);
-#pragma unroll
-            for (int j = 0; j < T::NJ; j++) {
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int tok = tok_of(j, 2 * e);
-                    const float pe = exp2f(z[j][e] - m);
-                    const float2 sm = unpack_half2(vm[tok]);
-                    l += pe;
-                    mn = fmaf(pe, sm.y, mn);
-                    const int r = tok & 15;
-                    pb[t * T::TOK + (tok & ~15) + 4 * (r & 3) + (r >> 2)] =
-                        __half_as_ushort(__float2half_rn(pe * sm.x));
-                }
-            }
-            __syncwarp();
-
-            // ---- O += Vcodes . p' ----
-            const uint32_t vb = smem_u32(st + T::OFF_V) + (lane & 7) * T::V_STRIDE + 16 * (lane >> 3);
-#pragma unroll
-            for (int sl = 0; sl < T::TSLABS; sl++) {
-                const uint2 bp = *reinterpret_cast<const uint2 *>(pb + gq * T::TOK + 16 * sl + 4 * t);
-#pragma unroll
-                for (int set = 0; set < T::NSET; set++) {
-                    uint32_t w[4], x[4], xs[4];
-                    ldmatrix_x4(w, vb + set * 8 * T::V_STRIDE + 64 * sl);
-                    split(w, x, xs);
-                    mma_rowsets_o(O, set, x, xs, bp.x, bp.y);
-                }
-            }
-            __syncwarp();
-            fence_proxy_async();
-            if (i + kStages < n) issue(t0 + i + kStages, s);
-        }
-        if (failed) {
-            // let copies already in flight land before the shared memory is reused
-            for (int s = 0; s < kStages; s++)
-                if (pending & (1u << s)) mbar_wait(&bars[s], (phase >> s) & 1u, p.status);
-            pending = 0;
-        }
-        // ---- warp partial ----
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l += __shfl_xor_sync(0xffffffffu, l, o);
-            mn += __shfl_xor_sync(0xffffffffu, mn, o);
-        }
-        const float mn0 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t) & 3));
-        const float mn1 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t + 1) & 3));
-        __syncwarp();
-        store_o(O, part, mn0, mn1);
-        if (gq == 0) {
-            part[t * (T::D + 2) + T::D] = m;
-            part[t * (T::D + 2) + T::D + 1] = l;
-        }
-    }
-
-    // hi part (fp16-rounded) or lo part (remainder, rounded later to fp16) of x.
-    __device__ __forceinline__ static float split_part(float x, bool lo) {
-        const float hi = __half2float(__float2half_rn(x));
-        return lo ? x - hi : hi;
-    }
-
-    __device__ __forceinline__ static void mma_rowsets(float (&acc)[T::NJ][4], const uint32_t (&x)[4],
-                                                       const uint32_t (&xs)[4], uint32_t b0, uint32_t b1) {
-        uint32_t a[4];
-#define KVQ_RS(J)                                           \
-    if (J < T::NJ) {                                        \
-        frag<J>(x, xs, a);                                  \
-        mma_16816(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1); \
-    }
-        KVQ_RS(0) KVQ_RS(1) KVQ_RS(2) KVQ_RS(3) KVQ_RS(4) KVQ_RS(5) KVQ_RS(6) KVQ_RS(7)
-#undef KVQ_RS
-    }
-
-    __device__ __forceinline__ static void mma_rowsets_o(float (&O)[8][4], int set, const uint32_t (&x)[4],
-                                                         const uint32_t (&xs)[4], uint32_t b0, uint32_t b1) {
-        uint32_t a[4];
-#define KVQ_RS(J)                                                              \
-    if (J < T::NJ) {                                                           \
-        frag<J>(x, xs, a);                                                     \
-        mma_16816(O[set * T::NJ + (J % T::NJ)], a[0], a[1], a[2], a[3], b0, b1); \
-    }
-        KVQ_RS(0) KVQ_RS(1) KVQ_RS(2) KVQ_RS(3) KVQ_RS(4) KVQ_RS(5) KVQ_RS(6) KVQ_RS(7)
-#undef KVQ_RS
-    }
-
-    // z[j][0] (row g) and z[j][1] (row g+8) of head t: hi + lo columns, unscaled, + constant.
-    __device__ __forceinline__ static void unscale_logits(const float (&acc)[T::NJ][4], float (&z)[T::NJ][2],
-                                                          float c) {
-#define KVQ_US(J)                                                                   \
-    if (J < T::NJ) {                                                                \
-        const float f = unscale<J>();                                               \
-        z[J % T::NJ][0] = fmaf(acc[J % T::NJ][0] + acc[J % T::NJ][1], f, c);        \
-        z[J % T::NJ][1] = fmaf(acc[J % T::NJ][2] + acc[J % T::NJ][3], f, c);        \
-    }
-        KVQ_US(0) KVQ_US(1) KVQ_US(2) KVQ_US(3) KVQ_US(4) KVQ_US(5) KVQ_US(6) KVQ_US(7)
-#undef KVQ_US
-    }
-
-    // O row set o = set*NJ + j: rows g <-> channel FPI*(gq+8*set) + j, g+8 <-> + FPI/2.
-    __device__ __forceinline__ void store_o(const float (&O)[8][4], float *part, float mn0, float mn1) const {
-        const int gq = lane >> 2, t = lane & 3;
-#define KVQ_SO(J)                                                                        \
-    if (J < T::NJ) {                                                                     \
-        const float f = unscale<J>();                                                    \
-        for (int set = 0; set < T::NSET; set++) {                                        \
-            const int o = set * T::NJ + (J % T::NJ);                                     \
-            const int ch = T::FPI * (gq + 8 * set) + (J % T::NJ);                        \
-            const int ch2 = ch + T::FPI / 2;                                             \
-            part[(2 * t) * (T::D + 2) + ch] = fmaf(O[o][0], f, mn0);                     \
-            part[(2 * t + 1) * (T::D + 2) + ch] = fmaf(O[o][1], f, mn1);                 \
-            part[(2 * t) * (T::D + 2) + ch2] = fmaf(O[o][2], f, mn0);                    \
-            part[(2 * t + 1) * (T::D + 2) + ch2] = fmaf(O[o][3], f, mn1);                \
-        }                                                                                \
-    }
-        KVQ_SO(0) KVQ_SO(1) KVQ_SO(2) KVQ_SO(3) KVQ_SO(4) KVQ_SO(5) KVQ_SO(6) KVQ_SO(7)
-#undef KVQ_SO
-    }
+struct Pool {
+    int64_t n, N, W;
+    int c0;  // first CTA of the pool in the grid
+    int C;
 };
-
-// ---------------------------------------------------------------------------------
-// Schedule arithmetic shared by every CTA (closed forms, no tables).
-// ---------------------------------------------------------------------------------
-// Fast warp k (of W = 8*C_f) owns flattened tiles [a_k, a_{k+1}), a_k = floor(k*N/W).
-__device__ __forceinline__ int64_t fast_a(const DecodeParams &p, int64_t k) {
-    return k * p.N_f / (8 * (int64_t)p.C_f);
+__device__ __forceinline__ int64_t pool_a(const Pool &P, int64_t k) { return k * P.N / P.W; }
+__device__ __forceinline__ int64_t pool_warp_of(const Pool &P, int64_t x) {
+    const int64_t k = ((x + 1) * P.W - 1) / P.N;
+    return k < P.W - 1 ? k : P.W - 1;
 }
-// The warp whose range holds flattened tile x: the largest k with a_k <= x.
-__device__ __forceinline__ int64_t fast_warp_of(const DecodeParams &p, int64_t x) {
-    const int64_t W = 8 * (int64_t)p.C_f;
-    const int64_t k = ((x + 1) * W - 1) / p.N_f;
-    return k < W - 1 ? k : W - 1;
+// CTAs of the pool that hold items of sequence u (first via *first).
+__device__ __forceinline__ int pool_ctas(const Pool &P, int wpc, int u, int *first) {
+    if (P.n == 0 || P.C == 0) {
+        *first = 0;
+        return 0;
+    }
+    const int f = (int)(pool_warp_of(P, (int64_t)u * P.n) / wpc);
+    const int l = (int)(pool_warp_of(P, (int64_t)(u + 1) * P.n - 1) / wpc);
+    *first = f;
+    return l - f + 1;
 }
-__device__ __forceinline__ int n_fast_ctas(const DecodeParams &p, int u, int *first) {
-    if (p.n_fast == 0) { *first = 0; return 0; }
-    const int c0 = (int)(fast_warp_of(p, (int64_t)u * p.n_fast) / 8);
-    const int c1 = (int)(fast_warp_of(p, (int64_t)(u + 1) * p.n_fast - 1) / 8);
-    *first = c0;
-    return c1 - c0 + 1;
-}
-__device__ __forceinline__ int n_gen_ctas(const DecodeParams &p, int u, int *first) {
-    if (p.n_gc == 0) { *first = 0; return 0; }
-    const int c0 = (int)(((int64_t)u * p.n_gc) / 8);
-    const int c1 = (int)(((int64_t)(u + 1) * p.n_gc - 1) / 8);
-    *first = c0;
-    return c1 - c0 + 1;
+__device__ __forceinline__ int gen_ctas(const DecodeParams &p, int u, int *first) {
+    if (p.n_gc == 0) {
+        *first = 0;
+        return 0;
+    }
+    const int f = (int)(((int64_t)u * p.n_gc) / p.wpc);
+    const int l = (int)(((int64_t)(u + 1) * p.n_gc - 1) / p.wpc);
+    *first = f;
+    return l - f + 1;
 }
 
-__device__ __forceinline__ void load_q(const DecodeParams &p, int u, uint16_t *q_w) {
+__device__ __forceinline__ void load_q_gen(const DecodeParams &p, int u, uint16_t *q_w) {
     const int lane = threadIdx.x & 31, D = p.D;
-    for (int i = lane; i < 8 * D / 8; i += 32) {
+    for (int i = lane; i < D; i += 32) {  // 8 heads x D halves in uint4 chunks
         const int h = (i * 8) / D, d = (i * 8) % D;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (h < p.g) v = *reinterpret_cast<const uint4 *>(p.q + ((size_t)u * p.g + h) * D + d);
@@ -652,52 +275,69 @@ __device__ __forceinline__ void load_q(const DecodeParams &p, int u, uint16_t *q
     __syncwarp();
 }
 
+// Weight tables of the merge and combine phases: behind warp 0's partial in a fast
+// kernel (its slots are free once the tiles are done), else behind the warp regions.
+constexpr int kGenTabFloats = 7168;
+template <int BITS, bool KITTY, bool FAST, int NW>
+__host__ __device__ inline int tab_offset(const DecodeParams &p) {
+    if (FAST) return part_bytes(p.D);
+    return NW * gen_warp_bytes(p.D);
+}
+template <int BITS, bool KITTY, bool FAST>
+__host__ __device__ inline int tab_capacity(int n_boost, int D) {
+    if (FAST) return (WarpSmem<BITS>(KITTY, n_boost).total - part_bytes(D)) / 4;
+    return kGenTabFloats;
+}
+
 // ---------------------------------------------------------------------------------
-// The kernel.
+// The kernel.  FAST: CTAs [0, C_f) fast warps, [C_f, C_f + C_m) mini warps.
+// Otherwise: generic warps only.
 // ---------------------------------------------------------------------------------
-template <int BITS, bool KITTY, bool FAST, int DPL>
-__global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const DecodeParams p) {
+template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_seg[kWarps][2];   // sequence of each warp segment (-1: none)
-    __shared__ int s_last[16];         // sequences this CTA must combine
+    __shared__ int s_seg[NW][2];  // sequence of each warp segment (-1: none)
+    __shared__ int s_last[24];    // sequences this CTA must combine
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, D = p.D, g = p.g;
-    const int wbytes = FAST ? fast_warp_bytes<BITS>(KITTY, p.n_boost) : gen_warp_bytes(D);
+    const int wbytes = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).total : gen_warp_bytes(D);
     unsigned char *wbase = smem + warp * wbytes;
-    float *part = reinterpret_cast<float *>(wbase);  // final partial of this warp, [8][D+2]
-    const bool fast_cta = FAST && c < p.C_f;
+    float *part = reinterpret_cast<float *>(wbase);  // the warp's last partial, [8][D+2]
     int seg0 = -1, seg1 = -1;
+    const Pool PF{p.n_fast, p.N_f, (int64_t)p.wpc * p.C_f, 0, p.C_f};
+    const Pool PM{p.n_mini, p.N_m, (int64_t)p.wpc * p.C_m, p.C_f, p.C_m};
+    int pool = 2;  // 0 fast, 1 mini, 2 generic
+    if (FAST) pool = c < p.C_f ? 0 : 1;
 
-    if (fast_cta) {
-        // ---- fast warp: flattened tile range, at most two sequences ----
-        const int64_t k = (int64_t)c * kWarps + warp;
-        const int64_t x0 = fast_a(p, k), x1 = fast_a(p, k + 1);
-        uint16_t *q_w = reinterpret_cast<uint16_t *>(wbase + fast_qbuf_off<BITS>(KITTY, p.n_boost));
-        FastWarp<BITS, KITTY> fw(p, wbase);
-        fw.init_bars();
+    if (FAST) {
+        const Pool &P = pool == 0 ? PF : PM;
+        const int64_t k = (int64_t)(c - P.c0) * p.wpc + warp;
+        const int64_t x0 = pool_a(P, k), x1 = pool_a(P, k + 1);
+        // a warp range touches at most two sequences; a first segment followed by a
+        // second one is parked in global scratch, the last one stays in shared memory
         int64_t x = x0;
+        int nseg = 0;
+        FastWarp<BITS, KITTY> fw(p, wbase);
+        MiniWarp<BITS, KITTY> mw(p, wbase, 0);
         if (x < x1) {
-            const int u0 = (int)(x / p.n_fast);
-            const int64_t e0 = kvq_min64(x1, (int64_t)(u0 + 1) * p.n_fast);
-            // a first segment followed by another one is parked in global scratch;
-            // the warp's last segment stays in its shared-memory slot
-            const bool two = e0 < x1;
-            float *dst = two ? p.scratch + (size_t)k * part_bytes(D) / 4 : part;
-            load_q(p, u0, q_w);
-            fw.run(u0, x - (int64_t)u0 * p.n_fast, e0 - (int64_t)u0 * p.n_fast, q_w, dst);
-            if (two) seg0 = u0;
-            else seg1 = u0;
-            x = e0;
+            if (pool == 0) fw.init_bars();
+            else mw.init_bars();
         }
-        if (x < x1) {
-            const int u1 = (int)(x / p.n_fast);
-            load_q(p, u1, q_w);
-            fw.run(u1, x - (int64_t)u1 * p.n_fast, x1 - (int64_t)u1 * p.n_fast, q_w, part);
-            seg1 = u1;
+        while (x < x1 && nseg < 2) {
+            const int u = (int)(x / P.n);
+            const int64_t e = kvq_min64(x1, (int64_t)(u + 1) * P.n);
+            const bool more = e < x1;
+            float *dst = more ? p.scratch + ((size_t)c * NW + warp) * (part_bytes(D) / 4) : part;
+            if (pool == 0) fw.run(u, x - (int64_t)u * P.n, e - (int64_t)u * P.n, dst);
+            else mw.run(u, x - (int64_t)u * P.n, e - (int64_t)u * P.n, dst);
+            if (more) seg0 = u;
+            else seg1 = u;
+            x = e;
+            nseg++;
         }
     } else {
         // ---- generic warp: one chunk of one sequence ----
-        const int64_t j = (int64_t)(c - (FAST ? p.C_f : 0)) * kWarps + warp;
+        const int64_t j = (int64_t)c * p.wpc + warp;
         GenState<DPL> st;
 #pragma unroll
         for (int h = 0; h < 8; h++) {
@@ -710,9 +350,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const DecodePara
             const int u = (int)(j / p.n_gc);
             const int64_t a = (j % p.n_gc) * p.gen_chunk;
             const int64_t b = kvq_min64(a + p.gen_chunk, p.n_gen);
-            uint16_t *q_w = reinterpret_cast<uint16_t *>(
-                wbase + (FAST ? fast_qbuf_off<BITS>(KITTY, p.n_boost) : part_bytes(D)));
-            load_q(p, u, q_w);
+            uint16_t *q_w = reinterpret_cast<uint16_t *>(wbase + part_bytes(D));
+            load_q_gen(p, u, q_w);
             generic_range<DPL>(p, u, q_w, a, b, st);
             generic_store<DPL>(p, st, part);
             seg1 = u;
@@ -725,120 +364,208 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const DecodePara
     __syncthreads();
 
     // ---- merge the warps of this CTA per sequence, publish, take a ticket ----
+    // Phase 1 (one thread per (sequence, head)): the running max over the warp
+    // partials of that sequence and each partial's weight exp2(m - M).  Phase 2: a
+    // flat loop over (sequence, head, channel) with independent loads.
     int ulo = 0x7fffffff, uhi = -1;
-    for (int w = 0; w < kWarps; w++)
+    for (int w = 0; w < NW; w++)
         for (int e = 0; e < 2; e++)
             if (s_seg[w][e] >= 0) {
                 ulo = min(ulo, s_seg[w][e]);
                 uhi = max(uhi, s_seg[w][e]);
             }
-    if (uhi - ulo >= 16) {  // cannot happen with the host schedule; never index past s_last
-        report(p.status, KVQ_DEV_BAD_STATE_BIT);
+    if (uhi < 0) return;
+    const int nu = uhi - ulo + 1;
+    if (nu > 24) {  // impossible with the host schedule; never index past s_last
+        if (tid == 0) report(p.status, KVQ_DEV_BAD_STATE_BIT);
         return;
     }
     const int wb = wbytes / 4;  // floats between warp partials in shared memory
     const float *wpart = reinterpret_cast<const float *>(smem);
-    for (int u = ulo; u <= uhi; u++) {
-        int f0, g0;
-        const int nf = n_fast_ctas(p, u, &f0);
-        const int ng = n_gen_ctas(p, u, &g0);
-        const int slot = fast_cta ? c - f0 : nf + (c - (FAST ? p.C_f : 0) - g0);
-        float *gpart = p.partials + ((size_t)u * p.max_slots + slot) * g * (D + 2);
-        for (int i = tid; i < g * (D + 2); i += blockDim.x) {
-            const int h = i / (D + 2), d = i % (D + 2);
-            const float *src[2 * kWarps];
-            int n = 0;
-            for (int w = 0; w < kWarps; w++) {
-                if (s_seg[w][0] == u)
-                    src[n++] = p.scratch + ((size_t)c * kWarps + w) * part_bytes(D) / 4;
-                if (s_seg[w][1] == u) src[n++] = wpart + w * wb;
+    const int R = prow(D);
+    // weight tables (merge: [nu*g][2*NW] + [nu*g][2]; combine: [nl*g][max_slots]) in
+    // shared memory the tiles no longer use (host checks the capacity)
+    float *wtab = reinterpret_cast<float *>(smem + tab_offset<BITS, KITTY, FAST, NW>(p));
+    __shared__ int s_slot[24];
+    auto src_of = [&](int w, int e) -> const float * {
+        return e == 0 ? p.scratch + ((size_t)c * NW + w) * (part_bytes(D) / 4) : wpart + w * wb;
+    };
+    for (int pi = tid; pi < nu * g; pi += blockDim.x) {
+        const int u = ulo + pi / g, h = pi % g;
+        float M = -INFINITY;
+        for (int w = 0; w < NW; w++)
+            for (int e = 0; e < 2; e++)
+                if (s_seg[w][e] == u) M = fmaxf(M, src_of(w, e)[h * R + D]);
+        float L = 0.f;
+        for (int w = 0; w < NW; w++)
+            for (int e = 0; e < 2; e++) {
+                float f = 0.f;
+                if (s_seg[w][e] == u) {
+                    const float mw = src_of(w, e)[h * R + D];
+                    if (mw != -INFINITY) f = exp2f(mw - M);
+                    L = fmaf(src_of(w, e)[h * R + D + 1], f, L);
+                }
+                wtab[pi * 2 * NW + 2 * w + e] = f;
             }
-            float M = -INFINITY;
-            for (int k2 = 0; k2 < n; k2++) M = fmaxf(M, src[k2][h * (D + 2) + D]);
-            float acc = 0.f;
-            for (int k2 = 0; k2 < n; k2++) {
-                const float mw = src[k2][h * (D + 2) + D];
-                if (mw == -INFINITY) continue;
-                const float f = exp2f(mw - M);
-                if (d < D) acc = fmaf(src[k2][h * (D + 2) + d], f, acc);
-                else if (d == D + 1) acc = fmaf(src[k2][h * (D + 2) + D + 1], f, acc);
-            }
-            gpart[h * (D + 2) + d] = (d == D) ? M : acc;
+        wtab[nu * g * 2 * NW + pi * 2] = M;
+        wtab[nu * g * 2 * NW + pi * 2 + 1] = L;
+        if (h == 0) {
+            int ff, fm, fg;
+            const int nf = pool_ctas(PF, p.wpc, u, &ff);
+            pool_ctas(PM, p.wpc, u, &fm);
+            if (!FAST) gen_ctas(p, u, &fg);
+            s_slot[u - ulo] = !FAST ? c - fg : (pool == 0 ? c - ff : nf + (c - p.C_f - fm));
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_last[u - ulo] = (atomicAdd(&p.tickets[u], 1) == nf + ng - 1);
-        __syncthreads();
     }
-    if (uhi < 0) return;
+    __syncthreads();
+    for (int i = tid; i < nu * g * (D / 4); i += blockDim.x) {
+        const int pi = i / (D / 4), d = 4 * (i % (D / 4));
+        const int ul = pi / g, h = pi % g, u = ulo + ul;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < NW; w++)
+            for (int e = 0; e < 2; e++) {
+                const float f = wtab[pi * 2 * NW + 2 * w + e];
+                if (f != 0.f) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src_of(w, e) + h * R + d);
+                    acc.x = fmaf(v.x, f, acc.x);
+                    acc.y = fmaf(v.y, f, acc.y);
+                    acc.z = fmaf(v.z, f, acc.z);
+                    acc.w = fmaf(v.w, f, acc.w);
+                }
+            }
+        float *gpart = p.partials + ((size_t)u * p.max_slots + s_slot[ul]) * g * R + h * R;
+        *reinterpret_cast<float4 *>(gpart + d) = acc;
+        if (d == 0) {
+            gpart[D] = wtab[nu * g * 2 * NW + pi * 2];
+            gpart[D + 1] = wtab[nu * g * 2 * NW + pi * 2 + 1];
+        }
+    }
+    // Publish: the CTA barrier orders every thread's partial stores before the
+    // GPU-scope release fence of the ticket thread of each sequence; the acquire
+    // fence after the ticket orders the combine's reads of the other CTAs' slots.
+    __syncthreads();
+    if (tid < nu) {
+        const int u = ulo + tid;
+        int f0;
+        const int n = pool_ctas(PF, p.wpc, u, &f0) + pool_ctas(PM, p.wpc, u, &f0) + (FAST ? 0 : gen_ctas(p, u, &f0));
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        s_last[tid] = (atomicAdd(&p.tickets[u], 1) == n - 1);
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    }
+    __syncthreads();
 
     // ---- the last CTA of a sequence: log-sum-exp combine of its slots ----
-    for (int u = ulo; u <= uhi; u++) {
-        if (!s_last[u - ulo]) continue;
-        __threadfence();
-        int f0, g0;
-        const int ns = n_fast_ctas(p, u, &f0) + n_gen_ctas(p, u, &g0);
-        const float *up = p.partials + (size_t)u * p.max_slots * g * (D + 2);
-        for (int i = tid; i < g * D; i += blockDim.x) {
-            const int h = i / D, d = i % D;
-            float M = -INFINITY;
-            for (int cc = 0; cc < ns; cc++) M = fmaxf(M, __ldcg(up + ((size_t)cc * g + h) * (D + 2) + D));
-            float L = 0.f, O = 0.f;
-            for (int cc = 0; cc < ns; cc++) {
-                const float *pc = up + ((size_t)cc * g + h) * (D + 2);
-                const float mc = __ldcg(pc + D);
-                if (mc == -INFINITY) continue;
-                const float f = exp2f(mc - M);
-                L = fmaf(__ldcg(pc + D + 1), f, L);
-                O = fmaf(__ldcg(pc + d), f, O);
-            }
-            p.out[((size_t)u * g + h) * D + d] = __half_as_ushort(__float2half_rn(O / L));
-        }
-        if (tid == 0) p.tickets[u] = 0;
+    // Phase 1 (one thread per (sequence, head)): weights w_c = exp2(m_c - M) / L of the
+    // slots; phase 2: out = sum_c w_c o_c over (sequence, head, channel).
+    __shared__ int s_lu[24];
+    if (tid == 0) {
+        int n = 0;
+        for (int k = 0; k < nu; k++)
+            if (s_last[k]) s_lu[n++] = ulo + k;
     }
+    int nl = 0;
+    for (int k = 0; k < nu; k++) nl += s_last[k] ? 1 : 0;
+    __syncthreads();
+    if (nl == 0) return;
+    const int ms = p.max_slots;
+    float *ctab = wtab;  // [nl * g][ms] weights (phase 2 of the merge is done)
+    __shared__ int s_ns[24];
+    for (int pi = tid; pi < nl * g; pi += blockDim.x) {
+        const int u = s_lu[pi / g], h = pi % g;
+        int f0;
+        const int ns = pool_ctas(PF, p.wpc, u, &f0) + pool_ctas(PM, p.wpc, u, &f0) + (FAST ? 0 : gen_ctas(p, u, &f0));
+        if (h == 0) s_ns[pi / g] = ns;
+        const float *up = p.partials + (size_t)u * ms * g * R + h * R;
+        float M = -INFINITY;
+        for (int cc = 0; cc < ns; cc++) M = fmaxf(M, __ldcg(up + (size_t)cc * g * R + D));
+        float L = 0.f;
+        for (int cc = 0; cc < ns; cc++) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(up + (size_t)cc * g * R + D));
+            const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            L = fmaf(ml.y, f, L);
+            ctab[pi * ms + cc] = f;
+        }
+        const float inv = 1.0f / L;
+        for (int cc = 0; cc < ns; cc++) ctab[pi * ms + cc] *= inv;
+    }
+    __syncthreads();
+    for (int i = tid; i < nl * g * (D / 4); i += blockDim.x) {
+        const int pi = i / (D / 4), d = 4 * (i % (D / 4));
+        const int u = s_lu[pi / g], h = pi % g, ns = s_ns[pi / g];
+        const float *up = p.partials + (size_t)u * ms * g * R + h * R + d;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int cc = 0; cc < ns; cc++) {
+            const float f = ctab[pi * ms + cc];
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(up + (size_t)cc * g * R));
+            O.x = fmaf(v.x, f, O.x);
+            O.y = fmaf(v.y, f, O.y);
+            O.z = fmaf(v.z, f, O.z);
+            O.w = fmaf(v.w, f, O.w);
+        }
+        uint2 hv;
+        hv.x = pack_half2(O.x, O.y);
+        hv.y = pack_half2(O.z, O.w);
+        *reinterpret_cast<uint2 *>(p.out + ((size_t)u * g + h) * D + d) = hv;
+    }
+    __syncthreads();
+    if (tid < nl) p.tickets[s_lu[tid]] = 0;
 }
 
 // ---------------------------------------------------------------------------------
-size_t decode_smem_bytes_impl(int bits, bool kitty, int n_boost, int D, bool fast) {
-    size_t w;
-    if (fast) w = bits == 2 ? fast_warp_bytes<2>(kitty, n_boost) : fast_warp_bytes<4>(kitty, n_boost);
-    else w = gen_warp_bytes(D);
-    return (size_t)kWarps * w;
+int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast) {
+    if (!fast) return 8;
+    const int w = bits == 2 ? WarpSmem<2>(kitty, n_boost).total : WarpSmem<4>(kitty, n_boost).total;
+    return w * 8 <= 227 * 1024 ? 8 : 6;
 }
 
-size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D) {
-    return decode_smem_bytes_impl(bits, kitty, n_boost, D, true);
+size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast) {
+    const int nw = decode_warps_per_cta(bits, kitty, n_boost, fast);
+    if (fast) return (size_t)nw * (bits == 2 ? WarpSmem<2>(kitty, n_boost).total : WarpSmem<4>(kitty, n_boost).total);
+    return (size_t)nw * gen_warp_bytes(D) + kGenTabFloats * 4;
 }
 
-template <int BITS, bool KITTY, bool FAST, int DPL>
+int decode_table_floats(int bits, bool kitty, int n_boost, int D, bool fast) {
+    if (!fast) return kGenTabFloats;
+    if (bits == 2) return kitty ? tab_capacity<2, true, true>(n_boost, D) : tab_capacity<2, false, true>(n_boost, D);
+    return tab_capacity<4, false, true>(n_boost, D);
+}
+
+template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
 static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
-    const size_t smem = decode_smem_bytes_impl(BITS, KITTY, p.n_boost, p.D, FAST);
-    auto k = decode_kernel<BITS, KITTY, FAST, DPL>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<(unsigned)(p.C_f + p.C_g), kWarps * 32, smem, st>>>(p);
+    const size_t smem = decode_smem_bytes(BITS, KITTY, p.n_boost, p.D, FAST);
+    auto k = decode_kernel<BITS, KITTY, FAST, DPL, NW>;
+    // The dynamic shared-memory limit is raised once per device to the most any
+    // configuration of this instantiation asks for (the opt-in maximum).
+    static int raised[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !raised[dev]) {
+        int optin = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) raised[dev] = 1;
+    }
+    if (smem > (size_t)(227 * 1024)) return cudaErrorInvalidValue;
+    k<<<(unsigned)(p.C_f + p.C_m + p.C_g), NW * 32, smem, st>>>(p);
     return cudaGetLastError();
-}
-
-int decode_max_ctas_per_sm(int bits, bool kitty, int n_boost, int D, bool fast) {
-    (void)bits;
-    (void)kitty;
-    (void)n_boost;
-    (void)D;
-    (void)fast;
-    return 1;  // __launch_bounds__(256, 1) and ~170 KB of shared memory per CTA
 }
 
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st) {
     if (fast) {
-        if (p.kitty) return launch_one<2, true, true, 4>(p, st);
-        if (p.bits == 2) return launch_one<2, false, true, 4>(p, st);
-        return launch_one<4, false, true, 4>(p, st);
+        if (p.kitty) {
+            if (p.wpc == 8) return launch_one<2, true, true, 4, 8>(p, st);
+            return launch_one<2, true, true, 4, 6>(p, st);
+        }
+        if (p.bits == 2) return launch_one<2, false, true, 4, 8>(p, st);
+        return launch_one<4, false, true, 4, 8>(p, st);
     }
     switch (p.D) {
-        case 64: return launch_one<2, false, false, 2>(p, st);
-        case 128: return launch_one<2, false, false, 4>(p, st);
-        case 256: return launch_one<2, false, false, 8>(p, st);
+        case 64: return launch_one<2, false, false, 2, 8>(p, st);
+        case 128: return launch_one<2, false, false, 4, 8>(p, st);
+        case 256: return launch_one<2, false, false, 8, 8>(p, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -45,15 +45,16 @@ struct AppendParams {
     int U, D;
 };
 
-// Decode attention schedule.  Fast items are tiles of TOK tokens whose keys and
-// values are both packed (tensor-core path); the flattened list of all sequences'
-// tiles (sequence-major, N_f = U * n_fast) is cut into W_f = 8 * C_f equal warp
-// ranges, each of length <= n_fast, so a warp touches at most two sequences.
-// Generic items are chunks of gen_chunk tokens of the rest of each sequence (sink,
-// fp16 buffers, packed tokens outside the tiles; CUDA-core path), one chunk per
-// warp, n_gc chunks per sequence.  CTAs [0, C_f) run fast warps, CTAs
-// [C_f, C_f + C_g) generic warps.  A CTA merges its warps' partial softmax states
-// per sequence into one slot; the last CTA of a sequence (ticket) combines.
+// Decode attention schedule.  Work items of one sequence:
+//   fast tiles: TOK tokens whose keys and values are both packed (tensor cores);
+//   mini tiles: 16 tokens whose values are fp16 -- sink, residual / Q-buffer, local
+//               window -- with fp16 keys or a packed key block (tensor cores);
+//   generic chunks: any token, CUDA cores (only for shapes the tile paths do not
+//               cover; then there are no fast or mini items).
+// Each kind has a pool of CTAs whose warps cut the sequence-major list of all
+// sequences' items into equal ranges; a range touches at most two sequences.
+// A CTA merges its warps' partial softmax states per sequence into one slot;
+// the last CTA of a sequence (ticket) combines the slots.
 struct DecodeParams {
     // shape
     int B, H_kv, g, D, G, bits, Gv, n_boost, kitty;
@@ -70,27 +71,30 @@ struct DecodeParams {
     const uint16_t *k_sink, *v_sink, *k_res, *v_res, *v_local;
     const uint16_t *q;
     uint16_t *out;
-    float *partials;       // [U][max_slots][g][D + 2]
-    float *scratch;        // [8 * C_f][8][D + 2] first-segment partials of fast warps
+    float *partials;       // [U][max_slots][g][D + 4]
+    float *scratch;        // [CTAs][warps][8][D + 4] first-segment partials
     int32_t *tickets;      // [U]
     int32_t *status;       // workspace status word
     // schedule
-    int U, C_f, C_g, n_gc, max_slots;
-    int64_t n_fast;        // fast tiles per sequence
-    int64_t N_f;           // U * n_fast
+    int U, wpc;            // sequences, warps per CTA
+    int C_f, C_m, C_g;     // CTAs of the fast, mini and generic pools (grid order)
+    int n_gc, max_slots;
+    int tpp_shift, g_shift;  // log2(packed tiles per page), log2(G) (tile paths only)
+    int64_t n_fast, N_f;   // fast tiles per sequence, in all
+    int64_t n_mini, N_m;   // mini tiles per sequence, in all
     int64_t n_gen;         // generic tokens per sequence
     int64_t gen_chunk;     // tokens per generic chunk (multiple of 32)
 };
 
-constexpr int kWarps = 8;
-constexpr int kStages = 2;
+constexpr int kMaxWarps = 8;
 
 cudaError_t launch_quant_k(const QuantKParams &p, int bits, bool kitty, cudaStream_t st);
 cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
 cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
-size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D);
-int decode_max_ctas_per_sm(int bits, bool kitty, int n_boost, int D, bool fast);
+size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast);
+int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast);
+int decode_table_floats(int bits, bool kitty, int n_boost, int D, bool fast);
 
 }  // namespace kvq
