@@ -72,7 +72,8 @@ def decode_bytes(wl, lengths) -> int:
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"):
+    for f in ("kvq_decode.cu", "kvq_decode_fast.cuh", "kvq_device.cuh", "kvq_internal.h",
+              "kvq_api.cu"):
         with open(os.path.join(ROOT, "bit_kv_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -146,6 +147,22 @@ class Clocks:
         reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def reduce_over_ranks(ms: float, nbytes: float, world: int, device=None):
+    """Whole-job numbers of a timed region: the slowest rank's time and the bytes
+    of all ranks (each rank works on its own shard; this is the only collective,
+    and it runs after the timed region)."""
+    if world <= 1:
+        return ms, nbytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, nbytes], dtype=torch.float64, device=device)
+    mx = t[:1].clone()
+    sm = t[1:].clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[0])
 
 
 def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
@@ -334,14 +351,7 @@ def main():
     if st != 0:
         print("device status %d" % st, file=sys.stderr)
     launches = 2 * K + flushes
-    if world > 1:
-        t = torch.tensor([ms, float(total_bytes)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        ms_max, bytes_all = float(mx[0]), float(t[1])
-    else:
-        ms_max, bytes_all = ms, float(total_bytes)
+    ms_max, bytes_all = reduce_over_ranks(ms, float(total_bytes), world, dev)
 
     # ---- end to end through host buffers (public API, pinned memory) ----
     kn_h = torch.from_numpy(kn).pin_memory()
