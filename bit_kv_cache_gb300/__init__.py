@@ -24,7 +24,7 @@ BUFFERS = ("k_codes", "k_hi", "k_bidx", "k_meta", "v_codes", "v_meta", "k_sink",
 EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_pack_k",
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
-           "kvq_read_status")
+           "kvq_read_status", "kvq_decode_attn_noalloc")
 
 
 class KvqError(RuntimeError):
@@ -66,6 +66,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_workspace_init": ([P, Sz, P], I),
         "kvq_decode_attn": ([CP, KP, P, P, P, Sz, P], I),
         "kvq_read_status": ([KP, P, ctypes.POINTER(ctypes.c_int32), P], I),
+        "kvq_decode_attn_noalloc": ([CP, KP, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)

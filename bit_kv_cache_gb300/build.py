@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu"]
+SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu", "kvq_noalloc.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode_fast.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

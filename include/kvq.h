@@ -178,6 +178,31 @@ int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream);
 int kvq_decode_attn(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
                     uint16_t *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Size of the library's own decode scratch region (16 MiB per device). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Decode attention exactly as kvq_decode_attn, but without a caller workspace: it
+ * uses a fixed KVQ_NOALLOC_SCRATCH_BYTES region that the library module itself
+ * reserves on each device when its code is loaded.  The pages have no counterpart;
+ * this exists for callers that cannot hand out device memory in their decode step,
+ * for example an inference engine whose memory pool is already fully reserved for
+ * weights and KV pages, or a plugin called from a host runtime that forbids
+ * allocations inside its step callback.  Nothing here allocates.
+ *   - The first call on a device (with that device current) looks the region up
+ *     and enqueues a zero fill of it on `stream`; the status word and the
+ *     split-T counters must start at zero, and every call leaves the counters at
+ *     zero again.  Make that first call before any stream capture.
+ *   - Configurations whose workspace (kvq_decode_attn_workspace_bytes) exceeds the
+ *     region are refused with KVQ_ERR_WORKSPACE; nothing is enqueued.
+ *   - The region is shared by all calls on a device: two calls whose kernels may
+ *     overlap (different streams, or different host threads without ordering)
+ *     race on it and give wrong results.  Serialize them, e.g. on one stream.
+ *   - Device-side error bits of these calls are kept in the region's own status
+ *     word and are not returned by kvq_read_status.
+ * Other arguments, layouts and errors as for kvq_decode_attn. */
+int kvq_decode_attn_noalloc(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                            uint16_t *out, void *stream);
+
 /* Synchronizes `stream`, then returns in *dev_status the OR of the error bits the
  * kernels wrote into the workspace status word and into cache->status (if cache is
  * not NULL and its status pointer is set), and clears both.  KVQ_ERR_DEVICE if any
