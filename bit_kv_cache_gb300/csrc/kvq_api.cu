@@ -67,17 +67,20 @@ int64_t slot_bound(const kvq_config *c) { return cdiv(4 * (int64_t)num_sms(), un
 // range within two sequences (about U / warps-per-CTA).
 int64_t max_pool_ctas(const kvq_config *c) { return std::max<int64_t>(num_sms(), cdiv(units(c), 6)); }
 
+// Workspace: [status word][slot counters U][item counters U][partials].  The
+// counters are zero between calls (the combining CTA resets them).
 struct WsLayout {
-    size_t status, tickets, scratch, partials, total;
+    size_t status, slot_ctr, item_ctr, partials, total;
 };
 
 WsLayout ws_layout(const kvq_config *c) {
     WsLayout w;
     const int64_t U = units(c), g = c->H_q / c->H_kv;
+    const size_t ctr = (size_t)cdiv(U * 4, 256) * 256;
     w.status = 0;
-    w.tickets = 256;
-    w.scratch = w.tickets + (size_t)cdiv(U * 4, 256) * 256;
-    w.partials = w.scratch + (size_t)2 * max_pool_ctas(c) * kMaxWarps * 8 * (c->D + 4) * 4;
+    w.slot_ctr = 256;
+    w.item_ctr = w.slot_ctr + ctr;
+    w.partials = w.item_ctr + ctr;
     w.total = w.partials + (size_t)U * slot_bound(c) * g * (c->D + 4) * 4;
     return w;
 }
@@ -519,12 +522,11 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
             if (p.n_gc > 0) sl += ((u + 1) * p.n_gc - 1) / wpc - (u * p.n_gc) / wpc + 1;
             max_slots = std::max(max_slots, sl);
         }
-        // merge / combine weight tables must fit the kernel's free shared memory
-        const int64_t tab = decode_table_floats(c->bits, kitty(c), kitty(c) ? c->n_boost : 0, c->D, fast);
-        const int64_t nu_max = std::min<int64_t>(24, U);
-        const bool tab_ok = 24 * g * (2 * wpc + 2) <= tab && nu_max * g * max_slots <= tab;
+        // item indices of the tile pools stay 32-bit in the kernel
+        const bool small = p.N_f < (1LL << 31) && p.N_m < (1LL << 31) && p.n_fast + p.n_mini < (1LL << 31) &&
+                           (int64_t)p.U * p.n_gc < (1LL << 31);
         if (max_slots < 1 || max_slots > slot_bound(c) || p.C_f > max_pool_ctas(c) || p.C_m > max_pool_ctas(c) ||
-            p.C_g > 4 * (int64_t)max_pool_ctas(c) || !tab_ok)
+            p.C_g > 4 * (int64_t)max_pool_ctas(c) || !small)
             return KVQ_ERR_UNSUPPORTED;
         p.max_slots = (int)max_slots;
         last_key = key;
@@ -533,6 +535,13 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
         have_last = true;
     }
 
+    p.n_items = fast ? (int)(p.n_fast + p.n_mini) : p.n_gc;
+    p.W_f = p.C_f * wpc;
+    p.W_m = p.C_m * wpc;
+    p.qN_f = p.W_f ? (int)(p.N_f / p.W_f) : 0;
+    p.rN_f = p.W_f ? (int)(p.N_f % p.W_f) : 0;
+    p.qN_m = p.W_m ? (int)(p.N_m / p.W_m) : 0;
+    p.rN_m = p.W_m ? (int)(p.N_m % p.W_m) : 0;
     p.B = c->B;
     p.H_kv = c->H_kv;
     p.g = g;
@@ -578,8 +587,8 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.out = out;
     char *w = static_cast<char *>(ws);
     p.status = reinterpret_cast<int32_t *>(w + wl.status);
-    p.tickets = reinterpret_cast<int32_t *>(w + wl.tickets);
-    p.scratch = reinterpret_cast<float *>(w + wl.scratch);
+    p.slot_ctr = reinterpret_cast<int32_t *>(w + wl.slot_ctr);
+    p.item_ctr = reinterpret_cast<int32_t *>(w + wl.item_ctr);
     p.partials = reinterpret_cast<float *>(w + wl.partials);
     return status_of(launch_decode(p, fast, (cudaStream_t)stream));
 }

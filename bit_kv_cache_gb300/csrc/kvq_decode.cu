@@ -228,40 +228,16 @@ __device__ void generic_store(const DecodeParams &p, const GenState<DPL> &st, fl
 }
 
 // ---------------------------------------------------------------------------------
-// Schedule arithmetic (closed forms, identical on host and device).
-// A pool of W = wpc * C warps cuts the sequence-major list of N = U * n items into
-// ranges [a_k, a_{k+1}), a_k = floor(k * N / W).
+// Schedule arithmetic.  A pool of W warps cuts the sequence-major list of N items
+// (n per sequence) into ranges [a_k, a_{k+1}), a_k = floor(k * N / W), evaluated as
+// k * (N / W) + floor(k * (N % W) / W) so that it stays in 32-bit values (the host
+// checks N < 2^31).
 // ---------------------------------------------------------------------------------
-struct Pool {
-    int64_t n, N, W;
-    int c0;  // first CTA of the pool in the grid
-    int C;
+struct Pool32 {
+    int n, qN, rN, W;
 };
-__device__ __forceinline__ int64_t pool_a(const Pool &P, int64_t k) { return k * P.N / P.W; }
-__device__ __forceinline__ int64_t pool_warp_of(const Pool &P, int64_t x) {
-    const int64_t k = ((x + 1) * P.W - 1) / P.N;
-    return k < P.W - 1 ? k : P.W - 1;
-}
-// CTAs of the pool that hold items of sequence u (first via *first).
-__device__ __forceinline__ int pool_ctas(const Pool &P, int wpc, int u, int *first) {
-    if (P.n == 0 || P.C == 0) {
-        *first = 0;
-        return 0;
-    }
-    const int f = (int)(pool_warp_of(P, (int64_t)u * P.n) / wpc);
-    const int l = (int)(pool_warp_of(P, (int64_t)(u + 1) * P.n - 1) / wpc);
-    *first = f;
-    return l - f + 1;
-}
-__device__ __forceinline__ int gen_ctas(const DecodeParams &p, int u, int *first) {
-    if (p.n_gc == 0) {
-        *first = 0;
-        return 0;
-    }
-    const int f = (int)(((int64_t)u * p.n_gc) / p.wpc);
-    const int l = (int)(((int64_t)(u + 1) * p.n_gc - 1) / p.wpc);
-    *first = f;
-    return l - f + 1;
+__device__ __forceinline__ int pool_a(const Pool32 &P, int k) {
+    return k * P.qN + (int)(((long long)k * P.rN) / P.W);
 }
 
 __device__ __forceinline__ void load_q_gen(const DecodeParams &p, int u, uint16_t *q_w) {
@@ -275,69 +251,76 @@ __device__ __forceinline__ void load_q_gen(const DecodeParams &p, int u, uint16_
     __syncwarp();
 }
 
-// Weight tables of the merge and combine phases: behind warp 0's partial in a fast
-// kernel (its slots are free once the tiles are done), else behind the warp regions.
-constexpr int kGenTabFloats = 7168;
-template <int BITS, bool KITTY, bool FAST, int NW>
-__host__ __device__ inline int tab_offset(const DecodeParams &p) {
-    if (FAST) return part_bytes(p.D);
-    return NW * gen_warp_bytes(p.D);
-}
-template <int BITS, bool KITTY, bool FAST>
-__host__ __device__ inline int tab_capacity(int n_boost, int D) {
-    if (FAST) return (WarpSmem<BITS>(KITTY, n_boost).total - part_bytes(D)) / 4;
-    return kGenTabFloats;
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *ptr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------------------------------
 // The kernel.  FAST: CTAs [0, C_f) fast warps, [C_f, C_f + C_m) mini warps.
-// Otherwise: generic warps only.
+// Otherwise: generic warps only, one chunk each.
+//
+// Epilogue, per sequence u that a CTA holds items of:
+//   1. merge: the CTA's warp partials of u (shared memory) -> one partial, written to
+//      slot s of u in global memory, s taken from a per-sequence slot counter;
+//   2. publish: one acquire-release atomic adds the CTA's item count of u to a
+//      per-sequence item counter; the CTA that completes the count of all items
+//      combines (no CTA ever waits for another);
+//   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
+//      CTA resets both counters to zero for the next call.
 // ---------------------------------------------------------------------------------
 template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_seg[NW][2];  // sequence of each warp segment (-1: none)
-    __shared__ int s_last[24];    // sequences this CTA must combine
+    __shared__ int s_seg[NW][2];   // sequence of each warp segment (-1: none)
+    __shared__ int s_cnt[NW][2];   // items of each warp segment
+    // a warp range holds at most two sequences, so a CTA holds at most 2 NW
+    __shared__ int s_slot[2 * NW]; // this CTA's slot in sequence ulo + i
+    __shared__ int s_lu[2 * NW];   // sequences this CTA combines
+    __shared__ int s_ns[2 * NW];   // their slot counts
+    __shared__ int s_nl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, D = p.D, g = p.g;
+    const int D = p.D, g = p.g;
     const int wbytes = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).total : gen_warp_bytes(D);
+    const int part0_off = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).part0 : 0;
     unsigned char *wbase = smem + warp * wbytes;
-    float *part = reinterpret_cast<float *>(wbase);  // the warp's last partial, [8][D+2]
-    int seg0 = -1, seg1 = -1;
-    const Pool PF{p.n_fast, p.N_f, (int64_t)p.wpc * p.C_f, 0, p.C_f};
-    const Pool PM{p.n_mini, p.N_m, (int64_t)p.wpc * p.C_m, p.C_f, p.C_m};
-    int pool = 2;  // 0 fast, 1 mini, 2 generic
-    if (FAST) pool = c < p.C_f ? 0 : 1;
+    int seg0 = -1, seg1 = -1, cnt0 = 0, cnt1 = 0;
 
     if (FAST) {
-        const Pool &P = pool == 0 ? PF : PM;
-        const int64_t k = (int64_t)(c - P.c0) * p.wpc + warp;
-        const int64_t x0 = pool_a(P, k), x1 = pool_a(P, k + 1);
-        // a warp range touches at most two sequences; a first segment followed by a
-        // second one is parked in global scratch, the last one stays in shared memory
-        int64_t x = x0;
-        int nseg = 0;
+        const bool fastpool = (int)blockIdx.x < p.C_f;
+        const Pool32 P = fastpool ? Pool32{(int)p.n_fast, p.qN_f, p.rN_f, p.W_f}
+                                  : Pool32{(int)p.n_mini, p.qN_m, p.rN_m, p.W_m};
+        const int k = ((int)blockIdx.x - (fastpool ? 0 : p.C_f)) * p.wpc + warp;
+        int x = pool_a(P, k);
+        const int x1 = pool_a(P, k + 1);
+        // a warp range touches at most two sequences; the first of two segments keeps
+        // its partial in the warp's part0 area, the last one in the (then idle) slots
         FastWarp<BITS, KITTY> fw(p, wbase);
         MiniWarp<BITS, KITTY> mw(p, wbase, 0);
         if (x < x1) {
-            if (pool == 0) fw.init_bars();
+            if (fastpool) fw.init_bars();
             else mw.init_bars();
         }
-        while (x < x1 && nseg < 2) {
-            const int u = (int)(x / P.n);
-            const int64_t e = kvq_min64(x1, (int64_t)(u + 1) * P.n);
-            const bool more = e < x1;
-            float *dst = more ? p.scratch + ((size_t)c * NW + warp) * (part_bytes(D) / 4) : part;
-            if (pool == 0) fw.run(u, x - (int64_t)u * P.n, e - (int64_t)u * P.n, dst);
-            else mw.run(u, x - (int64_t)u * P.n, e - (int64_t)u * P.n, dst);
-            if (more) seg0 = u;
-            else seg1 = u;
-            x = e;
-            nseg++;
+        for (int e = 0; e < 2 && x < x1; e++) {
+            const int u = x / P.n;
+            const int end = min(x1, (u + 1) * P.n);
+            const bool more = end < x1;
+            float *dst = reinterpret_cast<float *>(wbase + (more ? part0_off : 0));
+            if (fastpool) fw.run(u, x - u * P.n, end - u * P.n, dst);
+            else mw.run(u, x - u * P.n, end - u * P.n, dst);
+            if (more) {
+                seg0 = u;
+                cnt0 = end - x;
+            } else {
+                seg1 = u;
+                cnt1 = end - x;
+            }
+            x = end;
         }
     } else {
         // ---- generic warp: one chunk of one sequence ----
-        const int64_t j = (int64_t)c * p.wpc + warp;
+        const int64_t j = (int64_t)blockIdx.x * p.wpc + warp;
         GenState<DPL> st;
 #pragma unroll
         for (int h = 0; h < 8; h++) {
@@ -353,22 +336,24 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             uint16_t *q_w = reinterpret_cast<uint16_t *>(wbase + part_bytes(D));
             load_q_gen(p, u, q_w);
             generic_range<DPL>(p, u, q_w, a, b, st);
-            generic_store<DPL>(p, st, part);
+            generic_store<DPL>(p, st, reinterpret_cast<float *>(wbase));
             seg1 = u;
+            cnt1 = 1;
         }
     }
     if (lane == 0) {
         s_seg[warp][0] = seg0;
         s_seg[warp][1] = seg1;
+        s_cnt[warp][0] = cnt0;
+        s_cnt[warp][1] = cnt1;
     }
     __syncthreads();
 
-    // ---- merge the warps of this CTA per sequence, publish, take a ticket ----
-    // Phase 1 (one thread per (sequence, head)): the running max over the warp
-    // partials of that sequence and each partial's weight exp2(m - M).  Phase 2: a
-    // flat loop over (sequence, head, channel) with independent loads.
+    // ---- the CTA's sequences: a contiguous run ulo..uhi (at most 2 NW), each with a segment ----
     int ulo = 0x7fffffff, uhi = -1;
+#pragma unroll
     for (int w = 0; w < NW; w++)
+#pragma unroll
         for (int e = 0; e < 2; e++)
             if (s_seg[w][e] >= 0) {
                 ulo = min(ulo, s_seg[w][e]);
@@ -376,140 +361,111 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             }
     if (uhi < 0) return;
     const int nu = uhi - ulo + 1;
-    if (nu > 24) {  // impossible with the host schedule; never index past s_last
+    if (nu > 2 * NW) {  // impossible with the host schedule; never index past the tables
         if (tid == 0) report(p.status, KVQ_DEV_BAD_STATE_BIT);
         return;
     }
-    const int wb = wbytes / 4;  // floats between warp partials in shared memory
-    const float *wpart = reinterpret_cast<const float *>(smem);
-    const int R = prow(D);
-    // weight tables (merge: [nu*g][2*NW] + [nu*g][2]; combine: [nl*g][max_slots]) in
-    // shared memory the tiles no longer use (host checks the capacity)
-    float *wtab = reinterpret_cast<float *>(smem + tab_offset<BITS, KITTY, FAST, NW>(p));
-    __shared__ int s_slot[24];
+    if (tid < nu) s_slot[tid] = atomicAdd(&p.slot_ctr[ulo + tid], 1);
+    __syncthreads();
+
+    // ---- merge: one float4 of (sequence, head, channels) per thread and step ----
+    const int R = prow(D), D4 = D / 4;
     auto src_of = [&](int w, int e) -> const float * {
-        return e == 0 ? p.scratch + ((size_t)c * NW + w) * (part_bytes(D) / 4) : wpart + w * wb;
+        return reinterpret_cast<const float *>(smem + w * wbytes + (e == 0 ? part0_off : 0));
     };
-    for (int pi = tid; pi < nu * g; pi += blockDim.x) {
-        const int u = ulo + pi / g, h = pi % g;
+    for (int i = tid; i < nu * g * D4; i += NW * 32) {
+        const int pi = i / D4, d = 4 * (i - pi * D4);
+        const int ul = pi / g, h = pi - ul * g, u = ulo + ul;
         float M = -INFINITY;
+#pragma unroll
         for (int w = 0; w < NW; w++)
+#pragma unroll
             for (int e = 0; e < 2; e++)
                 if (s_seg[w][e] == u) M = fmaxf(M, src_of(w, e)[h * R + D]);
         float L = 0.f;
-        for (int w = 0; w < NW; w++)
-            for (int e = 0; e < 2; e++) {
-                float f = 0.f;
-                if (s_seg[w][e] == u) {
-                    const float mw = src_of(w, e)[h * R + D];
-                    if (mw != -INFINITY) f = exp2f(mw - M);
-                    L = fmaf(src_of(w, e)[h * R + D + 1], f, L);
-                }
-                wtab[pi * 2 * NW + 2 * w + e] = f;
-            }
-        wtab[nu * g * 2 * NW + pi * 2] = M;
-        wtab[nu * g * 2 * NW + pi * 2 + 1] = L;
-        if (h == 0) {
-            int ff, fm, fg;
-            const int nf = pool_ctas(PF, p.wpc, u, &ff);
-            pool_ctas(PM, p.wpc, u, &fm);
-            if (!FAST) gen_ctas(p, u, &fg);
-            s_slot[u - ulo] = !FAST ? c - fg : (pool == 0 ? c - ff : nf + (c - p.C_f - fm));
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < nu * g * (D / 4); i += blockDim.x) {
-        const int pi = i / (D / 4), d = 4 * (i % (D / 4));
-        const int ul = pi / g, h = pi % g, u = ulo + ul;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
         for (int w = 0; w < NW; w++)
-            for (int e = 0; e < 2; e++) {
-                const float f = wtab[pi * 2 * NW + 2 * w + e];
-                if (f != 0.f) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src_of(w, e) + h * R + d);
+#pragma unroll
+            for (int e = 0; e < 2; e++)
+                if (s_seg[w][e] == u) {
+                    const float *s = src_of(w, e) + h * R;
+                    const float mw = s[D];
+                    const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                    L = fmaf(s[D + 1], f, L);
+                    const float4 v = *reinterpret_cast<const float4 *>(s + d);
                     acc.x = fmaf(v.x, f, acc.x);
                     acc.y = fmaf(v.y, f, acc.y);
                     acc.z = fmaf(v.z, f, acc.z);
                     acc.w = fmaf(v.w, f, acc.w);
                 }
-            }
-        float *gpart = p.partials + ((size_t)u * p.max_slots + s_slot[ul]) * g * R + h * R;
-        *reinterpret_cast<float4 *>(gpart + d) = acc;
-        if (d == 0) {
-            gpart[D] = wtab[nu * g * 2 * NW + pi * 2];
-            gpart[D + 1] = wtab[nu * g * 2 * NW + pi * 2 + 1];
+        const int slot = s_slot[ul];
+        if (slot < p.max_slots) {
+            float *gp = p.partials + (((size_t)u * p.max_slots + slot) * g + h) * R;
+            *reinterpret_cast<float4 *>(gp + d) = acc;
+            if (d == 0) *reinterpret_cast<float2 *>(gp + D) = make_float2(M, L);
+        } else if (d == 0) {
+            report(p.status, KVQ_DEV_BAD_STATE_BIT);
         }
     }
-    // Publish: the CTA barrier orders every thread's partial stores before the
-    // GPU-scope release fence of the ticket thread of each sequence; the acquire
-    // fence after the ticket orders the combine's reads of the other CTAs' slots.
+    // ---- publish: the barrier orders every thread's partial stores before the
+    // release of the item-counter atomic; its acquire orders the combine's reads ----
+    __syncthreads();
+    if (tid == 0) s_nl = 0;
     __syncthreads();
     if (tid < nu) {
         const int u = ulo + tid;
-        int f0;
-        const int n = pool_ctas(PF, p.wpc, u, &f0) + pool_ctas(PM, p.wpc, u, &f0) + (FAST ? 0 : gen_ctas(p, u, &f0));
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        s_last[tid] = (atomicAdd(&p.tickets[u], 1) == n - 1);
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    }
-    __syncthreads();
-
-    // ---- the last CTA of a sequence: log-sum-exp combine of its slots ----
-    // Phase 1 (one thread per (sequence, head)): weights w_c = exp2(m_c - M) / L of the
-    // slots; phase 2: out = sum_c w_c o_c over (sequence, head, channel).
-    __shared__ int s_lu[24];
-    if (tid == 0) {
-        int n = 0;
-        for (int k = 0; k < nu; k++)
-            if (s_last[k]) s_lu[n++] = ulo + k;
-    }
-    int nl = 0;
-    for (int k = 0; k < nu; k++) nl += s_last[k] ? 1 : 0;
-    __syncthreads();
-    if (nl == 0) return;
-    const int ms = p.max_slots;
-    float *ctab = wtab;  // [nl * g][ms] weights (phase 2 of the merge is done)
-    __shared__ int s_ns[24];
-    for (int pi = tid; pi < nl * g; pi += blockDim.x) {
-        const int u = s_lu[pi / g], h = pi % g;
-        int f0;
-        const int ns = pool_ctas(PF, p.wpc, u, &f0) + pool_ctas(PM, p.wpc, u, &f0) + (FAST ? 0 : gen_ctas(p, u, &f0));
-        if (h == 0) s_ns[pi / g] = ns;
-        const float *up = p.partials + (size_t)u * ms * g * R + h * R;
-        float M = -INFINITY;
-        for (int cc = 0; cc < ns; cc++) M = fmaxf(M, __ldcg(up + (size_t)cc * g * R + D));
-        float L = 0.f;
-        for (int cc = 0; cc < ns; cc++) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(up + (size_t)cc * g * R + D));
-            const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            L = fmaf(ml.y, f, L);
-            ctab[pi * ms + cc] = f;
+        int items = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w++)
+#pragma unroll
+            for (int e = 0; e < 2; e++)
+                if (s_seg[w][e] == u) items += s_cnt[w][e];
+        const int before = atom_add_acq_rel_gpu(&p.item_ctr[u], items);
+        if (before + items == p.n_items) {
+            const int k = atomicAdd(&s_nl, 1);
+            s_lu[k] = u;
+            s_ns[k] = *reinterpret_cast<volatile int32_t *>(&p.slot_ctr[u]);
         }
-        const float inv = 1.0f / L;
-        for (int cc = 0; cc < ns; cc++) ctab[pi * ms + cc] *= inv;
     }
     __syncthreads();
-    for (int i = tid; i < nl * g * (D / 4); i += blockDim.x) {
-        const int pi = i / (D / 4), d = 4 * (i % (D / 4));
-        const int u = s_lu[pi / g], h = pi % g, ns = s_ns[pi / g];
-        const float *up = p.partials + (size_t)u * ms * g * R + h * R + d;
+    const int nl = s_nl;
+    if (nl == 0) return;
+
+    // ---- combine: out = sum_c exp2(m_c - M) o_c / sum_c exp2(m_c - M) l_c ----
+    for (int i = tid; i < nl * g * D4; i += NW * 32) {
+        const int pi = i / D4, d = 4 * (i - pi * D4);
+        const int lk = pi / g, h = pi - lk * g, u = s_lu[lk];
+        const int ns = min(s_ns[lk], p.max_slots);
+        const float *up = p.partials + ((size_t)u * p.max_slots * g + h) * R;
+        const size_t cs = (size_t)g * R;  // floats between slots
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int c = 0; c < ns; c++) M = fmaxf(M, __ldcg(up + c * cs + D));
+        float L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int cc = 0; cc < ns; cc++) {
-            const float f = ctab[pi * ms + cc];
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(up + (size_t)cc * g * R));
+        for (int c = 0; c < ns; c++) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(up + c * cs + D));
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(up + c * cs + d));
+            const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            L = fmaf(ml.y, f, L);
             O.x = fmaf(v.x, f, O.x);
             O.y = fmaf(v.y, f, O.y);
             O.z = fmaf(v.z, f, O.z);
             O.w = fmaf(v.w, f, O.w);
         }
+        const float inv = 1.0f / L;
         uint2 hv;
-        hv.x = pack_half2(O.x, O.y);
-        hv.y = pack_half2(O.z, O.w);
+        hv.x = pack_half2(O.x * inv, O.y * inv);
+        hv.y = pack_half2(O.z * inv, O.w * inv);
         *reinterpret_cast<uint2 *>(p.out + ((size_t)u * g + h) * D + d) = hv;
     }
     __syncthreads();
-    if (tid < nl) p.tickets[s_lu[tid]] = 0;
+    if (tid < nl) {
+        p.slot_ctr[s_lu[tid]] = 0;
+        p.item_ctr[s_lu[tid]] = 0;
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -522,13 +478,7 @@ int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast) {
 size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast) {
     const int nw = decode_warps_per_cta(bits, kitty, n_boost, fast);
     if (fast) return (size_t)nw * (bits == 2 ? WarpSmem<2>(kitty, n_boost).total : WarpSmem<4>(kitty, n_boost).total);
-    return (size_t)nw * gen_warp_bytes(D) + kGenTabFloats * 4;
-}
-
-int decode_table_floats(int bits, bool kitty, int n_boost, int D, bool fast) {
-    if (!fast) return kGenTabFloats;
-    if (bits == 2) return kitty ? tab_capacity<2, true, true>(n_boost, D) : tab_capacity<2, false, true>(n_boost, D);
-    return tab_capacity<4, false, true>(n_boost, D);
+    return (size_t)nw * gen_warp_bytes(D);
 }
 
 template <int BITS, bool KITTY, bool FAST, int DPL, int NW>

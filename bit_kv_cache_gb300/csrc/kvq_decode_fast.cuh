@@ -76,10 +76,10 @@ __host__ __device__ inline int slot_bytes(bool kitty, int nb) {
 
 // Per-warp shared memory (fast and mini warps):
 //   [kSlots slots][p' buffer x2][q fp16 [4][128]][q' pairs [4 heads][8 slabs][4 lanes] x 8 B]
-//   [slot index 64 B][mbarriers kSlots x 8 B]
+//   [slot index 64 B][mbarriers kSlots x 8 B][first-segment partial [4][D+4] fp32]
 template <int BITS>
 struct WarpSmem {
-    int slot, pbuf, qraw, qpair, invb, bars, total;
+    int slot, pbuf, qraw, qpair, invb, bars, part0, total;
     __host__ __device__ WarpSmem(bool kitty, int nb) {
         slot = slot_bytes<BITS>(kitty, nb);
         pbuf = kSlots * slot;
@@ -87,7 +87,8 @@ struct WarpSmem {
         qpair = qraw + 4 * 128 * 2;
         invb = qpair + 4 * 8 * 4 * 8;
         bars = invb + 64;
-        total = (bars + 8 * kSlots + 127) & ~127;
+        part0 = (bars + 8 * kSlots + 15) & ~15;     // partial of a first segment: 4 head rows
+        total = (part0 + 4 * prow(128) * 4 + 127) & ~127;
     }
 };
 
@@ -114,17 +115,33 @@ __device__ __forceinline__ int chan_of(int sl, int t, int kk) {  // kk: 0..3 = k
     return 16 * sl + t + off[kk];
 }
 
-// Loads the g query heads of sequence u into the warp's buffers:
+// The g query heads of sequence u, 2 x 16 bytes per lane (heads >= g zero).  Loaded
+// before a warp issues its first tile copies so that they are not queued behind them.
+struct QRegs {
+    uint4 v[2];
+};
+__device__ __forceinline__ QRegs load_q_regs(const DecodeParams &p, int u) {
+    const int lane = threadIdx.x & 31;
+    QRegs r;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const int i = lane + 32 * j, h = i / 16, d = (i % 16) * 8;
+        r.v[j] = make_uint4(0, 0, 0, 0);
+        if (h < p.g) r.v[j] = __ldg(reinterpret_cast<const uint4 *>(p.q + ((size_t)u * p.g + h) * 128 + d));
+    }
+    return r;
+}
+
+// Stores the query into the warp's buffers:
 //   qraw[h][ch] = q (fp16), heads >= g zero;
 //   qpair[h][sl][t] = the two half2 (q * 2^-4) of lane t's channels in slab sl.
 template <int PS>
-__device__ void load_q_warp(const DecodeParams &p, int u, uint16_t *qraw, uint2 *qpair) {
+__device__ void store_q_warp(const QRegs &qr, uint16_t *qraw, uint2 *qpair) {
     const int lane = threadIdx.x & 31;
-    for (int i = lane; i < 4 * 128 / 8; i += 32) {
-        const int h = i / 16, d = (i % 16) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < p.g) v = *reinterpret_cast<const uint4 *>(p.q + ((size_t)u * p.g + h) * 128 + d);
-        *reinterpret_cast<uint4 *>(qraw + h * 128 + d) = v;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const int i = lane + 32 * j, h = i / 16, d = (i % 16) * 8;
+        *reinterpret_cast<uint4 *>(qraw + h * 128 + d) = qr.v[j];
     }
     __syncwarp();
     const uint32_t s4 = 0x2C002C00u;  // half2(2^-4, 2^-4)
@@ -453,16 +470,17 @@ struct FastWarp {
     __device__ void run(int uu, int64_t t0, int64_t t1, float *part) {
         u = uu;
         const int64_t n = t1 - t0;
-        // slots: K(i) -> 2(i&1), V(i) -> 2(i&1)+1; the first copies go out before the
-        // query is staged so that their latency overlaps it
+        // slots: K(i) -> 2(i&1), V(i) -> 2(i&1)+1; the query's loads go out first, then
+        // the first copies, whose latency overlaps staging the query
+        const QRegs qr = load_q_regs(p, u);
         issue_k(t0, 0);
         issue_v(t0, 1);
         if (n > 1) {
             issue_k(t0 + 1, 2);
             issue_v(t0 + 1, 3);
         }
-        load_q_warp<T::PS>(p, u, reinterpret_cast<uint16_t *>(wbase + L.qraw),
-                           reinterpret_cast<uint2 *>(wbase + L.qpair));
+        store_q_warp<T::PS>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw),
+                            reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb0 = reinterpret_cast<uint16_t *>(wbase + L.pbuf);
         for (int i = lane; i < 4 * T::PROW; i += 32)  // both p' buffers (2 x 4 rows)
             reinterpret_cast<uint32_t *>(pb0)[i] = 0u;
@@ -524,6 +542,7 @@ struct FastWarp {
     }
 
     // O row set o = set*NJ + j: rows g <-> channel FPI*(g+8 set) + j, g+8 <-> + FPI/2.
+    // Writes head rows 0..3 (columns 2t, 2t+1 of lanes t < 2) and m, l.
     __device__ void finish(float *part, float m, float l, float mn, const float (&O)[8][4]) const {
         const int gq = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -535,7 +554,7 @@ struct FastWarp {
         const float mn1 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t + 1) & 3));
         __syncwarp();
 #define KVQ_SO(J)                                                                  \
-    if (J < T::NJ) {                                                               \
+    if (J < T::NJ && t < 2) {                                                      \
         const float f = unscale<J>();                                              \
         for (int set = 0; set < T::NSET; set++) {                                  \
             const int o = set * T::NJ + (J % T::NJ);                               \
@@ -672,12 +691,13 @@ struct MiniWarp {
         const bool lo_col = (gq & 1) != 0;
         const int64_t n = m1 - m0;
         uint16_t *qraw = reinterpret_cast<uint16_t *>(wbase + L.qraw);
-        load_q_warp<8>(p, u, qraw, reinterpret_cast<uint2 *>(wbase + L.qpair));
+        const QRegs qr = load_q_regs(p, u);
+        issue(mini_tile(p, u_base(m0)), 0);
+        if (n > 1) issue(mini_tile(p, u_base(m0 + 1)), 2);
+        store_q_warp<8>(qr, qraw, reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb = reinterpret_cast<uint16_t *>(wbase + L.pbuf);  // [4][16] p
         for (int i = lane; i < 8 * 16; i += 32) pb[i] = 0;           // heads 4..7 stay zero
         __syncwarp();
-        issue(mini_tile(p, u_base(m0)), 0);
-        if (n > 1) issue(mini_tile(p, u_base(m0 + 1)), 2);
         float m = -INFINITY, l = 0.f;
         float O[8][4];
 #pragma unroll
@@ -818,13 +838,15 @@ struct MiniWarp {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         __syncwarp();
+        if (t < 2) {  // head rows 0..3
 #pragma unroll
-        for (int o = 0; o < 8; o++) {
-            const int ch = 16 * o + gq;
-            part[(2 * t) * 132 + ch] = O[o][0];
-            part[(2 * t + 1) * 132 + ch] = O[o][1];
-            part[(2 * t) * 132 + ch + 8] = O[o][2];
-            part[(2 * t + 1) * 132 + ch + 8] = O[o][3];
+            for (int o = 0; o < 8; o++) {
+                const int ch = 16 * o + gq;
+                part[(2 * t) * 132 + ch] = O[o][0];
+                part[(2 * t + 1) * 132 + ch] = O[o][1];
+                part[(2 * t) * 132 + ch + 8] = O[o][2];
+                part[(2 * t + 1) * 132 + ch + 8] = O[o][3];
+            }
         }
         if (gq == 0) {
             part[t * 132 + 128] = m;

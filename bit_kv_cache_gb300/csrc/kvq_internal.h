@@ -53,8 +53,8 @@ struct AppendParams {
 //               cover; then there are no fast or mini items).
 // Each kind has a pool of CTAs whose warps cut the sequence-major list of all
 // sequences' items into equal ranges; a range touches at most two sequences.
-// A CTA merges its warps' partial softmax states per sequence into one slot;
-// the last CTA of a sequence (ticket) combines the slots.
+// A CTA merges its warps' partial softmax states per sequence into one slot; the
+// CTA that completes a sequence's item count combines the slots.
 struct DecodeParams {
     // shape
     int B, H_kv, g, D, G, bits, Gv, n_boost, kitty;
@@ -72,13 +72,16 @@ struct DecodeParams {
     const uint16_t *q;
     uint16_t *out;
     float *partials;       // [U][max_slots][g][D + 4]
-    float *scratch;        // [CTAs][warps][8][D + 4] first-segment partials
-    int32_t *tickets;      // [U]
+    int32_t *slot_ctr;     // [U] slots taken (zero between calls)
+    int32_t *item_ctr;     // [U] items merged (zero between calls)
     int32_t *status;       // workspace status word
     // schedule
     int U, wpc;            // sequences, warps per CTA
     int C_f, C_m, C_g;     // CTAs of the fast, mini and generic pools (grid order)
     int n_gc, max_slots;
+    int n_items;           // items per sequence over all pools
+    int W_f, qN_f, rN_f;   // fast pool: warps, N_f / W_f, N_f % W_f
+    int W_m, qN_m, rN_m;   // mini pool: the same
     int tpp_shift, g_shift;  // log2(packed tiles per page), log2(G) (tile paths only)
     int64_t n_fast, N_f;   // fast tiles per sequence, in all
     int64_t n_mini, N_m;   // mini tiles per sequence, in all
@@ -95,6 +98,5 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
 size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast);
 int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast);
-int decode_table_floats(int bits, bool kitty, int n_boost, int D, bool fast);
 
 }  // namespace kvq
