@@ -237,6 +237,7 @@ struct Pool32 {
     int n, qN, rN, W;
 };
 __device__ __forceinline__ int pool_a(const Pool32 &P, int k) {
+    if (P.W < 46341) return k * P.qN + (int)((unsigned)(k * P.rN) / (unsigned)P.W);  // k * rN < W^2 < 2^31
     return k * P.qN + (int)(((long long)k * P.rN) / P.W);
 }
 
@@ -272,43 +273,77 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *ptr, int v) {
 // ---------------------------------------------------------------------------------
 template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
+    // Work units: in the tile kernels a unit is a warp pair (query warp, value warp)
+    // that shares one region of shared memory; in the generic kernel, one warp.
+    constexpr int NU = FAST ? NW / 2 : NW;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_seg[NW][2];   // sequence of each warp segment (-1: none)
-    __shared__ int s_cnt[NW][2];   // items of each warp segment
-    // a warp range holds at most two sequences, so a CTA holds at most 2 NW
-    __shared__ int s_slot[2 * NW]; // this CTA's slot in sequence ulo + i
-    __shared__ int s_lu[2 * NW];   // sequences this CTA combines
-    __shared__ int s_ns[2 * NW];   // their slot counts
+    __shared__ int s_seg[NU][2];   // sequence of each unit segment (-1: none)
+    __shared__ int s_cnt[NU][2];   // items of each unit segment
+    // a unit range holds at most two sequences, so a CTA holds at most 2 NU
+    __shared__ int s_slot[2 * NU]; // this CTA's slot in sequence ulo + i
+    __shared__ int s_lu[2 * NU];   // sequences this CTA combines
+    __shared__ int s_ns[2 * NU];   // their slot counts
     __shared__ int s_nl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = FAST ? warp >> 1 : warp, role = FAST ? warp & 1 : 0;
     const int D = p.D, g = p.g;
     const int wbytes = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).total : gen_warp_bytes(D);
     const int part0_off = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).part0 : 0;
-    unsigned char *wbase = smem + warp * wbytes;
+    unsigned char *wbase = smem + unit * wbytes;
     int seg0 = -1, seg1 = -1, cnt0 = 0, cnt1 = 0;
 
+    // The CTA's sequences ulo .. ulo + nu - 1 follow from its item range.  Their slots
+    // are taken now (lanes of warp 0); the atomics' latency hides behind the tiles.
+    const bool fastpool = FAST && (int)blockIdx.x < p.C_f;
+    const Pool32 P = fastpool ? Pool32{(int)p.n_fast, p.qN_f, p.rN_f, p.W_f}
+                              : Pool32{(int)p.n_mini, p.qN_m, p.rN_m, p.W_m};
+    const int kc = ((int)blockIdx.x - (fastpool ? 0 : p.C_f)) * p.wpc;
+    int ulo, nu;
+    {
+        int a0, a1, n;
+        if (FAST) {
+            a0 = pool_a(P, kc);
+            a1 = pool_a(P, kc + p.wpc);
+            n = P.n;
+        } else {
+            a0 = (int)blockIdx.x * p.wpc;
+            a1 = min(a0 + p.wpc, p.U * p.n_gc);
+            n = p.n_gc;
+        }
+        if (a1 <= a0) return;  // no items (never with the host schedule)
+        ulo = a0 / n;
+        nu = (a1 - 1) / n - ulo + 1;
+    }
+    if (nu > 2 * NU) {  // impossible with the host schedule; never index past the tables
+        if (tid == 0) report(p.status, KVQ_DEV_BAD_STATE_BIT);
+        return;
+    }
+    int my_slot = 0;
+    if (tid < nu) my_slot = atomicAdd(&p.slot_ctr[ulo + tid], 1);
+
     if (FAST) {
-        const bool fastpool = (int)blockIdx.x < p.C_f;
-        const Pool32 P = fastpool ? Pool32{(int)p.n_fast, p.qN_f, p.rN_f, p.W_f}
-                                  : Pool32{(int)p.n_mini, p.qN_m, p.rN_m, p.W_m};
-        const int k = ((int)blockIdx.x - (fastpool ? 0 : p.C_f)) * p.wpc + warp;
+        const int k = kc + unit;
         int x = pool_a(P, k);
         const int x1 = pool_a(P, k + 1);
-        // a warp range touches at most two sequences; the first of two segments keeps
-        // its partial in the warp's part0 area, the last one in the (then idle) slots
-        FastWarp<BITS, KITTY> fw(p, wbase);
+        // a unit range touches at most two sequences; the first of two segments keeps
+        // its partial in the unit's part0 area, the last one in the (then idle) tile region
+        PairWarp<BITS, KITTY> pw(p, wbase);
         MiniWarp<BITS, KITTY> mw(p, wbase, 0);
-        if (x < x1) {
-            if (fastpool) fw.init_bars();
-            else mw.init_bars();
-        }
+        if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
+        __syncthreads();
+        // mini units: the query warp of the pair runs the 16-token tiles alone
+        const bool active = fastpool || role == 0;
         for (int e = 0; e < 2 && x < x1; e++) {
             const int u = x / P.n;
             const int end = min(x1, (u + 1) * P.n);
             const bool more = end < x1;
             float *dst = reinterpret_cast<float *>(wbase + (more ? part0_off : 0));
-            if (fastpool) fw.run(u, x - u * P.n, end - u * P.n, dst);
-            else mw.run(u, x - u * P.n, end - u * P.n, dst);
+            if (fastpool) {
+                if (role == 0) pw.run_q(u, x - u * P.n, end - u * P.n);
+                else pw.run_p(u, x - u * P.n, end - u * P.n, dst);
+            } else if (active) {
+                mw.run(u, x - u * P.n, end - u * P.n, dst);
+            }
             if (more) {
                 seg0 = u;
                 cnt0 = end - x;
@@ -341,31 +376,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             cnt1 = 1;
         }
     }
-    if (lane == 0) {
-        s_seg[warp][0] = seg0;
-        s_seg[warp][1] = seg1;
-        s_cnt[warp][0] = cnt0;
-        s_cnt[warp][1] = cnt1;
+    if (lane == 0 && role == 0) {
+        s_seg[unit][0] = seg0;
+        s_seg[unit][1] = seg1;
+        s_cnt[unit][0] = cnt0;
+        s_cnt[unit][1] = cnt1;
     }
-    __syncthreads();
-
-    // ---- the CTA's sequences: a contiguous run ulo..uhi (at most 2 NW), each with a segment ----
-    int ulo = 0x7fffffff, uhi = -1;
-#pragma unroll
-    for (int w = 0; w < NW; w++)
-#pragma unroll
-        for (int e = 0; e < 2; e++)
-            if (s_seg[w][e] >= 0) {
-                ulo = min(ulo, s_seg[w][e]);
-                uhi = max(uhi, s_seg[w][e]);
-            }
-    if (uhi < 0) return;
-    const int nu = uhi - ulo + 1;
-    if (nu > 2 * NW) {  // impossible with the host schedule; never index past the tables
-        if (tid == 0) report(p.status, KVQ_DEV_BAD_STATE_BIT);
-        return;
-    }
-    if (tid < nu) s_slot[tid] = atomicAdd(&p.slot_ctr[ulo + tid], 1);
+    if (tid < nu) s_slot[tid] = my_slot;
     __syncthreads();
 
     // ---- merge: one float4 of (sequence, head, channels) per thread and step ----
@@ -378,14 +395,14 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int ul = pi / g, h = pi - ul * g, u = ulo + ul;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; w++)
+        for (int w = 0; w < NU; w++)
 #pragma unroll
             for (int e = 0; e < 2; e++)
                 if (s_seg[w][e] == u) M = fmaxf(M, src_of(w, e)[h * R + D]);
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < NW; w++)
+        for (int w = 0; w < NU; w++)
 #pragma unroll
             for (int e = 0; e < 2; e++)
                 if (s_seg[w][e] == u) {
@@ -417,7 +434,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int u = ulo + tid;
         int items = 0;
 #pragma unroll
-        for (int w = 0; w < NW; w++)
+        for (int w = 0; w < NU; w++)
 #pragma unroll
             for (int e = 0; e < 2; e++)
                 if (s_seg[w][e] == u) items += s_cnt[w][e];
@@ -439,21 +456,40 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int ns = min(s_ns[lk], p.max_slots);
         const float *up = p.partials + ((size_t)u * p.max_slots * g + h) * R;
         const size_t cs = (size_t)g * R;  // floats between slots
-        float M = -INFINITY;
-#pragma unroll 4
-        for (int c = 0; c < ns; c++) M = fmaxf(M, __ldcg(up + c * cs + D));
-        float L = 0.f;
+        // one pass with a running maximum, four slots at a time: their loads go out
+        // together, then the chunk's maximum rescales the running sums once
+        float M = -INFINITY, L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < ns; c++) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(up + c * cs + D));
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(up + c * cs + d));
-            const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            L = fmaf(ml.y, f, L);
-            O.x = fmaf(v.x, f, O.x);
-            O.y = fmaf(v.y, f, O.y);
-            O.z = fmaf(v.z, f, O.z);
-            O.w = fmaf(v.w, f, O.w);
+        for (int c0 = 0; c0 < ns; c0 += 4) {
+            float2 ml[4];
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                ml[j] = make_float2(-INFINITY, 0.f);
+                v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c0 + j < ns) {
+                    ml[j] = __ldcg(reinterpret_cast<const float2 *>(up + (c0 + j) * cs + D));
+                    v[j] = __ldcg(reinterpret_cast<const float4 *>(up + (c0 + j) * cs + d));
+                }
+            }
+            const float Mn = fmaxf(fmaxf(M, fmaxf(ml[0].x, ml[1].x)), fmaxf(ml[2].x, ml[3].x));
+            if (Mn == -INFINITY) continue;
+            const float r = M == -INFINITY ? 0.f : exp2f(M - Mn);
+            L *= r;
+            O.x *= r;
+            O.y *= r;
+            O.z *= r;
+            O.w *= r;
+            M = Mn;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float f = ml[j].x == -INFINITY ? 0.f : exp2f(ml[j].x - M);
+                L = fmaf(ml[j].y, f, L);
+                O.x = fmaf(v[j].x, f, O.x);
+                O.y = fmaf(v[j].y, f, O.y);
+                O.z = fmaf(v[j].z, f, O.z);
+                O.w = fmaf(v[j].w, f, O.w);
+            }
         }
         const float inv = 1.0f / L;
         uint2 hv;
@@ -504,13 +540,13 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st) {
-    if (fast) {
+    if (fast) {  // p.wpc units of two warps
         if (p.kitty) {
-            if (p.wpc == 8) return launch_one<2, true, true, 4, 8>(p, st);
-            return launch_one<2, true, true, 4, 6>(p, st);
+            if (p.wpc == 8) return launch_one<2, true, true, 4, 16>(p, st);
+            return launch_one<2, true, true, 4, 12>(p, st);
         }
-        if (p.bits == 2) return launch_one<2, false, true, 4, 8>(p, st);
-        return launch_one<4, false, true, 4, 8>(p, st);
+        if (p.bits == 2) return launch_one<2, false, true, 4, 16>(p, st);
+        return launch_one<4, false, true, 4, 16>(p, st);
     }
     switch (p.D) {
         case 64: return launch_one<2, false, false, 2, 8>(p, st);

@@ -27,7 +27,8 @@ namespace kvq {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kQScale = 0.0625f;  // q is folded as q * 2^-4 (exact) to keep q*scale in fp16 range
-constexpr int kSlots = 4;           // per-warp ring: K(i), V(i), K(i+1), V(i+1)
+constexpr int kSlots = 4;           // copy mbarriers per unit (fast: 2 key halves, 2 value halves)
+constexpr int kBars = 9;            // + warp-pair handoff: p' full x2, p' empty x2, query side done
 
 __host__ __device__ inline int hi_stride(int nb) { return nb * 4 + 16; }
 // A warp / CTA partial: 8 head rows of prow(D) floats: o[0..D), m at D, l at D+1
@@ -65,30 +66,40 @@ struct Tile {
 constexpr int kMiniRow = 128 * 2 + 16;                 // padded fp16 row of the mini tiles
 constexpr int kMiniHalf = 16 * kMiniRow;               // 16 fp16 rows
 
-template <int BITS>
-__host__ __device__ inline int slot_bytes(bool kitty, int nb) {
-    using T = Tile<BITS>;
-    int k = T::OFF_HI + (kitty ? 8 * hi_stride(nb) + T::D : 0);
-    int s = k > T::V_HALF ? k : T::V_HALF;
-    s = s > kMiniHalf ? s : kMiniHalf;
-    return (s + 127) & ~127;
-}
+__host__ __device__ constexpr int round128(int x) { return (x + 127) & ~127; }
 
-// Per-warp shared memory (fast and mini warps):
-//   [kSlots slots][p' buffer x2][q fp16 [4][128]][q' pairs [4 heads][8 slabs][4 lanes] x 8 B]
-//   [slot index 64 B][mbarriers kSlots x 8 B][first-segment partial [4][D+4] fp32]
+// Per-warp shared memory (fast and mini warps share one layout):
+//   [tile region][p' buffer x2][q fp16 [4][128]][q' pairs [4 heads][8 slabs][4 lanes] x 8 B]
+//   [slot index 64 B][mbarriers kBars x 8 B][pair handoff: stats [3][4], alpha [2][4] fp32]
+//   [first-segment partial [4][D+4] fp32]
+// The tile region holds, for a fast warp, two key halves (codes + (scale, min) per
+// channel [+ Kitty planes]), two value-code halves and two value (scale, min) rows;
+// for a mini warp, four 16-row halves.  After the tiles it holds the warp's partial.
 template <int BITS>
 struct WarpSmem {
-    int slot, pbuf, qraw, qpair, invb, bars, part0, total;
+    int ksz, vsz, vmsz, mslot, k0, v0, vm0, region;
+    int pbuf, qraw, qpair, invb, bars, stats, alpha, part0, total;
     __host__ __device__ WarpSmem(bool kitty, int nb) {
-        slot = slot_bytes<BITS>(kitty, nb);
-        pbuf = kSlots * slot;
-        qraw = pbuf + 2 * Tile<BITS>::PBUF;
+        using T = Tile<BITS>;
+        ksz = round128(T::OFF_HI + (kitty ? 8 * hi_stride(nb) + T::D : 0));
+        vsz = round128(T::V_ROWS * T::V_STRIDE);
+        vmsz = round128(T::TOK * 4);
+        const int mk = 1024 + ((4 * nb + 15) & ~15) + 128;  // mini packed-key block
+        mslot = round128(kMiniHalf > mk ? kMiniHalf : mk);
+        k0 = 0;
+        v0 = 2 * ksz;
+        vm0 = v0 + 2 * vsz;
+        region = vm0 + 2 * vmsz;
+        if (region < kSlots * mslot) region = kSlots * mslot;
+        pbuf = region;
+        qraw = pbuf + 2 * T::PBUF;
         qpair = qraw + 4 * 128 * 2;
         invb = qpair + 4 * 8 * 4 * 8;
         bars = invb + 64;
-        part0 = (bars + 8 * kSlots + 15) & ~15;     // partial of a first segment: 4 head rows
-        total = (part0 + 4 * prow(128) * 4 + 127) & ~127;
+        stats = bars + 8 * 16;                      // m, l, mn of 4 heads
+        alpha = stats + 12 * 4;                     // per p' buffer: rescale of 4 heads (+4 unused = 1)
+        part0 = (alpha + 8 * 4 * 2 + 15) & ~15;     // partial of a first segment: 4 head rows
+        total = round128(part0 + 4 * prow(128) * 4);
     }
 };
 
@@ -156,24 +167,32 @@ __device__ void store_q_warp(const QRegs &qr, uint16_t *qraw, uint2 *qpair) {
     __syncwarp();
 }
 
+// The QK B operand column of a lane: column 2h carries the fp16 hi part of head h's
+// folded query, column 2h+1 the lo part.
+struct ColConst {
+    bool lo;
+};
+__device__ __forceinline__ ColConst col_const(bool lo_col) { return ColConst{lo_col}; }
+
 // B operands of one 16-channel slab from the page's (scale, min) words kmA..kmD of
-// channels chan_of(sl, t, 0..3): the folded query (hi or lo part by column parity)
-// and q * 2^-4 for the min mma (zero in lo columns); A operand of the min mma.
+// channels chan_of(sl, t, 0..3): the folded query (hi or lo part by column) and
+// q * 2^-4 for the min mma (zero in lo columns); A operand of the min mma.
+//   hi column: t = fl16(q s);  lo column: fl16(q s - t), exact (fused)
 struct SlabB {
     uint32_t b0, b1, c0, c1, am0, am1;
 };
 __device__ __forceinline__ SlabB slab_b(uint2 qp, uint32_t kmA, uint32_t kmB, uint32_t kmC, uint32_t kmD,
-                                        bool lo_col) {
+                                        const ColConst &cc) {
     SlabB r;
     const uint32_t s01 = prmt(kmA, kmB, 0x5410), s23 = prmt(kmC, kmD, 0x5410);
-    const uint32_t hi01 = hmul2(qp.x, s01), hi23 = hmul2(qp.y, s23);
-    if (lo_col) {
-        r.b0 = hfma2(qp.x, s01, hi01 ^ 0x80008000u);
-        r.b1 = hfma2(qp.y, s23, hi23 ^ 0x80008000u);
+    const uint32_t t01 = hmul2(qp.x, s01), t23 = hmul2(qp.y, s23);
+    if (cc.lo) {
+        r.b0 = hfma2(qp.x, s01, t01 ^ 0x80008000u);
+        r.b1 = hfma2(qp.y, s23, t23 ^ 0x80008000u);
         r.c0 = r.c1 = 0u;
     } else {
-        r.b0 = hi01;
-        r.b1 = hi23;
+        r.b0 = t01;
+        r.b1 = t23;
         r.c0 = qp.x;
         r.c1 = qp.y;
     }
@@ -204,11 +223,13 @@ struct FastWarp {
         : p(pp), wbase(wb), L(KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
         bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
     }
-    __device__ unsigned char *slot(int s) const { return wbase + s * L.slot; }
+    __device__ unsigned char *kslot(int s) const { return wbase + L.k0 + s * L.ksz; }
+    __device__ unsigned char *vslot(int s) const { return wbase + L.v0 + s * L.vsz; }
+    __device__ unsigned char *vmslot(int s) const { return wbase + L.vm0 + s * L.vmsz; }
 
     __device__ void init_bars() {
         if (lane == 0) {
-            for (int s = 0; s < kSlots; s++) mbar_init(&bars[s], 1);
+            for (int s = 0; s < kBars; s++) mbar_init(&bars[s], 1);
             fence_barrier_init();
         }
         __syncwarp();
@@ -221,12 +242,15 @@ struct FastWarp {
         return ok;
     }
 
-    // key half of tile ti -> slot s
-    __device__ void issue_k(int64_t ti, int s) {
+    // Batch K(j): key codes and (scale, min) of tile t0 + j -> key half j & 1, barrier
+    // j & 1; the first batch also brings the value (scale, min) of tile t0.
+    __device__ void issue_kb(int64_t t0, int j) {
+        const int s = j & 1;
+        const int64_t ti = t0 + j;
         pending |= 1u << s;
-        unsigned char *st = slot(s);
+        unsigned char *st = kslot(s);
         const int nb = KITTY ? p.n_boost : 0;
-        const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0);
+        const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + (j == 0 ? T::TOK * 4 : 0);
         if (lane == 0) mbar_arrive_expect_tx(&bars[s], bytes);
         __syncwarp();
         const int64_t page = ti >> p.tpp_shift;  // tiles per page: a power of two
@@ -237,31 +261,39 @@ struct FastWarp {
         } else if (i == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
                        &bars[s]);
-        } else if (KITTY && nb > 0 && i < 17) {
-            const int r = i - 9;
+        } else if (i == 9) {
+            if (j == 0)
+                issue_copy(vmslot(0), p.v_meta + ((size_t)u * p.max_T + ti * T::TOK) * 2, T::TOK * 4, &bars[s]);
+        } else if (KITTY && nb > 0 && i >= 10 && i < 18) {
+            const int r = i - 10;
             issue_copy(st + T::OFF_HI + r * hi_stride(nb),
                        p.k_hi + ((size_t)u * (p.max_T / 16) + ti * 8 + r) * nb, nb * 4, &bars[s]);
-        } else if (KITTY && i == 17) {
+        } else if (KITTY && i == 18) {
             issue_copy(st + T::OFF_HI + 8 * hi_stride(nb), p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * T::D,
                        T::D, &bars[s]);
         }
     }
 
-    // value half of tile ti -> slot s
-    __device__ void issue_v(int64_t ti, int s) {
+    // Batch V(j): value codes of tile t0 + j -> value half j & 1 and, if tile j + 1
+    // exists, its value (scale, min) -> value-meta row (j + 1) & 1; barrier 2 + (j & 1).
+    __device__ void issue_vb(int64_t t0, int j, int64_t n) {
+        const int s = 2 + (j & 1);
+        const int64_t ti = t0 + j;
+        const bool meta = j + 1 < n;
         pending |= 1u << s;
-        unsigned char *st = slot(s);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + T::TOK * 4);
+        unsigned char *st = vslot(j & 1);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
         __syncwarp();
-        const int64_t tok0 = ti * T::TOK, page = ti >> p.tpp_shift;
+        const int64_t page = ti >> p.tpp_shift;
         const int64_t off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
         const int i = lane;
         if (i < T::V_ROWS) {
-            issue_copy(st + T::OFF_V + i * T::V_STRIDE,
+            issue_copy(st + i * T::V_STRIDE,
                        p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * T::V_ROWS + i) * p.G + off, T::TOK * 4,
                        &bars[s]);
-        } else if (i == T::V_ROWS) {
-            issue_copy(st + T::OFF_VM, p.v_meta + ((size_t)u * p.max_T + tok0) * 2, T::TOK * 4, &bars[s]);
+        } else if (i == T::V_ROWS && meta) {
+            issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)u * p.max_T + (ti + 1) * T::TOK) * 2, T::TOK * 4,
+                       &bars[s]);
         }
     }
 
@@ -324,7 +356,7 @@ struct FastWarp {
         const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
         const uint2 qp = reinterpret_cast<const uint2 *>(wbase + L.qpair)[((gq >> 1) * 8 + sl) * 4 + t];
         const SlabB b = slab_b(qp, km[chan_of<T::PS>(sl, t, 0)], km[chan_of<T::PS>(sl, t, 1)],
-                               km[chan_of<T::PS>(sl, t, 2)], km[chan_of<T::PS>(sl, t, 3)], (gq & 1) != 0);
+                               km[chan_of<T::PS>(sl, t, 2)], km[chan_of<T::PS>(sl, t, 3)], col_const((gq & 1) != 0));
         mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
         uint32_t w[4], x[4], xs[4];
         ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3) + 64 * sl);
@@ -362,7 +394,7 @@ struct FastWarp {
             q2[1] = hmul2((uint32_t)qv[2] | ((uint32_t)qv[3] << 16), 0x2C002C00u);
             q2[0] = hmul2(q2[0], s4);
             q2[1] = hmul2(q2[1], s4);
-            const SlabB b = slab_b(make_uint2(q2[0], q2[1]), km4[0], km4[1], km4[2], km4[3], (gq & 1) != 0);
+            const SlabB b = slab_b(make_uint2(q2[0], q2[1]), km4[0], km4[1], km4[2], km4[3], col_const((gq & 1) != 0));
             uint32_t w[4], x[4], xs[4];
             ldmatrix_x4(w, hb + 64 * s2);
             split(w, x, xs);
@@ -379,19 +411,30 @@ struct FastWarp {
         uint2 bp = make_uint2(0u, 0u);
         if (gq < 4) bp = *reinterpret_cast<const uint2 *>(pb + gq * T::PROW + 16 * sl + 4 * t);
         uint32_t w[4], x[4], xs[4];
-        ldmatrix_x4(w, smem_u32(st + T::OFF_V) + (set * 8 + (lane & 7)) * T::V_STRIDE + 16 * (lane >> 3) + 64 * sl);
+        ldmatrix_x4(w, smem_u32(st) + (set * 8 + (lane & 7)) * T::V_STRIDE + 16 * (lane >> 3) + 64 * sl);
         split(w, x, xs);
         mma_sets_o(O, set, x, xs, bp.x, bp.y);
     }
 
-    // Softmax of a tile from its S accumulators; rescales O; writes p' to pb.
-    __device__ __forceinline__ void softmax(const float (&acc)[T::NJ][4], const float (&cm)[4],
-                                            const unsigned char *stv, uint16_t *pb, float &m, float &l,
-                                            float &mn, float (&O)[8][4]) const {
-        const int gq = lane >> 2, t = lane & 3;
+    // Softmax of a tile, first part: logits z (log2 units) from the S accumulators,
+    // the new running maximum, l and mn rescaled to it.  Returns the factors by which
+    // O must be rescaled once the previous tile's PV is in (a0 / a1: columns 2t /
+    // 2t+1); *grow tells whether any head's maximum rose.
+    __device__ __forceinline__ void softmax_begin(const float (&acc)[T::NJ][4], const float (&cm)[4],
+                                                  float (&z)[T::NJ][2], float &m, float &l, float &mn,
+                                                  float &a0, float &a1, bool &grow) const {
+        float a;
+        softmax_begin_a(acc, cm, z, m, l, mn, a, grow);
+        const int t = lane & 3;
+        a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
+        a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
+    }
+    // The same; `a` is the rescale factor of the lane's head (lane & 3).
+    __device__ __forceinline__ void softmax_begin_a(const float (&acc)[T::NJ][4], const float (&cm)[4],
+                                                    float (&z)[T::NJ][2], float &m, float &l, float &mn,
+                                                    float &a, bool &grow) const {
         const float C = kLog2e * rsqrtf((float)T::D) / kQScale;
         const float cst = cm[0] * C;  // row g, column 2t: sum_d q_d min_d of head t
-        float z[T::NJ][2];
         float tm = -INFINITY;
 #define KVQ_Z(J)                                                                        \
     if (J < T::NJ) {                                                                    \
@@ -405,55 +448,27 @@ struct FastWarp {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
         const float nm = fmaxf(m, tm);
-        const float a = exp2f(m - nm);
+        a = exp2f(m - nm);  // 0 while m is -inf
+        grow = __any_sync(0xffffffffu, nm > m);
         m = nm;
         l *= a;
         mn *= a;
-        const float a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
-        const float a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
-#pragma unroll
-        for (int o = 0; o < 8; o++) {
-            O[o][0] *= a0;
-            O[o][2] *= a0;
-            O[o][1] *= a1;
-            O[o][3] *= a1;
-        }
+    }
+
+    // Softmax of a tile, row set j: p = exp2(z - m) of the lane's two tokens, their
+    // sums, and p' = p * scale_v into the tile's p' buffer.
+    __device__ __forceinline__ void softmax_chunk(int j, const float (&z)[T::NJ][2], const unsigned char *vms,
+                                                  uint16_t *pb, float m, float &l, float &mn) const {
+        const int gq = lane >> 2, t = lane & 3;
         // value (scale, min) of the lane's tokens: 2 bits 16g..16g+15, 4 bits 8g..8g+7
-        const uint32_t *vm = reinterpret_cast<const uint32_t *>(stv + T::OFF_VM);
-        uint32_t vmr[16];
-        if (BITS == 2) {
-            const uint4 *v4 = reinterpret_cast<const uint4 *>(vm + 16 * gq);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const uint4 x = v4[i];
-                vmr[4 * i] = x.x;
-                vmr[4 * i + 1] = x.y;
-                vmr[4 * i + 2] = x.z;
-                vmr[4 * i + 3] = x.w;
-            }
-        } else {
-            const uint4 *v4 = reinterpret_cast<const uint4 *>(vm + 8 * gq);
-#pragma unroll
-            for (int i = 0; i < 2; i++) {
-                const uint4 x = v4[i];
-                vmr[4 * i] = x.x;
-                vmr[4 * i + 1] = x.y;
-                vmr[4 * i + 2] = x.z;
-                vmr[4 * i + 3] = x.w;
-            }
-        }
-        uint16_t *row = pb + t * T::PROW;
-#pragma unroll
-        for (int j = 0; j < T::NJ; j++) {
-            // rows g and g+8 of row set j: tokens (16g+j, 16g+j+8) or (8g+j, 8g+j+4)
-            const int i0 = BITS == 2 ? j : j, i1 = BITS == 2 ? j + 8 : j + 4;
-            const float2 sm0 = unpack_half2(vmr[i0]), sm1 = unpack_half2(vmr[i1]);
-            const float p0 = exp2f(z[j][0] - m), p1 = exp2f(z[j][1] - m);
-            l += p0 + p1;
-            mn = fmaf(p0, sm0.y, fmaf(p1, sm1.y, mn));
-            const int pos = BITS == 2 ? 16 * gq + 4 * (j & 3) + 2 * (j >> 2) : 16 * (gq >> 1) + 4 * j + 2 * (gq & 1);
-            *reinterpret_cast<uint32_t *>(row + pos) = pack_half2(p0 * sm0.x, p1 * sm1.x);
-        }
+        const uint32_t *vm = reinterpret_cast<const uint32_t *>(vms) + (BITS == 2 ? 16 : 8) * gq;
+        const int i0 = j, i1 = BITS == 2 ? j + 8 : j + 4;  // tokens of rows g and g+8 of row set j
+        const float2 sm0 = unpack_half2(vm[i0]), sm1 = unpack_half2(vm[i1]);
+        const float p0 = exp2f(z[j][0] - m), p1 = exp2f(z[j][1] - m);
+        l += p0 + p1;
+        mn = fmaf(p0, sm0.y, fmaf(p1, sm1.y, mn));
+        const int pos = BITS == 2 ? 16 * gq + 4 * (j & 3) + 2 * (j >> 2) : 16 * (gq >> 1) + 4 * j + 2 * (gq & 1);
+        *reinterpret_cast<uint32_t *>(pb + t * T::PROW + pos) = pack_half2(p0 * sm0.x, p1 * sm1.x);
     }
 
     __device__ __forceinline__ void zero(float (&a)[T::NJ][4], float (&cm)[4]) const {
@@ -465,20 +480,21 @@ struct FastWarp {
         for (int e = 0; e < 4; e++) cm[e] = 0.f;
     }
 
-    // Tiles [t0, t1) of sequence uu; writes the warp's partial [8][D+2] to `part`.
-    // Software pipeline: PV of tile i runs interleaved with QK of tile i+1.
+    // Tiles [t0, t1) of sequence uu; writes the warp's partial [4][D+4] to `part`.
+    // Software pipeline, iteration i: PV of tile i interleaved slab by slab with QK of
+    // tile i+1, then the softmax of tile i+1 (its p' goes to the other p' buffer; O is
+    // rescaled only if a head's running maximum rose).
+    // Copies: batch K(j) = key codes + (scale, min) of tile j -> key half j&1 (barrier
+    // j&1); batch V(j) = value codes of j + value (scale, min) of j+1 -> value half
+    // j&1, meta row (j+1)&1 (barrier 2 + j&1).  Both are issued two tiles ahead, each
+    // into a buffer whose previous contents the warp has just finished reading.
     __device__ void run(int uu, int64_t t0, int64_t t1, float *part) {
         u = uu;
         const int64_t n = t1 - t0;
-        // slots: K(i) -> 2(i&1), V(i) -> 2(i&1)+1; the query's loads go out first, then
-        // the first copies, whose latency overlaps staging the query
-        const QRegs qr = load_q_regs(p, u);
-        issue_k(t0, 0);
-        issue_v(t0, 1);
-        if (n > 1) {
-            issue_k(t0 + 1, 2);
-            issue_v(t0 + 1, 3);
-        }
+        const QRegs qr = load_q_regs(p, u);  // its loads go out before the first copies
+        issue_kb(t0, 0);
+        issue_vb(t0, 0, n);
+        if (n > 1) issue_kb(t0, 1);
         store_q_warp<T::PS>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw),
                             reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb0 = reinterpret_cast<uint16_t *>(wbase + L.pbuf);
@@ -492,46 +508,67 @@ struct FastWarp {
 #pragma unroll
             for (int e = 0; e < 4; e++) O[o][e] = 0.f;
         float acc[T::NJ][4], cm[4];
+        float z[T::NJ][2];
         bool ok = true;
 
-        // prologue: QK(0), softmax(0)
+        // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
         ok &= wait_slot(0);
         zero(acc, cm);
 #pragma unroll
-        for (int sl = 0; sl < 8; sl++) qk_slab(sl, slot(0), acc, cm);
-        if (KITTY && p.n_boost > 0) qk_boost(slot(0), acc);
+        for (int sl = 0; sl < 8; sl++) qk_slab(sl, kslot(0), acc, cm);
+        if (KITTY && p.n_boost > 0) qk_boost(kslot(0), acc);
+        {
+            float a0, a1;
+            bool grow;
+            softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
+#pragma unroll
+            for (int j = 0; j < T::NJ; j++) softmax_chunk(j, z, vmslot(0), pb0, m, l, mn);
+        }
         __syncwarp();
         fence_proxy_async();
-        if (n > 2) issue_k(t0 + 2, 0);
-        ok &= wait_slot(1);
-        softmax(acc, cm, slot(1), pb0, m, l, mn, O);
-        __syncwarp();
+        if (n > 2) issue_kb(t0, 2);
+        if (n > 1) issue_vb(t0, 1, n);  // its (scale, min) of tile 2 reuses meta row 0: after softmax(0)
 
         for (int64_t i = 0; i < n && ok; i++) {
-            const int kv = 2 * (int)(i & 1), kn = 2 * (int)((i + 1) & 1);
-            const uint16_t *pb = pb0 + (i & 1) * 4 * T::PROW;
-            if (i + 1 < n) {
-                ok &= wait_slot(kn);
+            const int cur = (int)(i & 1), nxt = cur ^ 1;
+            const bool more = i + 1 < n;
+            if (more) ok &= wait_slot(nxt);  // K(i+1)
+            ok &= wait_slot(2 + cur);        // V(i): codes of i, (scale, min) of i+1
+            if (!ok) break;
+            const uint16_t *pb = pb0 + cur * 4 * T::PROW;
+            if (more) {
                 zero(acc, cm);
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
-                    pv_step(sl, slot(kv + 1), pb, O);
-                    qk_slab(sl, slot(kn), acc, cm);
+                    pv_step(sl, vslot(cur), pb, O);
+                    qk_slab(sl, kslot(nxt), acc, cm);
                 }
-                if (KITTY && p.n_boost > 0) qk_boost(slot(kn), acc);
+                if (KITTY && p.n_boost > 0) qk_boost(kslot(nxt), acc);
             } else {
 #pragma unroll
-                for (int sl = 0; sl < 8; sl++) pv_step(sl, slot(kv + 1), pb, O);
+                for (int sl = 0; sl < 8; sl++) pv_step(sl, vslot(cur), pb, O);
+            }
+            if (more) {
+                float a0, a1;
+                bool grow;
+                softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
+                if (grow) {  // O holds tiles <= i relative to the previous maximum
+#pragma unroll
+                    for (int o = 0; o < 8; o++) {
+                        O[o][0] *= a0;
+                        O[o][2] *= a0;
+                        O[o][1] *= a1;
+                        O[o][3] *= a1;
+                    }
+                }
+                uint16_t *pbn = pb0 + nxt * 4 * T::PROW;
+#pragma unroll
+                for (int j = 0; j < T::NJ; j++) softmax_chunk(j, z, vmslot(nxt), pbn, m, l, mn);
             }
             __syncwarp();
             fence_proxy_async();
-            if (i + 2 < n) issue_v(t0 + i + 2, kv + 1);
-            if (i + 1 < n) {
-                if (i + 3 < n) issue_k(t0 + i + 3, kn);
-                ok &= wait_slot(kn + 1);
-                softmax(acc, cm, slot(kn + 1), pb0 + ((i + 1) & 1) * 4 * T::PROW, m, l, mn, O);
-                __syncwarp();
-            }
+            if (i + 3 < n) issue_kb(t0, (int)i + 3);     // key half (i+1)&1 is free
+            if (i + 2 < n) issue_vb(t0, (int)i + 2, n);  // value half i&1, meta row (i+1)&1
         }
         if (!ok) {
             // let copies still in flight land before the shared memory is reused
@@ -572,6 +609,204 @@ struct FastWarp {
             part[t * (T::D + 4) + T::D] = m;
             part[t * (T::D + 4) + T::D + 1] = l;
         }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Packed tiles on a warp pair.  The query warp streams the key halves and the value
+// (scale, min) rows, computes QK and the softmax, and hands each tile's p' and the
+// per-head rescale factor to the value warp through shared memory; the value warp
+// streams the value codes, rescales O and runs PV.  Handoff per p' buffer b:
+// "full" (query -> value) and "empty" (value -> query) mbarriers, waits bounded.
+// ---------------------------------------------------------------------------
+template <int BITS, bool KITTY>
+struct PairWarp : FastWarp<BITS, KITTY> {
+    using Base = FastWarp<BITS, KITTY>;
+    using T = typename Base::T;
+    static constexpr int B_FULL = 4, B_EMPTY = 6, B_QDONE = 8;
+
+    __device__ PairWarp(const DecodeParams &pp, unsigned char *ub) : Base(pp, ub) {}
+
+    __device__ void arrive(int s) {
+        __syncwarp();
+        if (this->lane == 0) mbar_arrive(&this->bars[s]);
+        __syncwarp();
+    }
+    __device__ float *stats() const { return reinterpret_cast<float *>(this->wbase + this->L.stats); }
+    __device__ float *alpha() const { return reinterpret_cast<float *>(this->wbase + this->L.alpha); }
+    __device__ uint16_t *pbuf(int b) const {
+        return reinterpret_cast<uint16_t *>(this->wbase + this->L.pbuf) + b * 4 * T::PROW;
+    }
+
+    // Batch K(j): key codes, key (scale, min), value (scale, min) of tile t0 + j ->
+    // key half j&1 and meta row j&1; barrier j&1.
+    __device__ void issue_kq(int64_t t0, int j) {
+        const DecodeParams &p = this->p;
+        const int s = j & 1, lane = this->lane;
+        const int64_t ti = t0 + j;
+        this->pending |= 1u << s;
+        unsigned char *st = this->kslot(s);
+        const int nb = KITTY ? p.n_boost : 0;
+        const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + T::TOK * 4;
+        if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], bytes);
+        __syncwarp();
+        const int64_t page = ti >> p.tpp_shift;
+        const int u = this->u;
+        if (lane < 8) {
+            issue_copy(st + T::OFF_K + lane * T::K_STRIDE,
+                       p.k_codes + ((size_t)u * (p.max_T / T::FPI) + ti * 8 + lane) * T::D, T::D * 4,
+                       &this->bars[s]);
+        } else if (lane == 8) {
+            issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
+                       &this->bars[s]);
+        } else if (lane == 9) {
+            issue_copy(this->vmslot(s), p.v_meta + ((size_t)u * p.max_T + ti * T::TOK) * 2, T::TOK * 4,
+                       &this->bars[s]);
+        } else if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
+            const int r = lane - 10;
+            issue_copy(st + T::OFF_HI + r * hi_stride(nb),
+                       p.k_hi + ((size_t)u * (p.max_T / 16) + ti * 8 + r) * nb, nb * 4, &this->bars[s]);
+        } else if (KITTY && lane == 18) {
+            issue_copy(st + T::OFF_HI + 8 * hi_stride(nb),
+                       p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * T::D, T::D, &this->bars[s]);
+        }
+    }
+
+    // Batch V(j): value codes of tile t0 + j -> value half j&1; barrier 2 + j&1.
+    __device__ void issue_vp(int64_t t0, int j) {
+        const DecodeParams &p = this->p;
+        const int s = 2 + (j & 1), lane = this->lane;
+        const int64_t ti = t0 + j;
+        this->pending |= 1u << s;
+        unsigned char *st = this->vslot(j & 1);
+        if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], T::V_ROWS * T::TOK * 4);
+        __syncwarp();
+        const int64_t page = ti >> p.tpp_shift;
+        const int64_t off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
+        if (lane < T::V_ROWS)
+            issue_copy(st + lane * T::V_STRIDE,
+                       p.v_codes + (((size_t)this->u * (p.max_T / p.G) + page) * T::V_ROWS + lane) * p.G + off,
+                       T::TOK * 4, &this->bars[s]);
+    }
+
+    __device__ void drain(uint32_t mask) {  // copies still in flight land before smem reuse
+        for (int s = 0; s < kSlots; s++)
+            if ((this->pending & mask) & (1u << s)) this->wait_slot(s);
+    }
+
+    // Query warp over tiles [t0, t1) of sequence uu.
+    __device__ void run_q(int uu, int64_t t0, int64_t t1) {
+        this->u = uu;
+        const int lane = this->lane;
+        const int64_t n = t1 - t0;
+        const QRegs qr = load_q_regs(this->p, uu);
+        issue_kq(t0, 0);
+        if (n > 1) issue_kq(t0, 1);
+        store_q_warp<T::PS>(qr, reinterpret_cast<uint16_t *>(this->wbase + this->L.qraw),
+                            reinterpret_cast<uint2 *>(this->wbase + this->L.qpair));
+        float m = -INFINITY, l = 0.f, mn = 0.f;
+        float acc[T::NJ][4], cm[4], z[T::NJ][2];
+        bool ok = true;
+        for (int64_t j = 0; j < n && ok; j++) {
+            const int s = (int)(j & 1);
+            ok &= this->wait_slot(s);  // K(j)
+            if (!ok) break;
+            this->zero(acc, cm);
+#pragma unroll
+            for (int sl = 0; sl < 8; sl++) this->qk_slab(sl, this->kslot(s), acc, cm);
+            if (KITTY && this->p.n_boost > 0) this->qk_boost(this->kslot(s), acc);
+            float a;
+            bool grow;
+            this->softmax_begin_a(acc, cm, z, m, l, mn, a, grow);
+            if (j >= 2) ok &= this->wait_slot(B_EMPTY + s);  // PV(j-2) is done with buffer s
+            if (!ok) break;
+            uint16_t *pb = pbuf(s);
+#pragma unroll
+            for (int jj = 0; jj < T::NJ; jj++) this->softmax_chunk(jj, z, this->vmslot(s), pb, m, l, mn);
+            if (lane < 4) alpha()[8 * s + lane] = a;
+            arrive(B_FULL + s);
+            fence_proxy_async();
+            if (j + 2 < n) issue_kq(t0, (int)j + 2);  // key half and meta row s are free
+        }
+        // the value warp's last two "empty" arrivals (PV(n-2), PV(n-1))
+        for (int64_t j = n >= 2 ? n - 2 : 0; j < n; j++) ok &= this->wait_slot(B_EMPTY + (int)(j & 1));
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+            mn += __shfl_xor_sync(0xffffffffu, mn, o);
+        }
+        if (lane < 4) {
+            stats()[lane] = m;
+            stats()[4 + lane] = l;
+            stats()[8 + lane] = mn;
+        }
+        arrive(B_QDONE);
+        if (!ok) drain(3u);
+    }
+
+    // Value warp over the same tiles; writes the pair's partial [4][D+4] to `part`.
+    __device__ void run_p(int uu, int64_t t0, int64_t t1, float *part) {
+        this->u = uu;
+        const int lane = this->lane, gq = lane >> 2, t = lane & 3;
+        const int64_t n = t1 - t0;
+        issue_vp(t0, 0);
+        if (n > 1) issue_vp(t0, 1);
+        // entries 4..7 of each buffer (columns of no head) read as 1; the query warp
+        // writes only entries 0..3
+        if (lane < 8) alpha()[8 * (lane >> 2) + 4 + (lane & 3)] = 1.f;
+        __syncwarp();
+        float O[8][4];
+#pragma unroll
+        for (int o = 0; o < 8; o++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) O[o][e] = 0.f;
+        bool ok = true;
+        for (int64_t j = 0; j < n && ok; j++) {
+            const int s = (int)(j & 1);
+            ok &= this->wait_slot(2 + s);       // V(j)
+            ok &= this->wait_slot(B_FULL + s);  // p'(j), alpha(j)
+            if (!ok) break;
+            const float a0 = alpha()[8 * s + 2 * t], a1 = alpha()[8 * s + 2 * t + 1];
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                for (int o = 0; o < 8; o++) {
+                    O[o][0] *= a0;
+                    O[o][2] *= a0;
+                    O[o][1] *= a1;
+                    O[o][3] *= a1;
+                }
+            }
+            const uint16_t *pb = pbuf(s);
+#pragma unroll
+            for (int sl = 0; sl < 8; sl++) this->pv_step(sl, this->vslot(s), pb, O);
+            arrive(B_EMPTY + s);
+            fence_proxy_async();
+            if (j + 2 < n) issue_vp(t0, (int)j + 2);  // value half s is free
+        }
+        ok &= this->wait_slot(B_QDONE);
+        if (!ok) drain(12u);
+        const float *st = stats();
+        const float mn0 = st[8 + ((2 * t) & 3)], mn1 = st[8 + ((2 * t + 1) & 3)];
+#define KVQ_SP(J)                                                                  \
+    if (J < T::NJ && t < 2) {                                                      \
+        const float f = Base::template unscale<J>();                               \
+        for (int set = 0; set < T::NSET; set++) {                                  \
+            const int o = set * T::NJ + (J % T::NJ);                               \
+            const int ch = T::FPI * (gq + 8 * set) + (J % T::NJ);                  \
+            const int ch2 = ch + T::FPI / 2;                                       \
+            part[(2 * t) * (T::D + 4) + ch] = fmaf(O[o][0], f, mn0);               \
+            part[(2 * t + 1) * (T::D + 4) + ch] = fmaf(O[o][1], f, mn1);           \
+            part[(2 * t) * (T::D + 4) + ch2] = fmaf(O[o][2], f, mn0);              \
+            part[(2 * t + 1) * (T::D + 4) + ch2] = fmaf(O[o][3], f, mn1);          \
+        }                                                                          \
+    }
+        KVQ_SP(0) KVQ_SP(1) KVQ_SP(2) KVQ_SP(3) KVQ_SP(4) KVQ_SP(5) KVQ_SP(6) KVQ_SP(7)
+#undef KVQ_SP
+        if (gq == 0) {
+            part[t * (T::D + 4) + T::D] = st[t];
+            part[t * (T::D + 4) + T::D + 1] = st[4 + t];
+        }
+        __syncwarp();
     }
 };
 
@@ -636,7 +871,7 @@ struct MiniWarp {
         (void)slot_bits;
         bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
     }
-    __device__ unsigned char *slot(int s) const { return wbase + s * L.slot; }
+    __device__ unsigned char *slot(int s) const { return wbase + s * L.mslot; }
     __device__ void init_bars() {
         if (lane == 0) {
             for (int s = 0; s < kSlots; s++) mbar_init(&bars[s], 1);
@@ -738,7 +973,7 @@ struct MiniWarp {
                 for (int sl = 0; sl < 8; sl++) {
                     const SlabB b = slab_b(qpair[(hq * 8 + sl) * 4 + t], km[chan_of<8>(sl, t, 0)],
                                            km[chan_of<8>(sl, t, 1)], km[chan_of<8>(sl, t, 2)],
-                                           km[chan_of<8>(sl, t, 3)], lo_col);
+                                           km[chan_of<8>(sl, t, 3)], col_const(lo_col));
                     mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
                     uint32_t wv[4], x[4], xs[4];
 #pragma unroll
@@ -774,7 +1009,7 @@ struct MiniWarp {
                         uint32_t q1 = hmul2((uint32_t)qv[2] | ((uint32_t)qv[3] << 16), 0x2C002C00u);
                         q0 = hmul2(q0, 0x44004400u);
                         q1 = hmul2(q1, 0x44004400u);
-                        const SlabB b = slab_b(make_uint2(q0, q1), km4[0], km4[1], km4[2], km4[3], lo_col);
+                        const SlabB b = slab_b(make_uint2(q0, q1), km4[0], km4[1], km4[2], km4[3], col_const(lo_col));
                         uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) wv[kk] = hw[16 * s2 + 4 * kk + t];
