@@ -135,6 +135,7 @@ QuantKParams qk_params(const kvq_config *c, kvq_cache *k) {
     p.k_hi = k->k_hi;
     p.k_bidx = k->k_bidx;
     p.k_meta = k->k_meta;
+    p.status = k->status;
     return p;
 }
 
@@ -148,6 +149,7 @@ QuantVParams qv_params(const kvq_config *c, kvq_cache *k) {
     p.Gv = gv_of(c);
     p.v_codes = k->v_codes;
     p.v_meta = k->v_meta;
+    p.status = k->status;
     return p;
 }
 

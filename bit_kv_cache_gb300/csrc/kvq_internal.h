@@ -18,6 +18,7 @@ struct QuantKParams {
     int32_t *k_codes, *k_hi;
     uint8_t *k_bidx;
     uint16_t *k_meta;
+    int32_t *status;       // device status word (may be null)
 };
 
 struct QuantVParams {
@@ -29,6 +30,7 @@ struct QuantVParams {
     int U, D, G, Gv;
     int32_t *v_codes;
     uint16_t *v_meta;
+    int32_t *status;       // device status word (may be null)
 };
 
 struct CopyRowsParams {

@@ -65,6 +65,34 @@ __device__ __forceinline__ unsigned long long abs_units(uint32_t h) {
 }
 
 // ------------------------------------------------------------------------------
+// Fast quantizer.  r = (x - mn) * rcp(s) in fp32 (x - mn is exact: both are fp16
+// values); t = r + 1.5 * 2^23 rounds r to the nearest integer, ties to even, into
+// the low mantissa bits (0 <= r < 2^22): its bits are 0x4B400000 + rint(r), clamped
+// to 0x4B400000 + max_int as integers.  A zero scale has rcp 0, so every code is 0.
+// Each thread tracks max |r - rint(r)|; one that comes within 2^-14 of a
+// half-integer redoes its block with quant_code (IEEE division), so the codes are
+// those of the plain definition: |r - q| <= 1.5 * 2^-23 * q for the correctly
+// rounded quotient q, below 2^-14 for q < 128, and larger quotients are clamped to
+// max_int by both.  A word accumulates t * 2^(b pos) by integer multiply-add and
+// subtracts 0x4B400000 * sum 2^(b pos) once (mod 2^32), which leaves the packed codes.
+// ------------------------------------------------------------------------------
+constexpr uint32_t kMagicBits = 0x4B400000u;  // 1.5 * 2^23
+constexpr float kTieMargin = 0.5f - 0x1p-14f;
+
+__device__ __forceinline__ uint32_t qbits(float x, float mn, float inv, uint32_t lim, float &emax) {
+    const float r = __fmul_rn(__fsub_rn(x, mn), inv);
+    const float t = __fadd_rn(r, 12582912.0f);
+    emax = fmaxf(emax, fabsf(__fsub_rn(r, __fsub_rn(t, 12582912.0f))));
+    return min(__float_as_uint(t), lim);
+}
+// 0x4B400000 * sum_{j < n} 2^(b j)  (mod 2^32): the offset a word of n codes picks up.
+__host__ __device__ constexpr uint32_t magic_sum(int b, int n) {
+    uint32_t s = 0;
+    for (int j = 0; j < n; j++) s += kMagicBits << (b * j);
+    return s;
+}
+
+// ------------------------------------------------------------------------------
 // Keys: one CTA per page of G tokens.  Thread (pair pr, slice sl) holds channels
 // 2pr, 2pr+1 for TPS consecutive tokens in registers; min/max (and, for Kitty, the
 // channel scores) are combined across slices in shared memory.
@@ -258,6 +286,107 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
 }
 
 // ------------------------------------------------------------------------------
+// Values, D = Gv = 128: one CTA per 128 tokens.  Lane (c8, hb) of warp w loads
+// channels 8 c8 .. + 7 of tokens 16 w + 2 i + hb (i = 0..7): each load of a warp is
+// two contiguous rows.  A token's min / max reduces over its 16 lanes by shuffles;
+// lane i computes the group of the half-warp's token i and shares it; codes pack
+// along channels and are staged in shared memory so that each word row of the page
+// leaves as contiguous 512-byte stores.
+// ------------------------------------------------------------------------------
+template <int BITS>
+__device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int64_t tl0, const uint16_t *src) {
+    constexpr int D = 128, FPI = 32 / BITS, NWORD = D / FPI;
+    __shared__ __align__(16) uint32_t s_codes[NWORD][128];
+    __shared__ __align__(16) uint32_t s_meta[128];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, c8 = lane & 15, hb = lane >> 4;
+    uint4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) x[i] = reinterpret_cast<const uint4 *>(src + (size_t)(16 * w + 2 * i + hb) * D)[c8];
+    float smn = 0.f, smx = 0.f;  // min / max of the half-warp's token c8 & 7
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        __half2 lo = *reinterpret_cast<const __half2 *>(&x[i].x), hi = lo;
+#pragma unroll
+        for (int k = 1; k < 4; k++) {
+            const uint32_t wk = (&x[i].x)[k];
+            const __half2 v = *reinterpret_cast<const __half2 *>(&wk);
+            lo = __hmin2(lo, v);
+            hi = __hmax2(hi, v);
+        }
+        float a = fminf(__low2float(lo), __high2float(lo)), b = fmaxf(__low2float(hi), __high2float(hi));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+        }
+        if ((c8 & 7) == i) smn = a, smx = b;
+    }
+    // lane c8 = i (< 8) of each half-warp forms the group of its token i
+    GroupQ mine = make_group(smn, smx, (1 << BITS) - 1);
+    if (c8 < 8) s_meta[16 * w + 2 * c8 + hb] = (uint32_t)mine.s16 | ((uint32_t)mine.mn16 << 16);
+    constexpr uint32_t lim = kMagicBits + (1u << BITS) - 1;
+    uint32_t part[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int srcl = (lane & 16) | i;
+        GroupQ g;
+        g.mn = __shfl_sync(0xffffffffu, mine.mn, srcl);
+        g.inv = __shfl_sync(0xffffffffu, mine.inv, srcl);
+        g.s = __shfl_sync(0xffffffffu, mine.s, srcl);
+        g.maxf = (float)((1 << BITS) - 1);
+        g.zero = g.s == 0.0f;
+        uint32_t a = 0;
+        float emax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const float2 f = unpack_half2((&x[i].x)[k]);
+            a += qbits(f.x, g.mn, g.inv, lim, emax) * (1u << (BITS * (2 * k)));
+            a += qbits(f.y, g.mn, g.inv, lim, emax) * (1u << (BITS * (2 * k + 1)));
+        }
+        a -= magic_sum(BITS, 8);
+        if (emax > kTieMargin) {  // near a half-integer in this piece: the exact path
+            a = 0;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const float2 f = unpack_half2((&x[i].x)[k]);
+                a |= quant_code(f.x, g) << (BITS * (2 * k));
+                a |= quant_code(f.y, g) << (BITS * (2 * k + 1));
+            }
+        }
+        part[i] = a;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int tt = 16 * w + 2 * i + hb;
+        if (BITS == 2) {  // 16 channels per word: lanes c8 and c8 ^ 1
+            const uint32_t nb = __shfl_xor_sync(0xffffffffu, part[i], 1);
+            if ((c8 & 1) == 0) s_codes[c8 >> 1][tt] = part[i] | (nb << 16);
+        } else {
+            s_codes[c8][tt] = part[i];
+        }
+    }
+    __syncthreads();
+    const int64_t tau0 = p.tok0 + tl0, page = tau0 / p.G, tin0 = tau0 % p.G;
+    for (int i = tid; i < NWORD * 32; i += 256) {
+        const int m = i >> 5, q4 = i & 31;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&s_codes[m][4 * q4]);
+        *reinterpret_cast<uint4 *>(p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * NWORD + m) * p.G + tin0 +
+                                   4 * q4) = v;
+    }
+    if (tid < 32)
+        reinterpret_cast<uint4 *>(reinterpret_cast<uint32_t *>(p.v_meta) + (size_t)u * p.max_T + tau0)[tid] =
+            *reinterpret_cast<const uint4 *>(&s_meta[4 * tid]);
+}
+
+// One CTA per 128 value tokens, reading its rows straight from global memory.
+template <int BITS>
+__global__ void __launch_bounds__(256) quant_v_rows(QuantVParams p) {
+    const int u = blockIdx.y;
+    const int64_t tl0 = (int64_t)blockIdx.x * 128;
+    quant_v_chunk<BITS>(p, u, tl0, p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + tl0) * 128);
+}
+
+// ------------------------------------------------------------------------------
 // Row copies between [U][*][D] fp16 buffers (prefill split, flush bookkeeping).
 // ------------------------------------------------------------------------------
 __global__ void copy_rows_kernel(CopyRowsParams p) {
@@ -338,6 +467,13 @@ cudaError_t launch_quant_k(const QuantKParams &p_in, int bits, bool kitty, cudaS
 
 cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st) {
     if (p.n_tok <= 0) return cudaSuccess;
+    if (p.D == 128 && p.Gv == 128 && p.G % 128 == 0 && p.n_tok % 128 == 0 && p.tok0 % 128 == 0) {
+        dim3 grid((unsigned)(p.n_tok / 128), (unsigned)p.U);
+        if (bits == 2) quant_v_rows<2><<<grid, 256, 0, st>>>(p);
+        else if (bits == 4) quant_v_rows<4><<<grid, 256, 0, st>>>(p);
+        else return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     dim3 grid((unsigned)((p.n_tok + 127) / 128), (unsigned)p.U);
 #define KVQ_QV(B, N, GVV)                                          \
     if (bits == B && p.D == N * 8 && p.Gv == GVV) {                \
