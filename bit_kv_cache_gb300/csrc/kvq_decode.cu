@@ -271,11 +271,11 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *ptr, int v) {
 //   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
 //      CTA resets both counters to zero for the next call.
 // ---------------------------------------------------------------------------------
-template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
+template <int BITS, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
-    // Work units: in the tile kernels a unit is a warp pair (query warp, value warp)
-    // that shares one region of shared memory; in the generic kernel, one warp.
-    constexpr int NU = FAST ? NW / 2 : NW;
+    // Work units: a warp, or with PAIR (tile kernels) a warp pair -- query warp and
+    // value warp -- that shares one region of shared memory.
+    constexpr int NU = PAIR ? NW / 2 : NW;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_seg[NU][2];   // sequence of each unit segment (-1: none)
     __shared__ int s_cnt[NU][2];   // items of each unit segment
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     __shared__ int s_ns[2 * NU];   // their slot counts
     __shared__ int s_nl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = FAST ? warp >> 1 : warp, role = FAST ? warp & 1 : 0;
+    const int unit = PAIR ? warp >> 1 : warp, role = PAIR ? warp & 1 : 0;
     const int D = p.D, g = p.g;
     const int wbytes = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).total : gen_warp_bytes(D);
     const int part0_off = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).part0 : 0;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         MiniWarp<BITS, KITTY> mw(p, wbase, 0);
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
         __syncthreads();
-        // mini units: the query warp of the pair runs the 16-token tiles alone
+        // mini units: the first warp of a pair runs the 16-token tiles alone
         const bool active = fastpool || role == 0;
         for (int e = 0; e < 2 && x < x1; e++) {
             const int u = x / P.n;
@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             const bool more = end < x1;
             float *dst = reinterpret_cast<float *>(wbase + (more ? part0_off : 0));
             if (fastpool) {
-                if (role == 0) pw.run_q(u, x - u * P.n, end - u * P.n);
+                if (!PAIR) pw.run(u, x - u * P.n, end - u * P.n, dst);
+                else if (role == 0) pw.run_q(u, x - u * P.n, end - u * P.n);
                 else pw.run_p(u, x - u * P.n, end - u * P.n, dst);
             } else if (active) {
                 mw.run(u, x - u * P.n, end - u * P.n, dst);
@@ -517,10 +518,10 @@ size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast) {
     return (size_t)nw * gen_warp_bytes(D);
 }
 
-template <int BITS, bool KITTY, bool FAST, int DPL, int NW>
+template <int BITS, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
 static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
     const size_t smem = decode_smem_bytes(BITS, KITTY, p.n_boost, p.D, FAST);
-    auto k = decode_kernel<BITS, KITTY, FAST, DPL, NW>;
+    auto k = decode_kernel<BITS, KITTY, FAST, PAIR, DPL, NW>;
     // The dynamic shared-memory limit is raised once per device to the most any
     // configuration of this instantiation asks for (the opt-in maximum).
     static int raised[64] = {0};
@@ -540,18 +541,18 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st) {
-    if (fast) {  // p.wpc units of two warps
+    if (fast) {  // p.wpc units; 4-bit tiles run on warp pairs, the others on single warps
         if (p.kitty) {
-            if (p.wpc == 8) return launch_one<2, true, true, 4, 16>(p, st);
-            return launch_one<2, true, true, 4, 12>(p, st);
+            if (p.wpc == 8) return launch_one<2, true, true, false, 4, 8>(p, st);
+            return launch_one<2, true, true, false, 4, 6>(p, st);
         }
-        if (p.bits == 2) return launch_one<2, false, true, 4, 16>(p, st);
-        return launch_one<4, false, true, 4, 16>(p, st);
+        if (p.bits == 2) return launch_one<2, false, true, false, 4, 8>(p, st);
+        return launch_one<4, false, true, true, 4, 16>(p, st);
     }
     switch (p.D) {
-        case 64: return launch_one<2, false, false, 2, 8>(p, st);
-        case 128: return launch_one<2, false, false, 4, 8>(p, st);
-        case 256: return launch_one<2, false, false, 8, 8>(p, st);
+        case 64: return launch_one<2, false, false, false, 2, 8>(p, st);
+        case 128: return launch_one<2, false, false, false, 4, 8>(p, st);
+        case 256: return launch_one<2, false, false, false, 8, 8>(p, st);
     }
     return cudaErrorInvalidValue;
 }
