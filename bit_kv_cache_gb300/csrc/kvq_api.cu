@@ -67,7 +67,7 @@ int64_t slot_bound(const kvq_config *c) { return cdiv(4 * (int64_t)num_sms(), un
 // range within two sequences (about U / warps-per-CTA).
 int64_t max_pool_ctas(const kvq_config *c) { return std::max<int64_t>(num_sms(), cdiv(units(c), 6)); }
 
-// Workspace: [status word][slot counters U][item counters U][partials].  The
+// Workspace: [status word][slot counters U x 4 B][item counters U x 8 B][partials].  The
 // counters are zero between calls (the combining CTA resets them).
 struct WsLayout {
     size_t status, slot_ctr, item_ctr, partials, total;
@@ -79,8 +79,8 @@ WsLayout ws_layout(const kvq_config *c) {
     const size_t ctr = (size_t)cdiv(U * 4, 256) * 256;
     w.status = 0;
     w.slot_ctr = 256;
-    w.item_ctr = w.slot_ctr + ctr;
-    w.partials = w.item_ctr + ctr;
+    w.item_ctr = w.slot_ctr + ctr;                       // 8 bytes per sequence
+    w.partials = w.item_ctr + 2 * ctr;
     w.total = w.partials + (size_t)U * slot_bound(c) * g * (c->D + 4) * 4;
     return w;
 }
@@ -590,7 +590,7 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     char *w = static_cast<char *>(ws);
     p.status = reinterpret_cast<int32_t *>(w + wl.status);
     p.slot_ctr = reinterpret_cast<int32_t *>(w + wl.slot_ctr);
-    p.item_ctr = reinterpret_cast<int32_t *>(w + wl.item_ctr);
+    p.item_ctr = reinterpret_cast<unsigned long long *>(w + wl.item_ctr);
     p.partials = reinterpret_cast<float *>(w + wl.partials);
     return status_of(launch_decode(p, fast, (cudaStream_t)stream));
 }

@@ -252,9 +252,9 @@ __device__ __forceinline__ void load_q_gen(const DecodeParams &p, int u, uint16_
     __syncwarp();
 }
 
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *ptr, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long *ptr, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
     return old;
 }
 
@@ -318,8 +318,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         if (tid == 0) report(p.status, KVQ_DEV_BAD_STATE_BIT);
         return;
     }
+    // The slots are taken by lanes 16.. of the last warp, which issue no copies and no
+    // release fences, so nothing waits for these atomics before the epilogue.
+    const int slot_lane = tid - (NW * 32 - 16);
     int my_slot = 0;
-    if (tid < nu) my_slot = atomicAdd(&p.slot_ctr[ulo + tid], 1);
 
     if (FAST) {
         const int k = kc + unit;
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         PairWarp<BITS, KITTY> pw(p, wbase);
         MiniWarp<BITS, KITTY> mw(p, wbase, 0);
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
-        __syncthreads();
+        if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // the pair's partner
+        if (slot_lane >= 0 && slot_lane < nu) my_slot = atomicAdd(&p.slot_ctr[ulo + slot_lane], 1);
         // mini units: the first warp of a pair runs the 16-token tiles alone
         const bool active = fastpool || role == 0;
         for (int e = 0; e < 2 && x < x1; e++) {
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         }
     } else {
         // ---- generic warp: one chunk of one sequence ----
+        if (slot_lane >= 0 && slot_lane < nu) my_slot = atomicAdd(&p.slot_ctr[ulo + slot_lane], 1);
         const int64_t j = (int64_t)blockIdx.x * p.wpc + warp;
         GenState<DPL> st;
 #pragma unroll
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         s_cnt[unit][0] = cnt0;
         s_cnt[unit][1] = cnt1;
     }
-    if (tid < nu) s_slot[tid] = my_slot;
+    if (slot_lane >= 0 && slot_lane < nu) s_slot[slot_lane] = my_slot;
     __syncthreads();
 
     // ---- merge: one float4 of (sequence, head, channels) per thread and step ----
@@ -439,11 +443,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
 #pragma unroll
             for (int e = 0; e < 2; e++)
                 if (s_seg[w][e] == u) items += s_cnt[w][e];
-        const int before = atom_add_acq_rel_gpu(&p.item_ctr[u], items);
-        if (before + items == p.n_items) {
-            const int k = atomicAdd(&s_nl, 1);
+        // item counter: items merged in the high word, CTAs arrived in the low word
+        const unsigned long long before = atom_add_acq_rel_gpu(&p.item_ctr[u], ((unsigned long long)items << 32) | 1u);
+        if ((int)(before >> 32) + items == p.n_items) {  // every CTA of u has arrived: it took
+            const int k = atomicAdd(&s_nl, 1);            // its slot before its arrival
             s_lu[k] = u;
-            s_ns[k] = *reinterpret_cast<volatile int32_t *>(&p.slot_ctr[u]);
+            s_ns[k] = (int)(before & 0xffffffffu) + 1;
         }
     }
     __syncthreads();
@@ -457,15 +462,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int ns = min(s_ns[lk], p.max_slots);
         const float *up = p.partials + ((size_t)u * p.max_slots * g + h) * R;
         const size_t cs = (size_t)g * R;  // floats between slots
-        // one pass with a running maximum, four slots at a time: their loads go out
+        // one pass with a running maximum, eight slots at a time: their loads go out
         // together, then the chunk's maximum rescales the running sums once
         float M = -INFINITY, L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < ns; c0 += 4) {
-            float2 ml[4];
-            float4 v[4];
+        for (int c0 = 0; c0 < ns; c0 += 8) {
+            float2 ml[8];
+            float4 v[8];
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
+            for (int j = 0; j < 8; j++) {
                 ml[j] = make_float2(-INFINITY, 0.f);
                 v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (c0 + j < ns) {
@@ -473,7 +478,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
                     v[j] = __ldcg(reinterpret_cast<const float4 *>(up + (c0 + j) * cs + d));
                 }
             }
-            const float Mn = fmaxf(fmaxf(M, fmaxf(ml[0].x, ml[1].x)), fmaxf(ml[2].x, ml[3].x));
+            float Mn = M;
+#pragma unroll
+            for (int j = 0; j < 8; j++) Mn = fmaxf(Mn, ml[j].x);
             if (Mn == -INFINITY) continue;
             const float r = M == -INFINITY ? 0.f : exp2f(M - Mn);
             L *= r;
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             O.w *= r;
             M = Mn;
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
+            for (int j = 0; j < 8; j++) {
                 const float f = ml[j].x == -INFINITY ? 0.f : exp2f(ml[j].x - M);
                 L = fmaf(ml[j].y, f, L);
                 O.x = fmaf(v[j].x, f, O.x);

@@ -326,13 +326,16 @@ struct FastWarp {
 #pragma unroll
         for (int r = 0; r < 4; r++) xs[r] = x[r] >> T::SH;
     }
+    // Z: the first slab of a tile, whose accumulators start from zero.
+    template <bool Z = false>
     __device__ __forceinline__ static void mma_sets(float (&acc)[T::NJ][4], const uint32_t (&x)[4],
                                                     const uint32_t (&xs)[4], uint32_t b0, uint32_t b1) {
         uint32_t a[4];
-#define KVQ_RS(J)                                                        \
-    if (J < T::NJ) {                                                     \
-        frag<J>(x, xs, a);                                               \
-        mma_16816(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1);      \
+#define KVQ_RS(J)                                                                      \
+    if (J < T::NJ) {                                                                   \
+        frag<J>(x, xs, a);                                                             \
+        if (Z) mma_16816_z(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1);            \
+        else mma_16816(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1);               \
     }
         KVQ_RS(0) KVQ_RS(1) KVQ_RS(2) KVQ_RS(3) KVQ_RS(4) KVQ_RS(5) KVQ_RS(6) KVQ_RS(7)
 #undef KVQ_RS
@@ -349,7 +352,8 @@ struct FastWarp {
 #undef KVQ_RS
     }
 
-    // One 16-channel slab of S = Kcodes . q' (+ the min mma) for the key half in st.
+    // One 16-channel slab of S = Kcodes . q' (+ the min mma) for the key half in st;
+    // slab 0 starts the accumulators from zero.
     __device__ __forceinline__ void qk_slab(int sl, const unsigned char *st, float (&acc)[T::NJ][4],
                                             float (&cm)[4]) const {
         const int gq = lane >> 2, t = lane & 3;
@@ -357,11 +361,13 @@ struct FastWarp {
         const uint2 qp = reinterpret_cast<const uint2 *>(wbase + L.qpair)[((gq >> 1) * 8 + sl) * 4 + t];
         const SlabB b = slab_b(qp, km[chan_of<T::PS>(sl, t, 0)], km[chan_of<T::PS>(sl, t, 1)],
                                km[chan_of<T::PS>(sl, t, 2)], km[chan_of<T::PS>(sl, t, 3)], col_const((gq & 1) != 0));
-        mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
+        if (sl == 0) mma_16816_z(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
+        else mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
         uint32_t w[4], x[4], xs[4];
         ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3) + 64 * sl);
         split(w, x, xs);
-        mma_sets(acc, x, xs, b.b0, b.b1);
+        if (sl == 0) mma_sets<true>(acc, x, xs, b.b0, b.b1);
+        else mma_sets<false>(acc, x, xs, b.b0, b.b1);
     }
 
     // Kitty: S += hi-plane codes . (4 q') over the boosted slots.
@@ -513,7 +519,6 @@ struct FastWarp {
 
         // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
         ok &= wait_slot(0);
-        zero(acc, cm);
 #pragma unroll
         for (int sl = 0; sl < 8; sl++) qk_slab(sl, kslot(0), acc, cm);
         if (KITTY && p.n_boost > 0) qk_boost(kslot(0), acc);
@@ -537,7 +542,6 @@ struct FastWarp {
             if (!ok) break;
             const uint16_t *pb = pb0 + cur * 4 * T::PROW;
             if (more) {
-                zero(acc, cm);
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
                     pv_step(sl, vslot(cur), pb, O);
@@ -711,7 +715,6 @@ struct PairWarp : FastWarp<BITS, KITTY> {
             const int s = (int)(j & 1);
             ok &= this->wait_slot(s);  // K(j)
             if (!ok) break;
-            this->zero(acc, cm);
 #pragma unroll
             for (int sl = 0; sl < 8; sl++) this->qk_slab(sl, this->kslot(s), acc, cm);
             if (KITTY && this->p.n_boost > 0) this->qk_boost(this->kslot(s), acc);

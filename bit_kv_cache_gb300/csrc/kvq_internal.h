@@ -75,7 +75,7 @@ struct DecodeParams {
     uint16_t *out;
     float *partials;       // [U][max_slots][g][D + 4]
     int32_t *slot_ctr;     // [U] slots taken (zero between calls)
-    int32_t *item_ctr;     // [U] items merged (zero between calls)
+    unsigned long long *item_ctr;  // [U] items merged << 32 | CTAs arrived (zero between calls)
     int32_t *status;       // workspace status word
     // schedule
     int U, wpc;            // sequences, warps per CTA
