@@ -56,7 +56,7 @@ def build(force: bool = False) -> str:
 
 
 class _Seq(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("D", "G", "bits", "Gv", "n_boost", "kitty")] + \
+    _fields_ = [(n, ctypes.c_int) for n in ("D", "G", "bits", "Gv", "n_boost", "kitty", "vbits")] + \
                [(n, ctypes.c_long) for n in ("n_sink", "T_k", "n_kres", "T_v", "n_vres",
                                              "n_local", "local_head", "local_cap")] + \
                [(n, ctypes.c_void_p) for n in ("k_sink", "v_sink", "k_codes", "k_hi", "k_bidx",
@@ -221,9 +221,10 @@ class OracleCache:
     """
 
     def __init__(self, B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi",
-                 max_T=None):
+                 max_T=None, v_bits=None):
         assert mode in ("kivi", "kitty")
         self.B, self.H_q, self.H_kv, self.D, self.G, self.bits = B, H_q, H_kv, D, G, bits
+        self.vbits = bits if not v_bits else v_bits  # value codes may use their own width
         self.S, self.R, self.n_boost, self.mode = S, (G if R is None else R), n_boost, mode
         self.Gv = min(G, D)
         self.kitty = mode == "kitty"
@@ -235,7 +236,7 @@ class OracleCache:
         self.k_sink, self.v_sink = z16(S), z16(S)
         self.k_res, self.v_res = z16(self.cap_kres), z16(self.cap_vres)
         self.v_local = z16(self.R if self.kitty else 0)
-        fpi = 32 // bits
+        fpi = 32 // self.vbits
         self.k_codes = np.zeros(U + (0, D), np.int32)
         self.k_hi = np.zeros(U + (0, n_boost), np.int32)
         self.k_bidx = np.zeros(U + (0, D), np.uint8)
@@ -264,7 +265,7 @@ class OracleCache:
     def _pack_v(self, src: np.ndarray):
         if src.shape[2] == 0:
             return
-        c, mt = quant_v(src, self.Gv, self.bits)
+        c, mt = quant_v(src, self.Gv, self.vbits)
         self.v_codes = np.concatenate([self.v_codes, c], 2)
         self.v_meta = np.concatenate([self.v_meta, mt], 2)
         self.T_v += src.shape[2]
@@ -344,6 +345,7 @@ class OracleCache:
         s = _Seq()
         s.D, s.G, s.bits, s.Gv, s.n_boost, s.kitty = (self.D, self.G, self.bits, self.Gv,
                                                        self.n_boost, int(self.kitty))
+        s.vbits = self.vbits
         s.n_sink, s.T_k, s.n_kres = self.n_sink, self.T_k, self.n_kres
         s.T_v, s.n_vres, s.n_local = self.T_v, self.n_vres, self.n_local
         s.local_head, s.local_cap = self.local_head, max(self.v_local.shape[2], 1)

@@ -279,7 +279,7 @@ void kvq_or_quant_k_kitty(const uint16_t *k, int U, long L, int D, int G, int n_
  * [sink | V packed | V residual (KIVI) or Q-buffer (Kitty) | local (Kitty)]
  * for values; both orders cover the same L tokens. */
 typedef struct {
-    int D, G, bits, Gv, n_boost, kitty;
+    int D, G, bits, Gv, n_boost, kitty, vbits;   /* bits: keys, vbits: values */
     long n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head, local_cap;
     const uint16_t *k_sink, *v_sink;   /* [n_sink][D] */
     const int32_t *k_codes;            /* [T_k/fpi][D] (Kitty: low plane, fpi 16) */
@@ -305,7 +305,7 @@ void kvq_or_seq_rows(const kvq_or_seq *s, double *Kh, double *Vh)
     int D = s->D;
     long L = kvq_or_seq_len(s);
     int kfpi = s->kitty ? 16 : 32 / s->bits, kbits = s->kitty ? 2 : s->bits;
-    int vfpi = 32 / s->bits, vbits = s->bits, vmask = (1 << vbits) - 1;
+    int vfpi = 32 / s->vbits, vbits = s->vbits, vmask = (1 << vbits) - 1;
     for (long t = 0; t < L; t++) {
         double *kr = Kh + t * D, *vr = Vh + t * D;
         /* keys */

@@ -464,3 +464,54 @@ def test_signed_zero_groups_store_positive_zero():
         assert np.float16(s).view(np.uint16) == 0 and np.float16(mn).view(np.uint16) == 0
     s, mn, c = oracle.quant_group(np.array([-1.0, -0.0], np.float16), 2)
     assert float(mn) == -1.0 and c.tolist() == [0, 3]
+
+
+# --------------------------------------------------------------------------- #
+# Separate key and value widths (K4V2, K2V4, K8V8, K2V2 with sinks)            #
+# --------------------------------------------------------------------------- #
+
+def _unpack_rows(words: np.ndarray, bits: int, along_last: bool) -> np.ndarray:
+    """Codes from packed int32 words, element j of a word at bit bits*j (numpy)."""
+    fpi = 32 // bits
+    w = words.astype(np.int64) & 0xFFFFFFFF
+    shifts = (np.arange(fpi) * bits).astype(np.int64)
+    c = (w[..., None] >> shifts) & ((1 << bits) - 1)           # [..., words, fpi]
+    if along_last:
+        return c.reshape(c.shape[:-2] + (-1,))                 # values: along channels
+    c = np.moveaxis(c, -1, -2)                                 # keys: [T/fpi, fpi, D]
+    return c.reshape(c.shape[:-3] + (-1, c.shape[-1]))
+
+
+@pytest.mark.parametrize("kb,vb,S", [(4, 2, 0), (2, 4, 0), (8, 8, 0), (2, 2, 4)])
+def test_mixed_widths_codes_and_attention(kb, vb, S):
+    rng = np.random.default_rng(40 + kb + vb + S)
+    B, Hq, Hkv, D, G = 1, 4, 2, 32, 32
+    L = S + 3 * G + 9
+    K = rng.standard_normal((B, Hkv, L, D)).astype(np.float16)
+    V = rng.standard_normal((B, Hkv, L, D)).astype(np.float16)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    c = OracleCache(B, Hq, Hkv, D, G, kb, S=S, R=G, v_bits=vb)
+    c.prefill(K, V)
+    T = 3 * G
+    assert (c.n_sink, c.T_k, c.T_v, c.n_kres, c.n_vres) == (S, T, T, 9, 9)
+    # the packed parts are the one-shot quantizers at their own widths
+    ck, mk = oracle.quant_k(K, G, kb, S, T)
+    cv, mv = oracle.quant_v(V, min(G, D), vb, S, T)
+    assert c.v_codes.shape[-1] == D * vb // 32
+    assert np.array_equal(c.k_codes, ck) and np.array_equal(c.v_codes, cv)
+    # attention equals a textbook softmax over rows dequantized here with numpy
+    kc = _unpack_rows(c.k_codes, kb, along_last=False)         # [B,H,T,D]
+    vc = _unpack_rows(c.v_codes, vb, along_last=True)          # [B,H,T,D]
+    km = c.k_meta.astype(np.float64)                           # [B,H,T/G,D,2]
+    vm = c.v_meta.astype(np.float64)                           # [B,H,T,1,2]
+    kd = kc * np.repeat(km[..., 0], G, axis=2) + np.repeat(km[..., 1], G, axis=2)
+    vd = vc * vm[..., 0] + vm[..., 1]
+    Kf = np.concatenate([K[:, :, :S].astype(np.float64), kd, K[:, :, S + T:].astype(np.float64)], 2)
+    Vf = np.concatenate([V[:, :, :S].astype(np.float64), vd, V[:, :, S + T:].astype(np.float64)], 2)
+    out = c.attend(q)
+    g = Hq // Hkv
+    for hq in range(Hq):
+        z = Kf[0, hq // g] @ q[0, hq].astype(np.float64) / math.sqrt(D)
+        p = np.exp(z - z.max())
+        ref = (p / p.sum()) @ Vf[0, hq // g]
+        assert np.allclose(out[0, hq], ref, rtol=1e-12, atol=1e-12)
