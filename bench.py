@@ -63,7 +63,7 @@ def decode_bytes(wl, lengths) -> int:
     b = U * T_k * D * kb // 8 + U * (T_k // G) * D * 4              # key codes + (scale, min)
     if wl.mode == "kitty" and wl.n_boost:
         b += U * T_k * wl.n_boost * 2 // 8 + U * (T_k // G) * D      # high plane + boost index
-    b += U * T_v * D * wl.bits // 8 + U * T_v * (D // Gv) * 4       # value codes + (scale, min)
+    b += U * T_v * D * wl.vbits // 8 + U * T_v * (D // Gv) * 4      # value codes + (scale, min)
     n16 = lengths["n_sink"] * 2 + lengths["n_kres"] + lengths["n_vres"] + lengths["n_local"]
     b += U * n16 * D * 2                                           # fp16 sink / buffers
     b += 2 * wl.B * wl.H_q * D * 2                                 # q in, out
@@ -181,7 +181,7 @@ def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
     sub = wl.replace(B=1, H_kv=n_units, H_q=n_units * wl.g)
     K, V = kvq_synth.prefill_kv(wl.replace(B=1, H_kv=min(wl.H_kv, n_units)), L0)
     ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S, R=sub.R,
-                             n_boost=sub.n_boost, mode=sub.mode)
+                             n_boost=sub.n_boost, mode=sub.mode, v_bits=sub.v_bits)
     ora.prefill(K, V)
     q = kvq_synth.queries(sub, 1)[0]
     lengths = dict(n_sink=ora.n_sink, T_k=ora.T_k, n_kres=ora.n_kres, T_v=ora.T_v,
@@ -216,7 +216,7 @@ def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
     def make(n_tok):
         Kx, Vx = kvq_synth.prefill_kv(sub, n_tok)
         ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S,
-                                 R=sub.R, n_boost=sub.n_boost, mode=sub.mode)
+                                 R=sub.R, n_boost=sub.n_boost, mode=sub.mode, v_bits=sub.v_bits)
         ora.prefill(Kx, Vx)
         return ora
 
@@ -247,7 +247,7 @@ def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, shapes of the workload)",
             "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
-                       "T": wl.T, "G": wl.G, "bits": wl.bits},
+                       "T": wl.T, "G": wl.G, "bits": wl.bits, "v_bits": wl.vbits},
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -301,7 +301,7 @@ def main():
         Kl = torch.roll(K0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
         Vl = torch.roll(V0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
         c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                         n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=dev)
+                         n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=dev, v_bits=wl.v_bits)
         c.prefill(Kl, Vl)
         caches.append(c)
         del Kl, Vl
@@ -424,7 +424,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded; shapes and outlier structure of the workload)",
         "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
-                   "T": wl.T, "G": wl.G, "R": wl.R, "bits": wl.bits, "S": wl.S,
+                   "T": wl.T, "G": wl.G, "R": wl.R, "bits": wl.bits, "v_bits": wl.vbits, "S": wl.S,
                    "n_boost": wl.n_boost, "mode": wl.mode,
                    "step": "append_token + decode_attn + flush_group (when full), one layer",
                    "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (

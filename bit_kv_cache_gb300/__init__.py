@@ -36,7 +36,7 @@ class KvqError(RuntimeError):
 class Config(ctypes.Structure):
     """kvq_config"""
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "H_q", "H_kv", "D", "G", "bits", "S", "R",
-                                              "n_boost", "mode")] + [("max_T", ctypes.c_int64)]
+                                              "n_boost", "mode", "v_bits")] + [("max_T", ctypes.c_int64)]
 
 
 class Cache(ctypes.Structure):
@@ -83,9 +83,10 @@ def _check(code: int, what: str):
         raise KvqError(code, what)
 
 
-def make_config(B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi", max_T=0) -> Config:
+def make_config(B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi", max_T=0,
+                v_bits=0) -> Config:
     m = {"kivi": KVQ_MODE_KIVI, "kitty": KVQ_MODE_KITTY}[mode]
-    return Config(B, H_q, H_kv, D, G, bits, S, G if R is None else R, n_boost, m, max_T)
+    return Config(B, H_q, H_kv, D, G, bits, S, G if R is None else R, n_boost, m, v_bits or 0, max_T)
 
 
 class KVQCache:
@@ -96,10 +97,10 @@ class KVQCache:
     current torch stream."""
 
     def __init__(self, B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi",
-                 max_T=0, device="cuda"):
+                 max_T=0, device="cuda", v_bits=0):
         import torch
         self.torch = torch
-        self.cfg = make_config(B, H_q, H_kv, D, G, bits, S, R, n_boost, mode, max_T)
+        self.cfg = make_config(B, H_q, H_kv, D, G, bits, S, R, n_boost, mode, max_T, v_bits)
         _check(lib.kvq_config_check(ctypes.byref(self.cfg)), "config")
         self.device = torch.device(device)
         self.c = Cache()
@@ -205,7 +206,7 @@ class KVQCache:
         U, D, T, G = cfg.B * cfg.H_kv, cfg.D, cfg.max_T, cfg.G
         kitty = cfg.mode == KVQ_MODE_KITTY
         kfpi = 16 if kitty else 32 // cfg.bits
-        vfpi = 32 // cfg.bits
+        vfpi = 32 // (cfg.v_bits or cfg.bits)
         Gv = min(G, D)
         b = self.buf[name]
         if name == "k_codes":

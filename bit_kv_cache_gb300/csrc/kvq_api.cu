@@ -19,23 +19,27 @@ constexpr int kMaxBoostFast = 64;
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int vbits_of(const kvq_config *c) { return c->v_bits ? c->v_bits : c->bits; }
 inline int kfpi(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY ? 16 : 32 / c->bits; }
-inline int vfpi(const kvq_config *c) { return 32 / c->bits; }
+inline int vfpi(const kvq_config *c) { return 32 / vbits_of(c); }
 inline int gv_of(const kvq_config *c) { return std::min(c->G, c->D); }
 inline bool kitty(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY; }
 inline int64_t cap_k(const kvq_config *c) { return kitty(c) ? c->G : c->R; }
 inline int64_t cap_v(const kvq_config *c) { return kitty(c) ? c->G : c->R; }
 inline int64_t units(const kvq_config *c) { return (int64_t)c->B * c->H_kv; }
 
-// Slices of the key quantizer (rows of tokens per thread must be 16, 32 or 64).
-bool key_slices_ok(const kvq_config *c) {
-    const int fpi = kfpi(c), pairs = c->D / 2, smax = 256 / pairs, nwords = c->G / fpi;
-    int S = 1;
-    for (int s = 1; s <= smax && s <= nwords; s++)
-        if (nwords % s == 0 && (c->G / s) <= 64) S = s;
-    const int tps = c->G / S;
-    return tps == 16 || tps == 32 || tps == 64;
+// Slices of the key quantizer: S slices of G/S tokens per thread, with G/S one of
+// 16, 32, 64 and whole words per slice (the kernel is instantiated for those).
+int key_slices(const kvq_config *c) {
+    const int fpi = kfpi(c), pairs = c->D / 2, smax = 256 / pairs;
+    for (int s = std::min(smax, c->G); s >= 1; s--) {
+        if (c->G % s) continue;
+        const int tps = c->G / s;
+        if ((tps == 16 || tps == 32 || tps == 64) && tps % fpi == 0) return s;
+    }
+    return 0;
 }
+bool key_slices_ok(const kvq_config *c) { return key_slices(c) > 0; }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
@@ -52,6 +56,8 @@ int num_sms() {
 
 bool fast_supported(const kvq_config *c) {
     const int tok = c->bits == 2 ? 128 : 64;
+    // tiles: keys and values of one width, 2 or 4 bits (Kitty: 2-bit planes, 2-bit values)
+    if ((c->bits != 2 && c->bits != 4) || vbits_of(c) != c->bits) return false;
     if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4
     if (c->G % tok != 0 || gv_of(c) != c->D) return false;
     if (c->G & (c->G - 1)) return false;  // pages of a power-of-two size (shift arithmetic)
@@ -191,7 +197,8 @@ int kvq_config_check(const kvq_config *c) {
         c->R < 0 || c->n_boost < 0)
         return KVQ_ERR_INVALID_ARG;
     if (c->mode != KVQ_MODE_KIVI && c->mode != KVQ_MODE_KITTY) return KVQ_ERR_INVALID_ARG;
-    if (c->bits != 2 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
+    if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KVQ_ERR_UNSUPPORTED;
+    if (c->v_bits != 0 && c->v_bits != 2 && c->v_bits != 4 && c->v_bits != 8) return KVQ_ERR_UNSUPPORTED;
     if (kitty(c) && c->bits != 2) return KVQ_ERR_UNSUPPORTED;
     if (c->H_q % c->H_kv) return KVQ_ERR_INVALID_ARG;
     if (c->H_q / c->H_kv > 8) return KVQ_ERR_UNSUPPORTED;
@@ -288,7 +295,7 @@ int kvq_quant_pack_v(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
         p.src_t0 = ns;
         p.n_tok = tv;
         p.tok0 = 0;
-        ce = launch_quant_v(p, c->bits, st);
+        ce = launch_quant_v(p, vbits_of(c), st);
     }
     if (ce == cudaSuccess && vres > 0) ce = copy_rows(c, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres, st);
     if (ce == cudaSuccess && nl > 0) ce = copy_rows(c, src, L0, ns + older, k->v_local, c->R, 0, nl, st);
@@ -382,7 +389,7 @@ int kvq_flush_group(const kvq_config *c, kvq_cache *k, int *flushed_k, int *flus
         p.src_t0 = 0;
         p.n_tok = cap_v(c);
         p.tok0 = k->T_v;
-        if (launch_quant_v(p, c->bits, st) != cudaSuccess) return KVQ_ERR_CUDA;
+        if (launch_quant_v(p, vbits_of(c), st) != cudaSuccess) return KVQ_ERR_CUDA;
         k->T_v += cap_v(c);
         k->n_vres = 0;
     }
@@ -558,6 +565,7 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.D = c->D;
     p.G = c->G;
     p.bits = c->bits;
+    p.vbits = vbits_of(c);
     p.Gv = gv_of(c);
     p.n_boost = kitty(c) ? c->n_boost : 0;
     p.kitty = kitty(c) ? 1 : 0;

@@ -119,13 +119,13 @@ __device__ __forceinline__ void load_v(const DecodeParams &p, int u, int64_t tl,
     } else {
         int64_t tv = tl - p.n_sink;
         if (tv < p.T_v) {
-            const int fpi = 32 / p.bits;
+            const int fpi = 32 / p.vbits;
             const int64_t page = tv / p.G, tin = tv % p.G;
 #pragma unroll
             for (int i = 0; i < DPL; i++) {
                 const int dd = d + i;
                 uint32_t w = (uint32_t)p.v_codes[(((size_t)u * (p.max_T / p.G) + page) * (D / fpi) + dd / fpi) * p.G + tin];
-                uint32_t code = (w >> (p.bits * (dd % fpi))) & ((1u << p.bits) - 1);
+                uint32_t code = (w >> (p.vbits * (dd % fpi))) & ((1u << p.vbits) - 1);
                 float2 sm = unpack_half2(reinterpret_cast<const uint32_t *>(p.v_meta)[((size_t)u * p.max_T + tv) * (D / p.Gv) + dd / p.Gv]);
                 vv[i] = (float)code * sm.x + sm.y;
             }

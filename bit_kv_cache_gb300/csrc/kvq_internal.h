@@ -59,7 +59,7 @@ struct AppendParams {
 // CTA that completes a sequence's item count combines the slots.
 struct DecodeParams {
     // shape
-    int B, H_kv, g, D, G, bits, Gv, n_boost, kitty;
+    int B, H_kv, g, D, G, bits, vbits, Gv, n_boost, kitty;  // bits: keys, vbits: values
     int S_cap, cap_k, cap_v, R_local;
     int64_t max_T;
     // lengths

@@ -450,24 +450,26 @@ cudaError_t launch_quant_k(const QuantKParams &p_in, int bits, bool kitty, cudaS
     if (p.n_pages <= 0) return cudaSuccess;
     const int fpi = kitty ? 16 : 32 / bits;
     const int pairs = p.D / 2;
-    int smax = 256 / pairs;
-    int nwords = p.G / fpi;  // word rows per page
-    int S = 1;
-    for (int s = 1; s <= smax && s <= nwords; s++)
-        if (nwords % s == 0 && (p.G / s) <= 64) S = s;
-    int tps = p.G / S;
-    if (tps > 64 || (tps != 16 && tps != 32 && tps != 64)) return cudaErrorInvalidValue;
+    const int smax = 256 / pairs;
+    // S slices of G/S tokens per thread: G/S one of 16, 32, 64 and whole words
+    int S = 0;
+    for (int s = smax < p.G ? smax : p.G; s >= 1 && S == 0; s--)
+        if (p.G % s == 0 && (p.G / s == 16 || p.G / s == 32 || p.G / s == 64) && (p.G / s) % fpi == 0) S = s;
+    if (S == 0) return cudaErrorInvalidValue;
+    const int tps = p.G / S;
     p.slices = S;
     size_t smem = (size_t)S * p.D * 8 + (kitty ? (size_t)S * p.D * 8 + (size_t)p.D * 4 : 0);
     if (kitty) return launch_qk_tps<2, true>(p, tps, smem, st);
     if (bits == 2) return launch_qk_tps<2, false>(p, tps, smem, st);
     if (bits == 4) return launch_qk_tps<4, false>(p, tps, smem, st);
+    if (bits == 8) return launch_qk_tps<8, false>(p, tps, smem, st);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st) {
     if (p.n_tok <= 0) return cudaSuccess;
-    if (p.D == 128 && p.Gv == 128 && p.G % 128 == 0 && p.n_tok % 128 == 0 && p.tok0 % 128 == 0) {
+    if ((bits == 2 || bits == 4) && p.D == 128 && p.Gv == 128 && p.G % 128 == 0 && p.n_tok % 128 == 0 &&
+        p.tok0 % 128 == 0) {
         dim3 grid((unsigned)(p.n_tok / 128), (unsigned)p.U);
         if (bits == 2) quant_v_rows<2><<<grid, 256, 0, st>>>(p);
         else if (bits == 4) quant_v_rows<4><<<grid, 256, 0, st>>>(p);
@@ -486,6 +488,7 @@ cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st) {
     KVQ_QV(B, 32, 32) KVQ_QV(B, 32, 64) KVQ_QV(B, 32, 128) KVQ_QV(B, 32, 256)
     KVQ_QV_B(2)
     KVQ_QV_B(4)
+    KVQ_QV_B(8)
 #undef KVQ_QV_B
 #undef KVQ_QV
     return cudaErrorInvalidValue;

@@ -1,8 +1,8 @@
 /*
  * kvq.h -- C ABI of the GB300 low-bit KV-cache library (libkvq.so).
  *
- * The library quantizes the key/value cache of one attention layer into 2- or
- * 4-bit codes and runs single-query (and grouped-query) decode attention
+ * The library quantizes the key/value cache of one attention layer into 2-, 4- or
+ * 8-bit codes and runs single-query (and grouped-query) decode attention
  * directly on the packed codes.  It follows:
  *   - KIVI ("KV Cache 量化算子：KIVI"): min-max asymmetric quantization,
  *     scale = (max-min)/(2^b-1), keys per channel over groups of G tokens,
@@ -60,7 +60,12 @@ enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
  *   B, H_q, H_kv, D : batch, query heads, key/value heads (H_q % H_kv == 0), head dim
  *   G               : group / page size in tokens (keys are quantized per channel over
  *                     G tokens; values per token over Gv = min(G, D) channels)
- *   bits            : 2 or 4 (Kitty: 2; its boosted key channels reach 4 bits)
+ *   bits            : key code width, 2, 4 or 8 (Kitty: 2; its boosted key channels
+ *                     reach 4 bits)
+ *   v_bits          : value code width, 2, 4 or 8; 0 means the same as bits (the
+ *                     K4V2 / K2V4 variants of the Kitty notes, Sec. 3.1).  Equal
+ *                     widths of 2 or 4 decode on tensor-core tiles; other widths on
+ *                     the CUDA-core path.
  *   S               : fp16 attention-sink tokens kept at the start (0 = none)
  *   R               : KIVI: fp16 residual capacity, a multiple of G, flushed as R/G
  *                     groups once full.  Kitty: the value local window.
@@ -71,12 +76,13 @@ enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
 typedef struct {
     int32_t B, H_q, H_kv, D, G, bits;
     int32_t S, R, n_boost, mode;
+    int32_t v_bits;
     int64_t max_T;
 } kvq_config;
 
 /* Caller-owned device buffers and host-side lengths of one layer's cache.
- * Layouts (U = B*H_kv sequences, fpi = 32/bits codes per int32, element j of a
- * word at bit bits*j, least significant first):
+ * Layouts (U = B*H_kv sequences, fpi = 32/bits codes per int32 for keys and
+ * 32/v_bits for values, element j of a word at bit bits*j, least significant first):
  *   k_codes  int32 [U][max_T/fpi][D]     keys packed along tokens: word (w, d) holds
  *                                        tokens fpi*w .. fpi*w+fpi-1 of channel d.
  *                                        Kitty: the low 2-bit plane (fpi = 16).
@@ -117,7 +123,8 @@ const char *kvq_status_str(int status);
 
 /* Validates a configuration.  KVQ_OK, KVQ_ERR_INVALID_ARG (H_q % H_kv, G % fpi,
  * D % fpi, Gv | D, R % G (KIVI), n_boost range, max_T % G, non-positive sizes) or
- * KVQ_ERR_UNSUPPORTED (bits not 2/4, Kitty with bits != 2, D not a multiple of 8). */
+ * KVQ_ERR_UNSUPPORTED (bits or v_bits not 2/4/8, Kitty with bits != 2, D not 64,
+ * 128 or 256, more than 8 query heads per KV head). */
 int kvq_config_check(const kvq_config *cfg);
 
 /* Byte size of each cache buffer for cfg: which = 0 k_codes, 1 k_hi, 2 k_bidx,

@@ -50,6 +50,11 @@ class Workload:
     k_outlier_scale: float = 1.0
     v_outlier_prob: float = 0.0
     v_outlier_scale: float = 1.0
+    v_bits: int = 0   # value code width; 0: the same as bits
+
+    @property
+    def vbits(self) -> int:
+        return self.v_bits or self.bits
 
     @property
     def g(self) -> int:
@@ -81,6 +86,17 @@ WORKLOADS = {
     "long_128k": Workload("long_128k", B=1, H_q=32, H_kv=8, D=128, T=131072, G=128, R=128,
                           bits=2, seed=5, k_outlier_channels=6, k_outlier_scale=10.0),
 }
+
+# Key / value width variants of the Llama-3-8B GQA layer (the Kitty notes' K4V2,
+# K2V4 and K2V2-with-sinks variants, Sec. 3.1, and 8-bit codes).
+_GQA = dict(B=4, H_q=32, H_kv=8, D=128, T=32768, G=128, R=128, k_outlier_channels=6,
+            k_outlier_scale=10.0, v_outlier_prob=0.001, v_outlier_scale=20.0)
+WORKLOADS.update({
+    "llama3_8b_gqa_k4v2": Workload("llama3_8b_gqa_k4v2", bits=4, v_bits=2, seed=6, **_GQA),
+    "llama3_8b_gqa_k2v4": Workload("llama3_8b_gqa_k2v4", bits=2, v_bits=4, seed=7, **_GQA),
+    "llama3_8b_gqa_k8v8": Workload("llama3_8b_gqa_k8v8", bits=8, seed=8, **_GQA),
+    "llama3_8b_gqa_k2v2s": Workload("llama3_8b_gqa_k2v2s", bits=2, S=32, seed=9, **_GQA),
+})
 
 
 def _rng(wl: Workload, stream: int) -> np.random.Generator:

@@ -11,9 +11,9 @@ TOL_REL = 2e-3
 def make_pair(wl, max_T, device):
     import bit_kv_cache_gb300 as kvq
     gpu = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                       n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=device)
+                       n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=device, v_bits=wl.v_bits)
     ora = oracle.OracleCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                             n_boost=wl.n_boost, mode=wl.mode)
+                             n_boost=wl.n_boost, mode=wl.mode, v_bits=wl.v_bits)
     return gpu, ora
 
 
@@ -48,7 +48,7 @@ def assert_state_equal(gpu, ora, units=None):
     cfg = gpu.cfg
     kitty = ora.kitty
     kfpi = 16 if kitty else 32 // cfg.bits
-    vfpi = 32 // cfg.bits
+    vfpi = 32 // (cfg.v_bits or cfg.bits)
 
     def pick(a):
         if units is None:

@@ -48,7 +48,9 @@ def test_config_check(kvq):
     assert ok() == 0
     assert ok(bits=4) == 0 and ok(G=32, R=32) == 0
     assert ok(mode="kitty", S=32, n_boost=16) == 0
-    assert ok(bits=3) == -2 and ok(bits=8) == -2
+    assert ok(bits=3) == -2 and ok(bits=8) == 0 and ok(bits=1) == -2
+    assert ok(v_bits=4) == 0 and ok(v_bits=8) == 0 and ok(v_bits=3) == -2
+    assert ok(bits=4, v_bits=2) == 0 and ok(mode="kitty", S=32, v_bits=4) == 0
     assert ok(mode="kitty", bits=4) == -2
     assert ok(H_q=7) == -1                 # H_q % H_kv
     assert ok(H_q=32, H_kv=2) == -2        # 16 query heads per KV head
@@ -76,6 +78,15 @@ def test_buffer_bytes_match_layouts(kvq):
     kb = [kvq.lib.kvq_buffer_bytes(ctypes.byref(k), i) for i in range(10)]
     assert kb[1] == U * (T // 16) * 16 * 4 and kb[2] == U * (T // G) * D
     assert kb[6] == U * 32 * D * 2 and kb[9] == U * 128 * D * 2
+
+
+def test_buffer_bytes_of_separate_widths(kvq):
+    U, T, D = 4, 1024, 128
+    for kb, vb in ((4, 2), (2, 4), (8, 8), (2, 8)):
+        c = _cfg(kvq, bits=kb, v_bits=vb)
+        assert kvq.lib.kvq_buffer_bytes(ctypes.byref(c), 0) == U * T * D * kb // 8
+        assert kvq.lib.kvq_buffer_bytes(ctypes.byref(c), 4) == U * T * D * vb // 8
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(_cfg(kvq, bits=4, v_bits=0)), 4) == U * T * D * 4 // 8
 
 
 def test_argument_errors_before_any_launch(kvq):

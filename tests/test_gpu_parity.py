@@ -33,6 +33,12 @@ SMALL = {
     "gqa_b4": (WORKLOADS["llama3_8b_gqa_b4"].replace(B=2, H_q=16, H_kv=4, T=1024), 1024 + 100, 4),
     "kitty": (WORKLOADS["kitty"].replace(B=2, H_q=16, H_kv=4, T=1024), 32 + 1024 + 128 + 60, 4),
     "long": (WORKLOADS["long_128k"].replace(T=2048), 2048 + 64, 3),
+    # key / value width variants: K4V2, K2V4 and K8V8 run on the CUDA-core path,
+    # K2V2 with sinks on the tensor-core tiles
+    "k4v2": (WORKLOADS["llama3_8b_gqa_k4v2"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
+    "k2v4": (WORKLOADS["llama3_8b_gqa_k2v4"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
+    "k8v8": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
+    "k2v2s": (WORKLOADS["llama3_8b_gqa_k2v2s"].replace(B=2, H_q=16, H_kv=4, T=1024), 32 + 1024 + 70, 3),
 }
 
 
