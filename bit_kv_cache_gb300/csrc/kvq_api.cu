@@ -55,9 +55,9 @@ int num_sms() {
 }
 
 bool fast_supported(const kvq_config *c) {
-    const int tok = c->bits == 2 ? 128 : 64;
-    // tiles: keys and values of one width, 2 or 4 bits (Kitty: 2-bit planes, 2-bit values)
-    if ((c->bits != 2 && c->bits != 4) || vbits_of(c) != c->bits) return false;
+    const int tok = 256 / c->bits;  // a tile holds 8 key word rows
+    // tiles: any key and value widths of 2, 4, 8 bits (Kitty: 2-bit planes, 2-bit values)
+    if (kitty(c) && vbits_of(c) != 2) return false;
     if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4
     if (c->G % tok != 0 || gv_of(c) != c->D) return false;
     if (c->G & (c->G - 1)) return false;  // pages of a power-of-two size (shift arithmetic)
@@ -421,12 +421,12 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     if (!ws || !aligned16(ws) || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE;
 
     const int U = (int)units(c), g = c->H_q / c->H_kv, nsm = num_sms();
-    const int tok = c->bits == 2 ? 128 : 64;
+    const int tok = 256 / c->bits;
     // The tile paths cover: D = 128, g <= 4, pages of whole tiles, one value group per
     // token, packed values never ahead of packed keys, mixed key blocks only at 2 bits.
     bool fast = fast_supported(c) && k->T_v <= k->T_k && k->T_v % tok == 0 &&
                 (k->T_k == k->T_v || (kitty(c) && (k->T_k - k->T_v) % 16 == 0));
-    const int wpc = decode_warps_per_cta(c->bits, kitty(c), kitty(c) ? c->n_boost : 0, fast);
+    const int wpc = decode_warps_per_cta(c->bits, vbits_of(c), kitty(c), kitty(c) ? c->n_boost : 0, fast);
 
     DecodeParams p;
     memset(&p, 0, sizeof(p));

@@ -151,7 +151,7 @@ __device__ void generic_range(const DecodeParams &p, int u, const uint16_t *q_w,
     for (int64_t base = a; base < b; base += 32) {
         const int64_t j = base + lane;
         const bool valid = j < b;
-        const int64_t tl = j < p.n_sink ? j : j + p.n_fast * (p.bits == 2 ? 128 : 64);
+        const int64_t tl = j < p.n_sink ? j : j + p.n_fast * (256 / p.bits);
         float z[8];
 #pragma unroll
         for (int h = 0; h < 8; h++) z[h] = 0.f;
@@ -194,7 +194,7 @@ __device__ void generic_range(const DecodeParams &p, int u, const uint16_t *q_w,
         const int nt = (int)kvq_min64(32, b - base);
         for (int tt = 0; tt < nt; tt++) {
             const int64_t jj = base + tt;
-            const int64_t tlv = jj < p.n_sink ? jj : jj + p.n_fast * (p.bits == 2 ? 128 : 64);
+            const int64_t tlv = jj < p.n_sink ? jj : jj + p.n_fast * (256 / p.bits);
             float vv[DPL];
             load_v<DPL>(p, u, tlv, lane * DPL, vv);
 #pragma unroll
@@ -271,7 +271,7 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long
 //   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
 //      CTA resets both counters to zero for the next call.
 // ---------------------------------------------------------------------------------
-template <int BITS, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
     // Work units: a warp, or with PAIR (tile kernels) a warp pair -- query warp and
     // value warp -- that shares one region of shared memory.
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = PAIR ? warp >> 1 : warp, role = PAIR ? warp & 1 : 0;
     const int D = p.D, g = p.g;
-    const int wbytes = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).total : gen_warp_bytes(D);
-    const int part0_off = FAST ? WarpSmem<BITS>(KITTY, p.n_boost).part0 : 0;
+    const int wbytes = FAST ? WarpSmem(KB, VB, KITTY, p.n_boost).total : gen_warp_bytes(D);
+    const int part0_off = FAST ? WarpSmem(KB, VB, KITTY, p.n_boost).part0 : 0;
     unsigned char *wbase = smem + unit * wbytes;
     int seg0 = -1, seg1 = -1, cnt0 = 0, cnt1 = 0;
 
@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int x1 = pool_a(P, k + 1);
         // a unit range touches at most two sequences; the first of two segments keeps
         // its partial in the unit's part0 area, the last one in the (then idle) tile region
-        PairWarp<BITS, KITTY> pw(p, wbase);
-        MiniWarp<BITS, KITTY> mw(p, wbase, 0);
+        PairWarp<KB, VB, KITTY> pw(p, wbase);
+        MiniWarp<KB, VB, KITTY> mw(p, wbase, 0);
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
         if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // the pair's partner
         if (slot_lane >= 0 && slot_lane < nu) my_slot = atomicAdd(&p.slot_ctr[ulo + slot_lane], 1);
@@ -513,22 +513,31 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
 }
 
 // ---------------------------------------------------------------------------------
-int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast) {
+constexpr int kSmemMax = 227 * 1024;
+
+// Units (warps, or warp pairs) per CTA of a tile kernel: as many of 8, 6, 4 as fit.
+constexpr int tile_units(int kb, int vb, bool kitty, int n_boost) {
+    const int w = WarpSmem(kb, vb, kitty, n_boost).total;
+    return w * 8 <= kSmemMax ? 8 : w * 6 <= kSmemMax ? 6 : 4;
+}
+// Tile kernels on warp pairs (query warp + value warp per unit): 4-bit keys.
+constexpr bool tile_pair(int kb, int vb) { return kb == 4 && vb == 4; }
+
+int decode_warps_per_cta(int bits, int vbits, bool kitty, int n_boost, bool fast) {
     if (!fast) return 8;
-    const int w = bits == 2 ? WarpSmem<2>(kitty, n_boost).total : WarpSmem<4>(kitty, n_boost).total;
-    return w * 8 <= 227 * 1024 ? 8 : 6;
+    return tile_units(bits, vbits, kitty, n_boost);
 }
 
-size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast) {
-    const int nw = decode_warps_per_cta(bits, kitty, n_boost, fast);
-    if (fast) return (size_t)nw * (bits == 2 ? WarpSmem<2>(kitty, n_boost).total : WarpSmem<4>(kitty, n_boost).total);
+size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bool fast) {
+    const int nw = decode_warps_per_cta(bits, vbits, kitty, n_boost, fast);
+    if (fast) return (size_t)nw * WarpSmem(bits, vbits, kitty, n_boost).total;
     return (size_t)nw * gen_warp_bytes(D);
 }
 
-template <int BITS, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW>
 static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
-    const size_t smem = decode_smem_bytes(BITS, KITTY, p.n_boost, p.D, FAST);
-    auto k = decode_kernel<BITS, KITTY, FAST, PAIR, DPL, NW>;
+    const size_t smem = decode_smem_bytes(KB, VB, KITTY, p.n_boost, p.D, FAST);
+    auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW>;
     // The dynamic shared-memory limit is raised once per device to the most any
     // configuration of this instantiation asks for (the opt-in maximum).
     static int raised[64] = {0};
@@ -542,24 +551,44 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) raised[dev] = 1;
     }
-    if (smem > (size_t)(227 * 1024)) return cudaErrorInvalidValue;
+    if (smem > (size_t)kSmemMax) return cudaErrorInvalidValue;
     k<<<(unsigned)(p.C_f + p.C_m + p.C_g), NW * 32, smem, st>>>(p);
     return cudaGetLastError();
 }
 
+// KIVI tiles of key width KB and value width VB; p.wpc == tile_units(KB, VB).
+template <int KB, int VB>
+static cudaError_t launch_tiles(const DecodeParams &p, cudaStream_t st) {
+    constexpr int U = tile_units(KB, VB, false, 0);
+    constexpr bool PAIR = tile_pair(KB, VB);
+    if (p.wpc != U) return cudaErrorInvalidValue;
+    return launch_one<KB, VB, false, true, PAIR, 4, PAIR ? 2 * U : U>(p, st);
+}
+
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st) {
-    if (fast) {  // p.wpc units; 4-bit tiles run on warp pairs, the others on single warps
+    if (fast) {  // p.wpc units of one warp, or of a warp pair
         if (p.kitty) {
-            if (p.wpc == 8) return launch_one<2, true, true, false, 4, 8>(p, st);
-            return launch_one<2, true, true, false, 4, 6>(p, st);
+            if (p.wpc == 8) return launch_one<2, 2, true, true, false, 4, 8>(p, st);
+            if (p.wpc == 6) return launch_one<2, 2, true, true, false, 4, 6>(p, st);
+            return cudaErrorInvalidValue;  // n_boost <= 64 keeps 6 units in the CTA
         }
-        if (p.bits == 2) return launch_one<2, false, true, false, 4, 8>(p, st);
-        return launch_one<4, false, true, true, 4, 16>(p, st);
+        switch (p.bits * 16 + p.vbits) {
+            case 2 * 16 + 2: return launch_tiles<2, 2>(p, st);
+            case 2 * 16 + 4: return launch_tiles<2, 4>(p, st);
+            case 2 * 16 + 8: return launch_tiles<2, 8>(p, st);
+            case 4 * 16 + 2: return launch_tiles<4, 2>(p, st);
+            case 4 * 16 + 4: return launch_tiles<4, 4>(p, st);
+            case 4 * 16 + 8: return launch_tiles<4, 8>(p, st);
+            case 8 * 16 + 2: return launch_tiles<8, 2>(p, st);
+            case 8 * 16 + 4: return launch_tiles<8, 4>(p, st);
+            case 8 * 16 + 8: return launch_tiles<8, 8>(p, st);
+        }
+        return cudaErrorInvalidValue;
     }
     switch (p.D) {
-        case 64: return launch_one<2, false, false, false, 2, 8>(p, st);
-        case 128: return launch_one<2, false, false, false, 4, 8>(p, st);
-        case 256: return launch_one<2, false, false, false, 8, 8>(p, st);
+        case 64: return launch_one<2, 2, false, false, false, 2, 8>(p, st);
+        case 128: return launch_one<2, 2, false, false, false, 4, 8>(p, st);
+        case 256: return launch_one<2, 2, false, false, false, 8, 8>(p, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -30,37 +30,58 @@ constexpr float kQScale = 0.0625f;  // q is folded as q * 2^-4 (exact) to keep q
 constexpr int kSlots = 4;           // copy mbarriers per unit (fast: 2 key halves, 2 value halves)
 constexpr int kBars = 9;            // + warp-pair handoff: p' full x2, p' empty x2, query side done
 
-__host__ __device__ inline int hi_stride(int nb) { return nb * 4 + 16; }
+__host__ __device__ constexpr int hi_stride(int nb) { return nb * 4 + 16; }
 // A warp / CTA partial: 8 head rows of prow(D) floats: o[0..D), m at D, l at D+1
 // (rows padded to 16 bytes for vector access).
-__host__ __device__ inline int prow(int D) { return D + 4; }
+__host__ __device__ constexpr int prow(int D) { return D + 4; }
 __host__ __device__ inline int part_bytes(int D) { return 8 * prow(D) * 4; }
 
-template <int BITS>
+// Code-width constants of the register extraction.  A packed word holds FPI codes of
+// B bits; after split(), each 16-bit half of a register holds FPI/2 of them, and row
+// set J of an mma reads code J of every half as an exact fp16 subnormal (code *
+// 2^(B JJ - 24)) through one AND.  Codes above bit 9 of a half would reach the
+// exponent field, so row sets J >= JDIRECT read a copy of the register shifted right
+// by SH.
+template <int B>
+struct Codes {
+    static constexpr int FPI = 32 / B;
+    static constexpr int NJ = FPI / 2;                         // mma row sets per word: 8, 4 or 2
+    static constexpr int JDIRECT = B == 2 ? 5 : B == 4 ? 2 : 1;
+    static constexpr int SH = B == 2 ? 6 : 8;
+    static constexpr uint32_t MASK0 = ((1u << B) - 1u) | (((1u << B) - 1u) << 16);
+    template <int J>
+    __device__ __forceinline__ static constexpr int jj() { return J < JDIRECT ? J : J - SH / B; }
+};
+
+// A packed tile: TOK tokens of keys (8 word rows of KB-bit codes, D channels) and of
+// values (D / VFPI word rows of VB-bit codes, TOK tokens).  P is the token (and key
+// channel) pairing of split(): a register pairs the values at offsets t and t + P of
+// a 16-wide slab; it is chosen so that the two tokens of a lane's QK rows g and g+8
+// (KFPI / 2 apart) land next to each other in the p' row.
+template <int KB, int VB>
 struct Tile {
+    using K = Codes<KB>;
+    using V = Codes<VB>;
     static constexpr int D = 128;
-    static constexpr int FPI = 32 / BITS;
-    static constexpr int TOK = BITS == 2 ? 128 : 64;   // tokens per packed tile (8 key word rows)
-    static constexpr int K_STRIDE = D * 4 + 16;        // padded key row: conflict-free ldmatrix
-    static constexpr int V_ROWS = D / FPI;             // value channel blocks: 8 or 16
+    static constexpr int TOK = 8 * K::FPI;                  // 128, 64 or 32 tokens
+    static constexpr int P = KB == 2 ? 8 : 4;
+    static constexpr bool P_ADJ = K::FPI / 2 == P;          // a lane's two p' values are adjacent
+    static constexpr int K_STRIDE = D * 4 + 16;             // padded key row: conflict-free ldmatrix
+    static constexpr int V_ROWS = D / V::FPI;               // value channel blocks: 8, 16 or 32
     static constexpr int V_STRIDE = TOK * 4 + 16;
-    static constexpr int NJ = FPI / 2;                 // mma row sets per word: 8 or 4
-    static constexpr int NSET = V_ROWS / 8;            // 1 or 2
-    static constexpr int TSLABS = TOK / 16;            // 16-token slabs for PV
-    static constexpr int JDIRECT = BITS == 2 ? 5 : 2;  // row sets readable without a pre-shift
-    static constexpr int SH = BITS == 2 ? 6 : 8;       // pre-shift for the others
-    static constexpr uint32_t MASK0 = BITS == 2 ? 0x00030003u : 0x000F000Fu;
-    static constexpr int PS = BITS == 2 ? 8 : 4;       // k = 2t+1 pairs token/channel t with t + PS
+    static constexpr int NSET = V_ROWS / 8;                 // 1, 2 or 4 sets of 8 word rows
+    static constexpr int TSLABS = TOK / 16;                 // 16-token slabs for PV
+    static constexpr int PV_STEPS = TSLABS * NSET;          // one ldmatrix + split each
     // key half-stage
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_KM = 8 * K_STRIDE;        // (scale, min) per channel, 512 B
-    static constexpr int OFF_HI = OFF_KM + D * 4;      // Kitty: 8 rows of hi_stride(nb), then D bytes of index
+    static constexpr int OFF_KM = 8 * K_STRIDE;             // (scale, min) per channel, 512 B
+    static constexpr int OFF_HI = OFF_KM + D * 4;           // Kitty: 8 rows of hi_stride(nb), then D bytes of index
     // value half-stage
     static constexpr int OFF_V = 0;
-    static constexpr int OFF_VM = V_ROWS * V_STRIDE;   // (scale, min) per token
+    static constexpr int OFF_VM = V_ROWS * V_STRIDE;        // (scale, min) per token
     static constexpr int V_HALF = OFF_VM + TOK * 4;
-    static constexpr int PROW = TOK + 8;               // p' row (halves), padded
-    static constexpr int PBUF = 4 * PROW * 2;          // one p' buffer: heads 0..3
+    static constexpr int PROW = TOK + 8;                    // p' row (halves), padded
+    static constexpr int PBUF = 4 * PROW * 2;               // one p' buffer: heads 0..3
 };
 
 constexpr int kMiniRow = 128 * 2 + 16;                 // padded fp16 row of the mini tiles
@@ -75,15 +96,16 @@ __host__ __device__ constexpr int round128(int x) { return (x + 127) & ~127; }
 // The tile region holds, for a fast warp, two key halves (codes + (scale, min) per
 // channel [+ Kitty planes]), two value-code halves and two value (scale, min) rows;
 // for a mini warp, four 16-row halves.  After the tiles it holds the warp's partial.
-template <int BITS>
 struct WarpSmem {
-    int ksz, vsz, vmsz, mslot, k0, v0, vm0, region;
-    int pbuf, qraw, qpair, invb, bars, stats, alpha, part0, total;
-    __host__ __device__ WarpSmem(bool kitty, int nb) {
-        using T = Tile<BITS>;
-        ksz = round128(T::OFF_HI + (kitty ? 8 * hi_stride(nb) + T::D : 0));
-        vsz = round128(T::V_ROWS * T::V_STRIDE);
-        vmsz = round128(T::TOK * 4);
+    int ksz = 0, vsz = 0, vmsz = 0, mslot = 0, k0 = 0, v0 = 0, vm0 = 0, region = 0;
+    int pbuf = 0, qraw = 0, qpair = 0, invb = 0, bars = 0, stats = 0, alpha = 0, part0 = 0, total = 0;
+    // kb, vb: key and value code widths of the tile (2, 4 or 8)
+    __host__ __device__ constexpr WarpSmem(int kb, int vb, bool kitty, int nb) {
+        const int D = 128, tok = 256 / kb, v_rows = D * vb / 32;
+        const int off_hi = 8 * (D * 4 + 16) + D * 4, pbuf1 = 4 * (tok + 8) * 2;
+        ksz = round128(off_hi + (kitty ? 8 * hi_stride(nb) + D : 0));
+        vsz = round128(v_rows * (tok * 4 + 16));
+        vmsz = round128(tok * 4);
         const int mk = 1024 + ((4 * nb + 15) & ~15) + 128;  // mini packed-key block
         mslot = round128(kMiniHalf > mk ? kMiniHalf : mk);
         k0 = 0;
@@ -92,7 +114,7 @@ struct WarpSmem {
         region = vm0 + 2 * vmsz;
         if (region < kSlots * mslot) region = kSlots * mslot;
         pbuf = region;
-        qraw = pbuf + 2 * T::PBUF;
+        qraw = pbuf + 2 * pbuf1;
         qpair = qraw + 4 * 128 * 2;
         invb = qpair + 4 * 8 * 4 * 8;
         bars = invb + 64;
@@ -208,19 +230,21 @@ __device__ __forceinline__ void issue_copy(void *dst, const void *src, uint32_t 
 // ---------------------------------------------------------------------------
 // Packed tiles
 // ---------------------------------------------------------------------------
-template <int BITS, bool KITTY>
+template <int KB, int VB, bool KITTY>
 struct FastWarp {
-    using T = Tile<BITS>;
+    using T = Tile<KB, VB>;
+    using CK = typename T::K;
+    using CV = typename T::V;
     const DecodeParams &p;
     unsigned char *wbase;
-    WarpSmem<BITS> L;
+    WarpSmem L;
     int u, lane;
     uint64_t *bars;
     uint32_t phase = 0;    // bit s: parity of the next completion of slot s
     uint32_t pending = 0;  // bit s: slot s has copies in flight
 
     __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
-        : p(pp), wbase(wb), L(KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
+        : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
         bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
     }
     __device__ unsigned char *kslot(int s) const { return wbase + L.k0 + s * L.ksz; }
@@ -257,7 +281,7 @@ struct FastWarp {
         const int i = lane;
         if (i < 8) {
             issue_copy(st + T::OFF_K + i * T::K_STRIDE,
-                       p.k_codes + ((size_t)u * (p.max_T / T::FPI) + ti * 8 + i) * T::D, T::D * 4, &bars[s]);
+                       p.k_codes + ((size_t)u * (p.max_T / CK::FPI) + ti * 8 + i) * T::D, T::D * 4, &bars[s]);
         } else if (i == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
                        &bars[s]);
@@ -291,28 +315,30 @@ struct FastWarp {
             issue_copy(st + i * T::V_STRIDE,
                        p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * T::V_ROWS + i) * p.G + off, T::TOK * 4,
                        &bars[s]);
-        } else if (i == T::V_ROWS && meta) {
+        }
+        if (i == T::V_ROWS % 32 && meta) {  // 8-bit values: every lane has a row, lane 0 also the meta
             issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)u * p.max_T + (ti + 1) * T::TOK) * 2, T::TOK * 4,
                        &bars[s]);
         }
     }
 
-    // 4 A registers of row set J from the split words (rows g / g+8, k pairs).
-    template <int J>
+    // 4 A registers of row set J (code width of C) from the split words (rows g /
+    // g+8, k pairs).
+    template <typename C, int J>
     __device__ __forceinline__ static void frag(const uint32_t (&x)[4], const uint32_t (&xs)[4], uint32_t (&a)[4]) {
-        constexpr int JJ = J < T::JDIRECT ? J : J - (T::SH / BITS);
-        constexpr uint32_t M = T::MASK0 << (BITS * JJ);
+        constexpr uint32_t M = C::MASK0 << (32 / C::FPI * C::template jj<J>());
 #pragma unroll
-        for (int r = 0; r < 4; r++) a[r] = (J < T::JDIRECT ? x[r] : xs[r]) & M;
+        for (int r = 0; r < 4; r++) a[r] = (J < C::JDIRECT ? x[r] : xs[r]) & M;
     }
-    template <int J>
+    template <typename C, int J>
     __device__ __forceinline__ static constexpr float unscale() {
-        return (float)(1u << (24 - BITS * (J < T::JDIRECT ? J : J - (T::SH / BITS))));
+        return (float)(1u << (24 - 32 / C::FPI * C::template jj<J>()));
     }
     // ldmatrix words W0..W3 (segments c = 0..3) -> k-paired registers (k = 2t, 2t+1 |
-    // 2t+8, 2t+9) for rows g (low halves) and g+8 (high halves).
+    // 2t+8, 2t+9) for rows g (low halves) and g+8 (high halves); xs: x >> SH of C.
+    template <typename C>
     __device__ __forceinline__ static void split(const uint32_t (&w)[4], uint32_t (&x)[4], uint32_t (&xs)[4]) {
-        if (BITS == 2) {  // pairs (t, t+8) and (t+4, t+12)
+        if (T::P == 8) {  // pairs (t, t+8) and (t+4, t+12)
             x[0] = prmt(w[0], w[2], 0x5410);
             x[1] = prmt(w[0], w[2], 0x7632);
             x[2] = prmt(w[1], w[3], 0x5410);
@@ -324,29 +350,31 @@ struct FastWarp {
             x[3] = prmt(w[2], w[3], 0x7632);
         }
 #pragma unroll
-        for (int r = 0; r < 4; r++) xs[r] = x[r] >> T::SH;
+        for (int r = 0; r < 4; r++) xs[r] = x[r] >> C::SH;
     }
-    // Z: the first slab of a tile, whose accumulators start from zero.
+    // S row sets of a key slab.  Z: the first slab of a tile, whose accumulators start
+    // from zero.
     template <bool Z = false>
-    __device__ __forceinline__ static void mma_sets(float (&acc)[T::NJ][4], const uint32_t (&x)[4],
+    __device__ __forceinline__ static void mma_sets(float (&acc)[CK::NJ][4], const uint32_t (&x)[4],
                                                     const uint32_t (&xs)[4], uint32_t b0, uint32_t b1) {
         uint32_t a[4];
 #define KVQ_RS(J)                                                                      \
-    if (J < T::NJ) {                                                                   \
-        frag<J>(x, xs, a);                                                             \
-        if (Z) mma_16816_z(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1);            \
-        else mma_16816(acc[J % T::NJ], a[0], a[1], a[2], a[3], b0, b1);               \
+    if (J < CK::NJ) {                                                                  \
+        frag<CK, J>(x, xs, a);                                                         \
+        if (Z) mma_16816_z(acc[J % CK::NJ], a[0], a[1], a[2], a[3], b0, b1);           \
+        else mma_16816(acc[J % CK::NJ], a[0], a[1], a[2], a[3], b0, b1);              \
     }
         KVQ_RS(0) KVQ_RS(1) KVQ_RS(2) KVQ_RS(3) KVQ_RS(4) KVQ_RS(5) KVQ_RS(6) KVQ_RS(7)
 #undef KVQ_RS
     }
+    // O row sets of value channel set `set`.
     __device__ __forceinline__ static void mma_sets_o(float (&O)[8][4], int set, const uint32_t (&x)[4],
                                                       const uint32_t (&xs)[4], uint32_t b0, uint32_t b1) {
         uint32_t a[4];
 #define KVQ_RS(J)                                                                  \
-    if (J < T::NJ) {                                                               \
-        frag<J>(x, xs, a);                                                         \
-        mma_16816(O[set * T::NJ + (J % T::NJ)], a[0], a[1], a[2], a[3], b0, b1);  \
+    if (J < CV::NJ) {                                                              \
+        frag<CV, J>(x, xs, a);                                                     \
+        mma_16816(O[set * CV::NJ + (J % CV::NJ)], a[0], a[1], a[2], a[3], b0, b1); \
     }
         KVQ_RS(0) KVQ_RS(1) KVQ_RS(2) KVQ_RS(3) KVQ_RS(4) KVQ_RS(5) KVQ_RS(6) KVQ_RS(7)
 #undef KVQ_RS
@@ -354,24 +382,25 @@ struct FastWarp {
 
     // One 16-channel slab of S = Kcodes . q' (+ the min mma) for the key half in st;
     // slab 0 starts the accumulators from zero.
-    __device__ __forceinline__ void qk_slab(int sl, const unsigned char *st, float (&acc)[T::NJ][4],
+    __device__ __forceinline__ void qk_slab(int sl, const unsigned char *st, float (&acc)[CK::NJ][4],
                                             float (&cm)[4]) const {
         const int gq = lane >> 2, t = lane & 3;
         const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
         const uint2 qp = reinterpret_cast<const uint2 *>(wbase + L.qpair)[((gq >> 1) * 8 + sl) * 4 + t];
-        const SlabB b = slab_b(qp, km[chan_of<T::PS>(sl, t, 0)], km[chan_of<T::PS>(sl, t, 1)],
-                               km[chan_of<T::PS>(sl, t, 2)], km[chan_of<T::PS>(sl, t, 3)], col_const((gq & 1) != 0));
+        const SlabB b = slab_b(qp, km[chan_of<T::P>(sl, t, 0)], km[chan_of<T::P>(sl, t, 1)],
+                               km[chan_of<T::P>(sl, t, 2)], km[chan_of<T::P>(sl, t, 3)], col_const((gq & 1) != 0));
         if (sl == 0) mma_16816_z(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
         else mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
         uint32_t w[4], x[4], xs[4];
         ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3) + 64 * sl);
-        split(w, x, xs);
+        split<CK>(w, x, xs);
         if (sl == 0) mma_sets<true>(acc, x, xs, b.b0, b.b1);
         else mma_sets<false>(acc, x, xs, b.b0, b.b1);
     }
 
     // Kitty: S += hi-plane codes . (4 q') over the boosted slots.
-    __device__ void qk_boost(const unsigned char *st, float (&acc)[T::NJ][4]) const {
+    __device__ void qk_boost(const unsigned char *st, float (&acc)[CK::NJ][4]) const {
+        static_assert(!KITTY || KB == 2, "Kitty planes are 2-bit");
         const int gq = lane >> 2, t = lane & 3, hq = gq >> 1;
         const int nb = p.n_boost;
         const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
@@ -392,7 +421,7 @@ struct FastWarp {
             uint16_t qv[4];
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
-                const int ch = invb[chan_of<T::PS>(s2, t, kk)] & (T::D - 1);
+                const int ch = invb[chan_of<T::P>(s2, t, kk)] & (T::D - 1);
                 km4[kk] = km[ch];
                 qv[kk] = qraw[hq * 128 + ch];
             }
@@ -403,7 +432,7 @@ struct FastWarp {
             const SlabB b = slab_b(make_uint2(q2[0], q2[1]), km4[0], km4[1], km4[2], km4[3], col_const((gq & 1) != 0));
             uint32_t w[4], x[4], xs[4];
             ldmatrix_x4(w, hb + 64 * s2);
-            split(w, x, xs);
+            split<CK>(w, x, xs);
             mma_sets(acc, x, xs, b.b0, b.b1);
         }
         __syncwarp();
@@ -418,7 +447,7 @@ struct FastWarp {
         if (gq < 4) bp = *reinterpret_cast<const uint2 *>(pb + gq * T::PROW + 16 * sl + 4 * t);
         uint32_t w[4], x[4], xs[4];
         ldmatrix_x4(w, smem_u32(st) + (set * 8 + (lane & 7)) * T::V_STRIDE + 16 * (lane >> 3) + 64 * sl);
-        split(w, x, xs);
+        split<CV>(w, x, xs);
         mma_sets_o(O, set, x, xs, bp.x, bp.y);
     }
 
@@ -426,8 +455,8 @@ struct FastWarp {
     // the new running maximum, l and mn rescaled to it.  Returns the factors by which
     // O must be rescaled once the previous tile's PV is in (a0 / a1: columns 2t /
     // 2t+1); *grow tells whether any head's maximum rose.
-    __device__ __forceinline__ void softmax_begin(const float (&acc)[T::NJ][4], const float (&cm)[4],
-                                                  float (&z)[T::NJ][2], float &m, float &l, float &mn,
+    __device__ __forceinline__ void softmax_begin(const float (&acc)[CK::NJ][4], const float (&cm)[4],
+                                                  float (&z)[CK::NJ][2], float &m, float &l, float &mn,
                                                   float &a0, float &a1, bool &grow) const {
         float a;
         softmax_begin_a(acc, cm, z, m, l, mn, a, grow);
@@ -436,18 +465,18 @@ struct FastWarp {
         a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
     }
     // The same; `a` is the rescale factor of the lane's head (lane & 3).
-    __device__ __forceinline__ void softmax_begin_a(const float (&acc)[T::NJ][4], const float (&cm)[4],
-                                                    float (&z)[T::NJ][2], float &m, float &l, float &mn,
+    __device__ __forceinline__ void softmax_begin_a(const float (&acc)[CK::NJ][4], const float (&cm)[4],
+                                                    float (&z)[CK::NJ][2], float &m, float &l, float &mn,
                                                     float &a, bool &grow) const {
         const float C = kLog2e * rsqrtf((float)T::D) / kQScale;
         const float cst = cm[0] * C;  // row g, column 2t: sum_d q_d min_d of head t
         float tm = -INFINITY;
 #define KVQ_Z(J)                                                                        \
-    if (J < T::NJ) {                                                                    \
-        const float f = unscale<J>() * C;                                               \
-        z[J % T::NJ][0] = fmaf(acc[J % T::NJ][0] + acc[J % T::NJ][1], f, cst);          \
-        z[J % T::NJ][1] = fmaf(acc[J % T::NJ][2] + acc[J % T::NJ][3], f, cst);          \
-        tm = fmaxf(tm, fmaxf(z[J % T::NJ][0], z[J % T::NJ][1]));                        \
+    if (J < CK::NJ) {                                                                   \
+        const float f = unscale<CK, J>() * C;                                           \
+        z[J % CK::NJ][0] = fmaf(acc[J % CK::NJ][0] + acc[J % CK::NJ][1], f, cst);       \
+        z[J % CK::NJ][1] = fmaf(acc[J % CK::NJ][2] + acc[J % CK::NJ][3], f, cst);       \
+        tm = fmaxf(tm, fmaxf(z[J % CK::NJ][0], z[J % CK::NJ][1]));                      \
     }
         KVQ_Z(0) KVQ_Z(1) KVQ_Z(2) KVQ_Z(3) KVQ_Z(4) KVQ_Z(5) KVQ_Z(6) KVQ_Z(7)
 #undef KVQ_Z
@@ -461,25 +490,38 @@ struct FastWarp {
         mn *= a;
     }
 
-    // Softmax of a tile, row set j: p = exp2(z - m) of the lane's two tokens, their
-    // sums, and p' = p * scale_v into the tile's p' buffer.
-    __device__ __forceinline__ void softmax_chunk(int j, const float (&z)[T::NJ][2], const unsigned char *vms,
+    // Position of tile token tk in a p' row: the k index of the PV B operand under the
+    // pairing of split() (slab tk / 16; segment c = (tk % 16) / 4 and lane t = tk % 4
+    // of the ldmatrix words).
+    __device__ __forceinline__ static int ppos(int tk) {
+        const int c = (tk >> 2) & 3, cp = T::P == 8 ? ((c & 1) << 1) | (c >> 1) : c;
+        return 16 * (tk >> 4) + 4 * (tk & 3) + cp;
+    }
+
+    // Softmax of a tile, row set j: p = exp2(z - m) of the lane's two tokens (rows g
+    // and g+8: tokens KFPI g + j and KFPI g + KFPI/2 + j), their sums, and p' = p *
+    // scale_v into the tile's p' buffer.
+    __device__ __forceinline__ void softmax_chunk(int j, const float (&z)[CK::NJ][2], const unsigned char *vms,
                                                   uint16_t *pb, float m, float &l, float &mn) const {
         const int gq = lane >> 2, t = lane & 3;
-        // value (scale, min) of the lane's tokens: 2 bits 16g..16g+15, 4 bits 8g..8g+7
-        const uint32_t *vm = reinterpret_cast<const uint32_t *>(vms) + (BITS == 2 ? 16 : 8) * gq;
-        const int i0 = j, i1 = BITS == 2 ? j + 8 : j + 4;  // tokens of rows g and g+8 of row set j
-        const float2 sm0 = unpack_half2(vm[i0]), sm1 = unpack_half2(vm[i1]);
+        const int tk0 = CK::FPI * gq + j, tk1 = tk0 + CK::FPI / 2;
+        const uint32_t *vm = reinterpret_cast<const uint32_t *>(vms);
+        const float2 sm0 = unpack_half2(vm[tk0]), sm1 = unpack_half2(vm[tk1]);
         const float p0 = exp2f(z[j][0] - m), p1 = exp2f(z[j][1] - m);
         l += p0 + p1;
         mn = fmaf(p0, sm0.y, fmaf(p1, sm1.y, mn));
-        const int pos = BITS == 2 ? 16 * gq + 4 * (j & 3) + 2 * (j >> 2) : 16 * (gq >> 1) + 4 * j + 2 * (gq & 1);
-        *reinterpret_cast<uint32_t *>(pb + t * T::PROW + pos) = pack_half2(p0 * sm0.x, p1 * sm1.x);
+        uint16_t *row = pb + t * T::PROW;
+        if (T::P_ADJ) {
+            *reinterpret_cast<uint32_t *>(row + ppos(tk0)) = pack_half2(p0 * sm0.x, p1 * sm1.x);
+        } else {
+            row[ppos(tk0)] = __half_as_ushort(__float2half_rn(p0 * sm0.x));
+            row[ppos(tk1)] = __half_as_ushort(__float2half_rn(p1 * sm1.x));
+        }
     }
 
-    __device__ __forceinline__ void zero(float (&a)[T::NJ][4], float (&cm)[4]) const {
+    __device__ __forceinline__ void zero(float (&a)[CK::NJ][4], float (&cm)[4]) const {
 #pragma unroll
-        for (int j = 0; j < T::NJ; j++)
+        for (int j = 0; j < CK::NJ; j++)
 #pragma unroll
             for (int e = 0; e < 4; e++) a[j][e] = 0.f;
 #pragma unroll
@@ -501,7 +543,7 @@ struct FastWarp {
         issue_kb(t0, 0);
         issue_vb(t0, 0, n);
         if (n > 1) issue_kb(t0, 1);
-        store_q_warp<T::PS>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw),
+        store_q_warp<T::P>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw),
                             reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb0 = reinterpret_cast<uint16_t *>(wbase + L.pbuf);
         for (int i = lane; i < 4 * T::PROW; i += 32)  // both p' buffers (2 x 4 rows)
@@ -513,8 +555,8 @@ struct FastWarp {
         for (int o = 0; o < 8; o++)
 #pragma unroll
             for (int e = 0; e < 4; e++) O[o][e] = 0.f;
-        float acc[T::NJ][4], cm[4];
-        float z[T::NJ][2];
+        float acc[CK::NJ][4], cm[4];
+        float z[CK::NJ][2];
         bool ok = true;
 
         // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
@@ -527,7 +569,7 @@ struct FastWarp {
             bool grow;
             softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
 #pragma unroll
-            for (int j = 0; j < T::NJ; j++) softmax_chunk(j, z, vmslot(0), pb0, m, l, mn);
+            for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vmslot(0), pb0, m, l, mn);
         }
         __syncwarp();
         fence_proxy_async();
@@ -541,16 +583,21 @@ struct FastWarp {
             ok &= wait_slot(2 + cur);        // V(i): codes of i, (scale, min) of i+1
             if (!ok) break;
             const uint16_t *pb = pb0 + cur * 4 * T::PROW;
-            if (more) {
+            if (more) {  // the PV steps spread evenly over the 8 key slabs
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
-                    pv_step(sl, vslot(cur), pb, O);
+                    if (T::PV_STEPS >= 8) {
+#pragma unroll
+                        for (int r = 0; r < T::PV_STEPS / 8; r++) pv_step(sl * (T::PV_STEPS / 8) + r, vslot(cur), pb, O);
+                    } else if (sl % (8 / T::PV_STEPS) == 0) {
+                        pv_step(sl / (8 / T::PV_STEPS), vslot(cur), pb, O);
+                    }
                     qk_slab(sl, kslot(nxt), acc, cm);
                 }
                 if (KITTY && p.n_boost > 0) qk_boost(kslot(nxt), acc);
             } else {
 #pragma unroll
-                for (int sl = 0; sl < 8; sl++) pv_step(sl, vslot(cur), pb, O);
+                for (int s = 0; s < T::PV_STEPS; s++) pv_step(s, vslot(cur), pb, O);
             }
             if (more) {
                 float a0, a1;
@@ -567,7 +614,7 @@ struct FastWarp {
                 }
                 uint16_t *pbn = pb0 + nxt * 4 * T::PROW;
 #pragma unroll
-                for (int j = 0; j < T::NJ; j++) softmax_chunk(j, z, vmslot(nxt), pbn, m, l, mn);
+                for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vmslot(nxt), pbn, m, l, mn);
             }
             __syncwarp();
             fence_proxy_async();
@@ -595,12 +642,12 @@ struct FastWarp {
         const float mn1 = __shfl_sync(0xffffffffu, mn, (lane & ~3) | ((2 * t + 1) & 3));
         __syncwarp();
 #define KVQ_SO(J)                                                                  \
-    if (J < T::NJ && t < 2) {                                                      \
-        const float f = unscale<J>();                                              \
+    if (J < CV::NJ && t < 2) {                                                     \
+        const float f = unscale<CV, J>();                                          \
         for (int set = 0; set < T::NSET; set++) {                                  \
-            const int o = set * T::NJ + (J % T::NJ);                               \
-            const int ch = T::FPI * (gq + 8 * set) + (J % T::NJ);                  \
-            const int ch2 = ch + T::FPI / 2;                                       \
+            const int o = set * CV::NJ + (J % CV::NJ);                             \
+            const int ch = CV::FPI * (gq + 8 * set) + (J % CV::NJ);                \
+            const int ch2 = ch + CV::FPI / 2;                                      \
             part[(2 * t) * (T::D + 4) + ch] = fmaf(O[o][0], f, mn0);               \
             part[(2 * t + 1) * (T::D + 4) + ch] = fmaf(O[o][1], f, mn1);           \
             part[(2 * t) * (T::D + 4) + ch2] = fmaf(O[o][2], f, mn0);              \
@@ -623,10 +670,12 @@ struct FastWarp {
 // streams the value codes, rescales O and runs PV.  Handoff per p' buffer b:
 // "full" (query -> value) and "empty" (value -> query) mbarriers, waits bounded.
 // ---------------------------------------------------------------------------
-template <int BITS, bool KITTY>
-struct PairWarp : FastWarp<BITS, KITTY> {
-    using Base = FastWarp<BITS, KITTY>;
+template <int KB, int VB, bool KITTY>
+struct PairWarp : FastWarp<KB, VB, KITTY> {
+    using Base = FastWarp<KB, VB, KITTY>;
     using T = typename Base::T;
+    using CK = typename T::K;
+    using CV = typename T::V;
     static constexpr int B_FULL = 4, B_EMPTY = 6, B_QDONE = 8;
 
     __device__ PairWarp(const DecodeParams &pp, unsigned char *ub) : Base(pp, ub) {}
@@ -658,7 +707,7 @@ struct PairWarp : FastWarp<BITS, KITTY> {
         const int u = this->u;
         if (lane < 8) {
             issue_copy(st + T::OFF_K + lane * T::K_STRIDE,
-                       p.k_codes + ((size_t)u * (p.max_T / T::FPI) + ti * 8 + lane) * T::D, T::D * 4,
+                       p.k_codes + ((size_t)u * (p.max_T / CK::FPI) + ti * 8 + lane) * T::D, T::D * 4,
                        &this->bars[s]);
         } else if (lane == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
@@ -706,10 +755,10 @@ struct PairWarp : FastWarp<BITS, KITTY> {
         const QRegs qr = load_q_regs(this->p, uu);
         issue_kq(t0, 0);
         if (n > 1) issue_kq(t0, 1);
-        store_q_warp<T::PS>(qr, reinterpret_cast<uint16_t *>(this->wbase + this->L.qraw),
+        store_q_warp<T::P>(qr, reinterpret_cast<uint16_t *>(this->wbase + this->L.qraw),
                             reinterpret_cast<uint2 *>(this->wbase + this->L.qpair));
         float m = -INFINITY, l = 0.f, mn = 0.f;
-        float acc[T::NJ][4], cm[4], z[T::NJ][2];
+        float acc[CK::NJ][4], cm[4], z[CK::NJ][2];
         bool ok = true;
         for (int64_t j = 0; j < n && ok; j++) {
             const int s = (int)(j & 1);
@@ -725,7 +774,7 @@ struct PairWarp : FastWarp<BITS, KITTY> {
             if (!ok) break;
             uint16_t *pb = pbuf(s);
 #pragma unroll
-            for (int jj = 0; jj < T::NJ; jj++) this->softmax_chunk(jj, z, this->vmslot(s), pb, m, l, mn);
+            for (int jj = 0; jj < CK::NJ; jj++) this->softmax_chunk(jj, z, this->vmslot(s), pb, m, l, mn);
             if (lane < 4) alpha()[8 * s + lane] = a;
             arrive(B_FULL + s);
             fence_proxy_async();
@@ -781,7 +830,7 @@ struct PairWarp : FastWarp<BITS, KITTY> {
             }
             const uint16_t *pb = pbuf(s);
 #pragma unroll
-            for (int sl = 0; sl < 8; sl++) this->pv_step(sl, this->vslot(s), pb, O);
+            for (int sl = 0; sl < T::PV_STEPS; sl++) this->pv_step(sl, this->vslot(s), pb, O);
             arrive(B_EMPTY + s);
             fence_proxy_async();
             if (j + 2 < n) issue_vp(t0, (int)j + 2);  // value half s is free
@@ -791,12 +840,12 @@ struct PairWarp : FastWarp<BITS, KITTY> {
         const float *st = stats();
         const float mn0 = st[8 + ((2 * t) & 3)], mn1 = st[8 + ((2 * t + 1) & 3)];
 #define KVQ_SP(J)                                                                  \
-    if (J < T::NJ && t < 2) {                                                      \
-        const float f = Base::template unscale<J>();                               \
+    if (J < CV::NJ && t < 2) {                                                     \
+        const float f = Base::template unscale<CV, J>();                           \
         for (int set = 0; set < T::NSET; set++) {                                  \
-            const int o = set * T::NJ + (J % T::NJ);                               \
-            const int ch = T::FPI * (gq + 8 * set) + (J % T::NJ);                  \
-            const int ch2 = ch + T::FPI / 2;                                       \
+            const int o = set * CV::NJ + (J % CV::NJ);                             \
+            const int ch = CV::FPI * (gq + 8 * set) + (J % CV::NJ);                \
+            const int ch2 = ch + CV::FPI / 2;                                      \
             part[(2 * t) * (T::D + 4) + ch] = fmaf(O[o][0], f, mn0);               \
             part[(2 * t + 1) * (T::D + 4) + ch] = fmaf(O[o][1], f, mn1);           \
             part[(2 * t) * (T::D + 4) + ch2] = fmaf(O[o][2], f, mn0);              \
@@ -825,7 +874,7 @@ struct MiniTile {
 
 __device__ __forceinline__ MiniTile mini_tile(const DecodeParams &p, int64_t mi) {
     MiniTile m;
-    const int64_t ms = (p.n_sink + 15) >> 4, tok_fast = p.n_fast * (p.bits == 2 ? 128 : 64);
+    const int64_t ms = (p.n_sink + 15) >> 4, tok_fast = p.n_fast * (256 / p.bits);
     const int64_t mp = (p.T_k - tok_fast) >> 4;
     if (mi < ms) {
         m.tok0 = 16 * mi;
@@ -857,11 +906,11 @@ __device__ __forceinline__ const uint16_t *krow16(const DecodeParams &p, int u, 
     return p.k_res + ((size_t)u * p.cap_k + (tl - p.n_sink - p.T_k)) * 128;
 }
 
-template <int BITS, bool KITTY>
+template <int KB, int VB, bool KITTY>
 struct MiniWarp {
     const DecodeParams &p;
     unsigned char *wbase;
-    WarpSmem<BITS> L;  // the CTA's per-warp layout (slots are large enough for a mini tile)
+    WarpSmem L;  // the CTA's per-warp layout (slots are large enough for a mini tile)
     int u, lane;
     uint64_t *bars;
     uint32_t phase = 0, pending = 0;
@@ -870,7 +919,7 @@ struct MiniWarp {
     static constexpr int MB_W = 0, MB_M = 512, MB_HI = 1024;
 
     __device__ MiniWarp(const DecodeParams &pp, unsigned char *wb, int slot_bits)
-        : p(pp), wbase(wb), L(KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
+        : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
         (void)slot_bits;
         bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
     }
@@ -981,7 +1030,7 @@ struct MiniWarp {
                     uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++) wv[kk] = w[16 * sl + 4 * kk + t];
-                    FastWarp<2, KITTY>::split(wv, x, xs);
+                    FastWarp<2, 2, KITTY>::template split<Codes<2>>(wv, x, xs);
                     uint32_t a[4];
 #pragma unroll
                     for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;
@@ -1016,7 +1065,7 @@ struct MiniWarp {
                         uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) wv[kk] = hw[16 * s2 + 4 * kk + t];
-                        FastWarp<2, KITTY>::split(wv, x, xs);
+                        FastWarp<2, 2, KITTY>::template split<Codes<2>>(wv, x, xs);
                         uint32_t a[4];
 #pragma unroll
                         for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;

@@ -98,7 +98,7 @@ cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
 cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
-size_t decode_smem_bytes(int bits, bool kitty, int n_boost, int D, bool fast);
-int decode_warps_per_cta(int bits, bool kitty, int n_boost, bool fast);
+size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bool fast);
+int decode_warps_per_cta(int bits, int vbits, bool kitty, int n_boost, bool fast);
 
 }  // namespace kvq

@@ -33,12 +33,19 @@ SMALL = {
     "gqa_b4": (WORKLOADS["llama3_8b_gqa_b4"].replace(B=2, H_q=16, H_kv=4, T=1024), 1024 + 100, 4),
     "kitty": (WORKLOADS["kitty"].replace(B=2, H_q=16, H_kv=4, T=1024), 32 + 1024 + 128 + 60, 4),
     "long": (WORKLOADS["long_128k"].replace(T=2048), 2048 + 64, 3),
-    # key / value width variants: K4V2, K2V4 and K8V8 run on the CUDA-core path,
-    # K2V2 with sinks on the tensor-core tiles
+    # key / value width variants, all on the tensor-core tiles (keys set the tile:
+    # 128, 64 or 32 tokens; values the PV steps)
     "k4v2": (WORKLOADS["llama3_8b_gqa_k4v2"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
     "k2v4": (WORKLOADS["llama3_8b_gqa_k2v4"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
     "k8v8": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512), 512 + 70, 3),
     "k2v2s": (WORKLOADS["llama3_8b_gqa_k2v2s"].replace(B=2, H_q=16, H_kv=4, T=1024), 32 + 1024 + 70, 3),
+    "k2v8": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512, bits=2), 512 + 70, 2),
+    "k8v2": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512, v_bits=2), 512 + 70, 2),
+    "k4v8": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512, bits=4), 512 + 70, 2),
+    "k8v4": (WORKLOADS["llama3_8b_gqa_k8v8"].replace(B=2, H_q=16, H_kv=4, T=512, v_bits=4), 512 + 70, 2),
+    # G = 32: 8-bit keys fill one 32-token tile per page; 2-bit keys take the CUDA-core path
+    "tiny_k8v2": (WORKLOADS["tiny_kivi"].replace(bits=8, v_bits=2), 256 + 31, 3),
+    "tiny_k2v4": (WORKLOADS["tiny_kivi"].replace(v_bits=4), 256 + 31, 3),
 }
 
 
