@@ -255,6 +255,187 @@ def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
     return 0
 
 
+def paged_bytes(wl, lens_host) -> int:
+    """decode_bytes of a paged cache: the sum over active slots of each slot's bytes."""
+    H, D, G = wl.H_kv, wl.D, wl.G
+    Gv = min(G, D)
+    b = 0
+    for s in range(wl.B):
+        ns, T, nr, act = lens_host[4 * s: 4 * s + 4]
+        if not act:
+            continue
+        b += H * T * D * wl.bits // 8 + H * (T // G) * D * 4
+        b += H * T * D * wl.vbits // 8 + H * T * (D // Gv) * 4
+        b += H * (2 * ns + 2 * nr) * D * 2
+    return b + 2 * wl.B * wl.H_q * D * 2
+
+
+def paged_main(args, wl, baseline, rank, world, dev):
+    """The paged cache: B slots of different lengths (kvq_synth.slot_lengths) over a
+    page pool, N_LAYERS layer caches rotated; a step is kvq_paged_append +
+    kvq_paged_decode_attn + kvq_paged_flush.  Every slot's logical pages are mapped to
+    shuffled physical pages at set-up, so flushes find their pages mapped."""
+    import ctypes
+    import torch
+    import torch.distributed as dist
+    import bit_kv_cache_gb300 as kvq
+    lens0 = kvq_synth.slot_lengths(wl)
+    grow = -(-(args.steps + args.warmup + 256) // N_LAYERS)
+    max_T = (int(lens0.max()) + grow + 3 * wl.G) // wl.G * wl.G
+    mp = max_T // wl.G
+    K0, V0 = kvq_synth.prefill_kv(wl.replace(B=1), int(lens0.max()) + wl.G, replica=rank)
+    K0 = torch.from_numpy(K0[0]).to(dev)
+    V0 = torch.from_numpy(V0[0]).to(dev)
+    rng = np.random.default_rng(wl.seed + 31 * rank)
+    caches = []
+    for li in range(N_LAYERS):
+        c = kvq.KVQPagedCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, n_pages=wl.B * mp, max_T=max_T,
+                              S=wl.S, R=wl.R, device=dev, v_bits=wl.v_bits)
+        perm = rng.permutation(wl.B * mp).astype(np.int32).reshape(wl.B, mp)
+        c.table.copy_(torch.from_numpy(perm))
+        for b in range(wl.B):
+            c.pages[b] = [int(x) for x in perm[b]]
+        c.free = []
+        for b in range(wl.B):
+            L0 = int(lens0[b]) + (li * wl.G) // N_LAYERS
+            Kb = torch.roll(K0, shifts=977 * (b + 3 * li), dims=1)[:, :L0].contiguous()
+            Vb = torch.roll(V0, shifts=977 * (b + 3 * li), dims=1)[:, :L0].contiguous()
+            rc = kvq.lib.kvq_paged_prefill(ctypes.byref(c.cfg), ctypes.byref(c.p), b,
+                                           ctypes.c_void_p(Kb.data_ptr()), ctypes.c_void_p(Vb.data_ptr()), L0,
+                                           kvq.KVQCache._stream())
+            if rc:
+                raise RuntimeError("paged prefill of slot %d failed: %d" % (b, rc))
+            del Kb, Vb
+        caches.append(c)
+    del K0, V0
+    kn, vn = kvq_synth.decode_tokens(wl, 64, replica=rank)
+    qs = kvq_synth.queries(wl, 64, replica=rank)
+    kn_d, vn_d, q_d = (torch.from_numpy(a).to(dev) for a in (kn, vn, qs))
+    out = torch.empty((wl.B, wl.H_q, wl.D), dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+    assert sum(c.read_status() for c in caches) == 0
+    stream = torch.cuda.current_stream()
+    lib = kvq.lib
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    la = [(ctypes.byref(c.cfg), ctypes.byref(c.p), ctypes.c_void_p(c.ws.data_ptr()), c.ws.numel(), c.lens_host)
+          for c in caches]
+    knp = [ctypes.c_void_p(kn_d[j].data_ptr()) for j in range(64)]
+    vnp = [ctypes.c_void_p(vn_d[j].data_ptr()) for j in range(64)]
+    qp = [ctypes.c_void_p(q_d[j].data_ptr()) for j in range(64)]
+    outp = ctypes.c_void_p(out.data_ptr())
+    nfl = ctypes.c_int(0)
+    nflr = ctypes.byref(nfl)
+
+    def step(i, ev=None, inputs=None):
+        cfg, pc, ws, wsb, lh = la[i % N_LAYERS]
+        j = i % 64
+        k_, v_, q_ = inputs if inputs else (knp[j], vnp[j], qp[j])
+        rc = lib.kvq_paged_append(cfg, pc, k_, v_, sp)
+        b = paged_bytes(wl, lh)
+        if ev is not None:
+            ev[0].record(stream)
+        rc |= lib.kvq_paged_decode_attn(cfg, pc, q_, outp, ws, wsb, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        rc |= lib.kvq_paged_flush(cfg, pc, nflr, sp)
+        if rc:
+            raise RuntimeError("libkvq call failed in step %d" % i)
+        return b, nfl.value
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total_bytes, flushes = 0, 0
+    clk = Clocks(dev.index or 0)
+    clk.start()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        b, f = step(args.warmup + i, evs[i])
+        total_bytes += b
+        flushes += 2 if f else 0  # a flush is one value and one key launch
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk.stop()
+    ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(bb) for a, bb in evs]
+    st = sum(c.read_status() for c in caches)
+    if st != 0:
+        print("device status %d" % st, file=sys.stderr)
+    launches = 2 * K + flushes
+    ms_max, bytes_all = reduce_over_ranks(ms, float(total_bytes), world, dev)
+
+    # ---- end to end through the C ABI with pinned host buffers ----
+    kn_h, vn_h, q_h = (torch.from_numpy(a).pin_memory() for a in (kn, vn, qs))
+    out_h = torch.empty((wl.B, wl.H_q, wl.D), dtype=torch.float16).pin_memory()
+    kn_s, vn_s, q_s = torch.empty_like(kn_d[0]), torch.empty_like(vn_d[0]), torch.empty_like(q_d[0])
+    ins = (ctypes.c_void_p(kn_s.data_ptr()), ctypes.c_void_p(vn_s.data_ptr()), ctypes.c_void_p(q_s.data_ptr()))
+    Ke = max(1, min(K, args.e2e_steps))
+    e_bytes = 0
+    for i in range(Ke + 3):
+        if i == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e_bytes = 0
+        j = (args.warmup + K + i) % 64
+        kn_s.copy_(kn_h[j], non_blocking=True)
+        vn_s.copy_(vn_h[j], non_blocking=True)
+        q_s.copy_(q_h[j], non_blocking=True)
+        b, _ = step(args.warmup + K + i, inputs=ins)
+        e_bytes += b
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e_dt = time.perf_counter() - t0
+    h2d = (kn_s.numel() + vn_s.numel() + q_s.numel()) * 2
+    d2h = out.numel() * 2
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = measured_peaks()
+    value = bytes_all / (ms_max * 1e-3) / 1e9
+    dec_avg_ms = statistics.mean(dec_ms)
+    dec_bytes = total_bytes / K
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    line = {
+        "metric": baseline["metric"], "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K,
+        "us_per_step": ms_max * 1e3 / K, "hbm_frac_step": value / world / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; shapes and outlier structure of the workload, ragged slot lengths)",
+        "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
+                   "T_mean": wl.T, "slot_lengths": [int(x) for x in lens0], "G": wl.G, "R": wl.R,
+                   "bits": wl.bits, "v_bits": wl.vbits, "S": wl.S, "mode": "kivi", "cache": "paged",
+                   "step": "paged append + paged decode_attn + paged flush (when full), one layer",
+                   "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (
+                       N_LAYERS, dec_bytes / 1e6, N_LAYERS * dec_bytes / 1e9),
+                   "parallelism": "independent replicas per GPU" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel (paged)", "us_per_launch": dec_avg_ms * 1e3,
+                     "algorithmic_bytes_per_launch": dec_bytes, "traffic": None},
+        "gpu_launches": launches,
+        "clocks": clk.summary(w0, w1),
+        "e2e": {"value": e_bytes / e_dt / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": e_dt / Ke * 1e6},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, dt, n, desc = cpu_oracle_rate(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -286,6 +467,8 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     import bit_kv_cache_gb300 as kvq
+    if wl.ragged:
+        return paged_main(args, wl, baseline, rank, world, dev)
 
     # ---- N_LAYERS layer caches: one seeded draw, rolled per layer; staggered fills ----
     extra = (wl.S + wl.R) if wl.mode == "kitty" else 0

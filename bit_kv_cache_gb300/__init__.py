@@ -24,7 +24,11 @@ BUFFERS = ("k_codes", "k_hi", "k_bidx", "k_meta", "v_codes", "v_meta", "k_sink",
 EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_pack_k",
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
-           "kvq_read_status", "kvq_decode_attn_noalloc")
+           "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_paged_bytes", "kvq_paged_init",
+           "kvq_paged_prefill", "kvq_paged_append", "kvq_paged_flush_plan", "kvq_paged_flush",
+           "kvq_paged_release", "kvq_paged_workspace_bytes", "kvq_paged_decode_attn",
+           "kvq_paged_read_status")
+PAGED_MAX_B = 512
 
 
 class KvqError(RuntimeError):
@@ -48,12 +52,21 @@ class Cache(ctypes.Structure):
                                               "n_local", "local_head")]
 
 
+class Paged(ctypes.Structure):
+    """kvq_paged"""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("k_codes", "k_meta", "v_codes", "v_meta")] + \
+               [("n_pages", ctypes.c_int64)] + \
+               [(n, ctypes.c_void_p) for n in ("page_table", "k_sink", "v_sink", "k_res", "v_res", "lens",
+                                               "lens_host", "status")]
+
+
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError("libkvq.so not built (%s); run: python bit_kv_cache_gb300/build.py" % path)
     L = ctypes.CDLL(path)
     P, I, I64, Sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
-    CP, KP = ctypes.POINTER(Config), ctypes.POINTER(Cache)
+    CP, KP, PP = ctypes.POINTER(Config), ctypes.POINTER(Cache), ctypes.POINTER(Paged)
+    IP = ctypes.POINTER(I)
     sig = {
         "kvq_status_str": ([I], ctypes.c_char_p),
         "kvq_config_check": ([CP], I),
@@ -67,6 +80,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_decode_attn": ([CP, KP, P, P, P, Sz, P], I),
         "kvq_read_status": ([KP, P, ctypes.POINTER(ctypes.c_int32), P], I),
         "kvq_decode_attn_noalloc": ([CP, KP, P, P, P], I),
+        "kvq_paged_bytes": ([CP, I64, I], Sz),
+        "kvq_paged_init": ([CP, PP, P], I),
+        "kvq_paged_prefill": ([CP, PP, I, P, P, I64, P], I),
+        "kvq_paged_append": ([CP, PP, P, P, P], I),
+        "kvq_paged_flush_plan": ([CP, PP, ctypes.POINTER(ctypes.c_int32), IP], I),
+        "kvq_paged_flush": ([CP, PP, IP, P], I),
+        "kvq_paged_release": ([CP, PP, I, P], I),
+        "kvq_paged_workspace_bytes": ([CP], Sz),
+        "kvq_paged_decode_attn": ([CP, PP, P, P, P, Sz, P], I),
+        "kvq_paged_read_status": ([PP, P, ctypes.POINTER(ctypes.c_int32), P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -224,3 +247,137 @@ class KVQCache:
         rows = {"k_sink": cfg.S, "v_sink": cfg.S, "k_res": G if kitty else cfg.R,
                 "v_res": G if kitty else cfg.R, "v_local": cfg.R if kitty else 0}[name]
         return b[: U * rows * D * 2].view(torch.float16).view(cfg.B, cfg.H_kv, rows, D)
+
+
+class KVQPagedCache:
+    """A paged low-bit KV cache (KIVI mode): B batch slots of their own lengths over a
+    pool of n_pages physical pages, each holding one group of G tokens of all H_kv
+    heads of one slot.  The page table and the pool live in torch device memory; this
+    class keeps the free list on the host and writes the table rows a slot needs before
+    the library packs into them (prefill, flush).  ``max_T`` is the packed-token
+    capacity of one slot."""
+
+    def __init__(self, B, H_q, H_kv, D, G, bits, n_pages, max_T, S=0, R=None, device="cuda", v_bits=0):
+        import torch
+        self.torch = torch
+        self.cfg = make_config(B, H_q, H_kv, D, G, bits, S, R, 0, "kivi", max_T, v_bits)
+        self.device = torch.device(device)
+        self.n_pages = n_pages
+        cp = ctypes.byref(self.cfg)
+        self.p = Paged()
+        self.buf = {}
+        for name, which in (("k_codes", 0), ("k_meta", 3), ("v_codes", 4), ("v_meta", 5), ("k_sink", 6),
+                            ("v_sink", 6), ("k_res", 7), ("v_res", 8)):
+            n = lib.kvq_paged_bytes(cp, n_pages, which)
+            if n == 0 and which in (0, 3, 4, 5, 7, 8) and n_pages > 0:
+                raise KvqError(-2, "paged config")
+            t = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.device)
+            self.buf[name] = t
+            setattr(self.p, name, t.data_ptr() if n else None)
+        self.max_pages = max_T // G
+        self.table = torch.zeros((B, self.max_pages), dtype=torch.int32, device=self.device)
+        self.lens = torch.zeros((B, 4), dtype=torch.int32, device=self.device)
+        self.lens_host = (ctypes.c_int32 * (4 * B))()
+        self.status = torch.zeros(4, dtype=torch.int32, device=self.device)
+        self.p.n_pages = n_pages
+        self.p.page_table = self.table.data_ptr()
+        self.p.lens = self.lens.data_ptr()
+        self.p.lens_host = ctypes.cast(self.lens_host, ctypes.c_void_p)
+        self.p.status = self.status.data_ptr()
+        self.ws = torch.zeros(lib.kvq_paged_workspace_bytes(cp), dtype=torch.uint8, device=self.device)
+        self.free = list(range(n_pages - 1, -1, -1))  # pop() hands out the lowest id first
+        self.pages = [[] for _ in range(B)]           # physical pages of each slot, logical order
+        _check(lib.kvq_paged_init(cp, ctypes.byref(self.p), KVQCache._stream()), "paged init")
+
+    def _ptr(self, t, shape, what):
+        return KVQCache._ptr(self, t, shape, what)
+
+    def lengths(self, b) -> dict:
+        l = self.lens_host[4 * b: 4 * b + 4]
+        return {"n_sink": l[0], "T": l[1], "n_res": l[2], "active": l[3]}
+
+    def _map(self, b, n):
+        """Maps the next n logical pages of slot b to free physical pages."""
+        if len(self.free) < n:
+            raise KvqError(-3, "page pool exhausted")
+        j0 = len(self.pages[b])
+        new = [self.free.pop() for _ in range(n)]
+        self.pages[b].extend(new)
+        if n:
+            self.table[b, j0:j0 + n] = self.torch.tensor(new, dtype=self.torch.int32)
+
+    def prefill(self, b, k, v):
+        """k, v: float16 [H_kv][L0][D] of batch slot b (empty)."""
+        cfg = self.cfg
+        L0 = k.shape[1]
+        self._ptr(k, (cfg.H_kv, L0, cfg.D), "k")
+        self._ptr(v, (cfg.H_kv, L0, cfg.D), "v")
+        if self.lens_host[4 * b + 3]:
+            raise KvqError(-1, "prefill of an occupied slot")
+        ns = min(cfg.S, L0)
+        self._map(b, (L0 - ns) // cfg.G)
+        _check(lib.kvq_paged_prefill(ctypes.byref(self.cfg), ctypes.byref(self.p), b, ctypes.c_void_p(k.data_ptr()),
+                                     ctypes.c_void_p(v.data_ptr()), L0, KVQCache._stream()), "paged prefill")
+
+    def append(self, k_new, v_new):
+        cfg = self.cfg
+        kp = self._ptr(k_new, (cfg.B, cfg.H_kv, cfg.D), "k_new")
+        vp = self._ptr(v_new, (cfg.B, cfg.H_kv, cfg.D), "v_new")
+        _check(lib.kvq_paged_append(ctypes.byref(self.cfg), ctypes.byref(self.p), kp, vp, KVQCache._stream()),
+               "paged append")
+
+    def flush(self) -> list:
+        """Packs every full residual into new pages; returns the flushed slots."""
+        cfg = self.cfg
+        seqs = (ctypes.c_int32 * cfg.B)()
+        n = ctypes.c_int(0)
+        _check(lib.kvq_paged_flush_plan(ctypes.byref(self.cfg), ctypes.byref(self.p), seqs, ctypes.byref(n)),
+               "flush plan")
+        out = list(seqs[: n.value])
+        for b in out:
+            self._map(b, cfg.R // cfg.G)
+        nf = ctypes.c_int(0)
+        _check(lib.kvq_paged_flush(ctypes.byref(self.cfg), ctypes.byref(self.p), ctypes.byref(nf),
+                                   KVQCache._stream()), "paged flush")
+        return out
+
+    def release(self, b):
+        self.free.extend(reversed(self.pages[b]))
+        self.pages[b] = []
+        _check(lib.kvq_paged_release(ctypes.byref(self.cfg), ctypes.byref(self.p), b, KVQCache._stream()),
+               "paged release")
+
+    def decode_attn(self, q, out=None):
+        cfg = self.cfg
+        qp = self._ptr(q, (cfg.B, cfg.H_q, cfg.D), "q")
+        if out is None:
+            out = self.torch.zeros_like(q)
+        op = self._ptr(out, (cfg.B, cfg.H_q, cfg.D), "out")
+        _check(lib.kvq_paged_decode_attn(ctypes.byref(self.cfg), ctypes.byref(self.p), qp, op,
+                                         ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+                                         KVQCache._stream()), "paged decode")
+        return out
+
+    def read_status(self) -> int:
+        st = ctypes.c_int32(0)
+        lib.kvq_paged_read_status(ctypes.byref(self.p), ctypes.c_void_p(self.ws.data_ptr()), ctypes.byref(st),
+                                  KVQCache._stream())
+        return st.value
+
+    def view(self, name: str):
+        """Typed views of the page pools ([n_pages][H_kv] ...) and the fp16 buffers."""
+        torch = self.torch
+        cfg = self.cfg
+        P, H, D, G = self.n_pages, cfg.H_kv, cfg.D, cfg.G
+        kfpi, vfpi, Gv = 32 // cfg.bits, 32 // (cfg.v_bits or cfg.bits), min(G, D)
+        b = self.buf[name]
+        if name == "k_codes":
+            return b.view(torch.int32).view(P, H, G // kfpi, D)
+        if name == "k_meta":
+            return b.view(torch.float16).view(P, H, D, 2)
+        if name == "v_codes":
+            return b.view(torch.int32).view(P, H, D // vfpi, G)
+        if name == "v_meta":
+            return b.view(torch.float16).view(P, H, G, D // Gv, 2)
+        rows = {"k_sink": cfg.S, "v_sink": cfg.S, "k_res": cfg.R, "v_res": cfg.R}[name]
+        return b[: cfg.B * H * rows * D * 2].view(torch.float16).view(cfg.B, H, rows, D)

@@ -18,8 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu", "kvq_noalloc.cu"]
-HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode_fast.cuh"]
+SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu", "kvq_noalloc.cu", "kvq_paged.cu",
+           "kvq_decode_paged.cu"]
+HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode_fast.cuh", "kvq_host.h",
+           "kvq_decode.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -227,10 +227,75 @@ __device__ __forceinline__ void issue_copy(void *dst, const void *src, uint32_t 
     bulk_g2s(dst, src, bytes, bar);
 }
 
+// Lengths of sequence u: the call's (dense cache) or its batch slot's (paged cache:
+// KIVI, keys and values packed alike, no local window).
+struct SeqLen {
+    int64_t n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head, L, n_fast;
+};
+template <bool PG>
+__device__ __forceinline__ SeqLen seq_len(const DecodeParams &p, int u) {
+    SeqLen s;
+    if (!PG) {
+        s.n_sink = p.n_sink;
+        s.T_k = p.T_k;
+        s.n_kres = p.n_kres;
+        s.T_v = p.T_v;
+        s.n_vres = p.n_vres;
+        s.n_local = p.n_local;
+        s.local_head = p.local_head;
+        s.L = p.L;
+        s.n_fast = p.n_fast;
+    } else {
+        const int4 ln = __ldg(reinterpret_cast<const int4 *>(p.lens) + u / p.H_kv);
+        s.n_sink = ln.x;
+        s.T_k = s.T_v = ln.y;
+        s.n_kres = s.n_vres = ln.z;
+        s.n_local = 0;
+        s.local_head = 0;
+        s.L = (int64_t)ln.x + ln.y + ln.z;
+        s.n_fast = ((int64_t)ln.y * p.bits) >> 8;  // tiles of 256 / bits tokens
+    }
+    return s;
+}
+
+// Page index (page-major buffers) of logical page j of sequence u.  Dense: u * max_T/G
+// + j.  Paged: page_table row of u's batch slot, read 32 entries at a time into one
+// register per lane; lookups are warp-wide (shuffles) and must be made by all lanes.
+template <bool PG>
+struct PageIds {
+    int64_t dense0 = 0;
+    __device__ void set(const DecodeParams &p, int u) { dense0 = (int64_t)u * (p.max_T / p.G); }
+    __device__ __forceinline__ int64_t operator()(const DecodeParams &, int64_t j) const { return dense0 + j; }
+};
+template <>
+struct PageIds<true> {
+    const int32_t *row = nullptr;  // the slot's table row
+    int64_t dense0 = 0;            // head h
+    int base = 0, reg = 0;         // entries [base, base + 32) are in reg (lane j: base + j)
+    __device__ void set(const DecodeParams &p, int u) {
+        const int b = u / p.H_kv;
+        dense0 = u - b * p.H_kv;
+        row = p.ptab + (size_t)b * p.ptab_stride;
+        base = -(1 << 30);  // nothing loaded
+    }
+    __device__ __forceinline__ int64_t operator()(const DecodeParams &p, int64_t j) {
+        if (j < base || j >= base + 32) {
+            base = (int)j;
+            const int e = (int)j + (int)(threadIdx.x & 31);
+            reg = e < p.ptab_stride ? __ldg(row + e) : 0;
+            if (reg < 0 || reg >= p.n_pages) {  // a bad table entry reads page 0
+                if (e < p.ptab_stride) report(p.status, 2 /*KVQ_DEV_BAD_STATE*/);
+                reg = 0;
+            }
+        }
+        return (int64_t)__shfl_sync(0xffffffffu, reg, (int)j - base) * p.H_kv + dense0;
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Packed tiles
 // ---------------------------------------------------------------------------
-template <int KB, int VB, bool KITTY>
+template <int KB, int VB, bool KITTY, bool PG = false>
 struct FastWarp {
     using T = Tile<KB, VB>;
     using CK = typename T::K;
@@ -242,6 +307,7 @@ struct FastWarp {
     uint64_t *bars;
     uint32_t phase = 0;    // bit s: parity of the next completion of slot s
     uint32_t pending = 0;  // bit s: slot s has copies in flight
+    PageIds<PG> pid;       // page index of a logical page of sequence u
 
     __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
         : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
@@ -277,24 +343,23 @@ struct FastWarp {
         const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + (j == 0 ? T::TOK * 4 : 0);
         if (lane == 0) mbar_arrive_expect_tx(&bars[s], bytes);
         __syncwarp();
-        const int64_t page = ti >> p.tpp_shift;  // tiles per page: a power of two
+        // tiles per page: a power of two; pg: page index, tin: tile within the page
+        const int64_t pg = pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
         const int i = lane;
         if (i < 8) {
             issue_copy(st + T::OFF_K + i * T::K_STRIDE,
-                       p.k_codes + ((size_t)u * (p.max_T / CK::FPI) + ti * 8 + i) * T::D, T::D * 4, &bars[s]);
+                       p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8 + i) * T::D, T::D * 4, &bars[s]);
         } else if (i == 8) {
-            issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
-                       &bars[s]);
+            issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &bars[s]);
         } else if (i == 9) {
             if (j == 0)
-                issue_copy(vmslot(0), p.v_meta + ((size_t)u * p.max_T + ti * T::TOK) * 2, T::TOK * 4, &bars[s]);
+                issue_copy(vmslot(0), p.v_meta + ((size_t)pg * p.G + tin * T::TOK) * 2, T::TOK * 4, &bars[s]);
         } else if (KITTY && nb > 0 && i >= 10 && i < 18) {
             const int r = i - 10;
-            issue_copy(st + T::OFF_HI + r * hi_stride(nb),
-                       p.k_hi + ((size_t)u * (p.max_T / 16) + ti * 8 + r) * nb, nb * 4, &bars[s]);
+            issue_copy(st + T::OFF_HI + r * hi_stride(nb), p.k_hi + ((size_t)pg * (p.G / 16) + tin * 8 + r) * nb,
+                       nb * 4, &bars[s]);
         } else if (KITTY && i == 18) {
-            issue_copy(st + T::OFF_HI + 8 * hi_stride(nb), p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * T::D,
-                       T::D, &bars[s]);
+            issue_copy(st + T::OFF_HI + 8 * hi_stride(nb), p.k_bidx + (size_t)pg * T::D, T::D, &bars[s]);
         }
     }
 
@@ -308,17 +373,16 @@ struct FastWarp {
         unsigned char *st = vslot(j & 1);
         if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
         __syncwarp();
-        const int64_t page = ti >> p.tpp_shift;
-        const int64_t off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
+        const int tmask = (1 << p.tpp_shift) - 1;
+        const int64_t pg = pid(p, ti >> p.tpp_shift), off = (ti & tmask) * T::TOK;
+        const int64_t pg1 = meta ? pid(p, (ti + 1) >> p.tpp_shift) : 0, off1 = ((ti + 1) & tmask) * T::TOK;
         const int i = lane;
         if (i < T::V_ROWS) {
-            issue_copy(st + i * T::V_STRIDE,
-                       p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * T::V_ROWS + i) * p.G + off, T::TOK * 4,
+            issue_copy(st + i * T::V_STRIDE, p.v_codes + ((size_t)pg * T::V_ROWS + i) * p.G + off, T::TOK * 4,
                        &bars[s]);
         }
         if (i == T::V_ROWS % 32 && meta) {  // 8-bit values: every lane has a row, lane 0 also the meta
-            issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)u * p.max_T + (ti + 1) * T::TOK) * 2, T::TOK * 4,
-                       &bars[s]);
+            issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)pg1 * p.G + off1) * 2, T::TOK * 4, &bars[s]);
         }
     }
 
@@ -538,6 +602,7 @@ struct FastWarp {
     // into a buffer whose previous contents the warp has just finished reading.
     __device__ void run(int uu, int64_t t0, int64_t t1, float *part) {
         u = uu;
+        pid.set(p, uu);
         const int64_t n = t1 - t0;
         const QRegs qr = load_q_regs(p, u);  // its loads go out before the first copies
         issue_kb(t0, 0);
@@ -670,9 +735,9 @@ struct FastWarp {
 // streams the value codes, rescales O and runs PV.  Handoff per p' buffer b:
 // "full" (query -> value) and "empty" (value -> query) mbarriers, waits bounded.
 // ---------------------------------------------------------------------------
-template <int KB, int VB, bool KITTY>
-struct PairWarp : FastWarp<KB, VB, KITTY> {
-    using Base = FastWarp<KB, VB, KITTY>;
+template <int KB, int VB, bool KITTY, bool PG = false>
+struct PairWarp : FastWarp<KB, VB, KITTY, PG> {
+    using Base = FastWarp<KB, VB, KITTY, PG>;
     using T = typename Base::T;
     using CK = typename T::K;
     using CV = typename T::V;
@@ -703,25 +768,22 @@ struct PairWarp : FastWarp<KB, VB, KITTY> {
         const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + T::TOK * 4;
         if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], bytes);
         __syncwarp();
-        const int64_t page = ti >> p.tpp_shift;
-        const int u = this->u;
+        const int64_t pg = this->pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
         if (lane < 8) {
             issue_copy(st + T::OFF_K + lane * T::K_STRIDE,
-                       p.k_codes + ((size_t)u * (p.max_T / CK::FPI) + ti * 8 + lane) * T::D, T::D * 4,
+                       p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8 + lane) * T::D, T::D * 4,
                        &this->bars[s]);
         } else if (lane == 8) {
-            issue_copy(st + T::OFF_KM, p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * T::D * 2, T::D * 4,
-                       &this->bars[s]);
+            issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &this->bars[s]);
         } else if (lane == 9) {
-            issue_copy(this->vmslot(s), p.v_meta + ((size_t)u * p.max_T + ti * T::TOK) * 2, T::TOK * 4,
+            issue_copy(this->vmslot(s), p.v_meta + ((size_t)pg * p.G + tin * T::TOK) * 2, T::TOK * 4,
                        &this->bars[s]);
         } else if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
             const int r = lane - 10;
-            issue_copy(st + T::OFF_HI + r * hi_stride(nb),
-                       p.k_hi + ((size_t)u * (p.max_T / 16) + ti * 8 + r) * nb, nb * 4, &this->bars[s]);
+            issue_copy(st + T::OFF_HI + r * hi_stride(nb), p.k_hi + ((size_t)pg * (p.G / 16) + tin * 8 + r) * nb,
+                       nb * 4, &this->bars[s]);
         } else if (KITTY && lane == 18) {
-            issue_copy(st + T::OFF_HI + 8 * hi_stride(nb),
-                       p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * T::D, T::D, &this->bars[s]);
+            issue_copy(st + T::OFF_HI + 8 * hi_stride(nb), p.k_bidx + (size_t)pg * T::D, T::D, &this->bars[s]);
         }
     }
 
@@ -734,11 +796,9 @@ struct PairWarp : FastWarp<KB, VB, KITTY> {
         unsigned char *st = this->vslot(j & 1);
         if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], T::V_ROWS * T::TOK * 4);
         __syncwarp();
-        const int64_t page = ti >> p.tpp_shift;
-        const int64_t off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
+        const int64_t pg = this->pid(p, ti >> p.tpp_shift), off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
         if (lane < T::V_ROWS)
-            issue_copy(st + lane * T::V_STRIDE,
-                       p.v_codes + (((size_t)this->u * (p.max_T / p.G) + page) * T::V_ROWS + lane) * p.G + off,
+            issue_copy(st + lane * T::V_STRIDE, p.v_codes + ((size_t)pg * T::V_ROWS + lane) * p.G + off,
                        T::TOK * 4, &this->bars[s]);
     }
 
@@ -750,6 +810,7 @@ struct PairWarp : FastWarp<KB, VB, KITTY> {
     // Query warp over tiles [t0, t1) of sequence uu.
     __device__ void run_q(int uu, int64_t t0, int64_t t1) {
         this->u = uu;
+        this->pid.set(this->p, uu);
         const int lane = this->lane;
         const int64_t n = t1 - t0;
         const QRegs qr = load_q_regs(this->p, uu);
@@ -799,6 +860,7 @@ struct PairWarp : FastWarp<KB, VB, KITTY> {
     // Value warp over the same tiles; writes the pair's partial [4][D+4] to `part`.
     __device__ void run_p(int uu, int64_t t0, int64_t t1, float *part) {
         this->u = uu;
+        this->pid.set(this->p, uu);
         const int lane = this->lane, gq = lane >> 2, t = lane & 3;
         const int64_t n = t1 - t0;
         issue_vp(t0, 0);
@@ -872,41 +934,41 @@ struct MiniTile {
     bool kpacked;   // keys from a packed 16-token block (Kitty), else fp16 rows
 };
 
-__device__ __forceinline__ MiniTile mini_tile(const DecodeParams &p, int64_t mi) {
+__device__ __forceinline__ MiniTile mini_tile(const DecodeParams &p, const SeqLen &sq, int64_t mi) {
     MiniTile m;
-    const int64_t ms = (p.n_sink + 15) >> 4, tok_fast = p.n_fast * (256 / p.bits);
-    const int64_t mp = (p.T_k - tok_fast) >> 4;
+    const int64_t ms = (sq.n_sink + 15) >> 4, tok_fast = sq.n_fast * (256 / p.bits);
+    const int64_t mp = (sq.T_k - tok_fast) >> 4;
     if (mi < ms) {
         m.tok0 = 16 * mi;
-        m.n = (int)kvq_min64(16, p.n_sink - m.tok0);
+        m.n = (int)kvq_min64(16, sq.n_sink - m.tok0);
         m.kpacked = false;
     } else if (mi < ms + mp) {
-        m.tok0 = p.n_sink + tok_fast + 16 * (mi - ms);
+        m.tok0 = sq.n_sink + tok_fast + 16 * (mi - ms);
         m.n = 16;
         m.kpacked = true;
     } else {
-        m.tok0 = p.n_sink + p.T_k + 16 * (mi - ms - mp);
-        m.n = (int)kvq_min64(16, p.L - m.tok0);
+        m.tok0 = sq.n_sink + sq.T_k + 16 * (mi - ms - mp);
+        m.n = (int)kvq_min64(16, sq.L - m.tok0);
         m.kpacked = false;
     }
     return m;
 }
 
 // fp16 value row of logical token tl (tl outside the packed values).
-__device__ __forceinline__ const uint16_t *vrow16(const DecodeParams &p, int u, int64_t tl) {
-    if (tl < p.n_sink) return p.v_sink + ((size_t)u * p.S_cap + tl) * 128;
-    const int64_t r = tl - p.n_sink - p.T_v;
-    if (r < p.n_vres) return p.v_res + ((size_t)u * p.cap_v + r) * 128;
-    int64_t slot = p.local_head + (r - p.n_vres);  // < 2 R: local_head < R, r - n_vres < n_local <= R
+__device__ __forceinline__ const uint16_t *vrow16(const DecodeParams &p, const SeqLen &sq, int u, int64_t tl) {
+    if (tl < sq.n_sink) return p.v_sink + ((size_t)u * p.S_cap + tl) * 128;
+    const int64_t r = tl - sq.n_sink - sq.T_v;
+    if (r < sq.n_vres) return p.v_res + ((size_t)u * p.cap_v + r) * 128;
+    int64_t slot = sq.local_head + (r - sq.n_vres);  // < 2 R: local_head < R, r - n_vres < n_local <= R
     if (slot >= p.R_local) slot -= p.R_local;
     return p.v_local + ((size_t)u * p.R_local + slot) * 128;
 }
-__device__ __forceinline__ const uint16_t *krow16(const DecodeParams &p, int u, int64_t tl) {
-    if (tl < p.n_sink) return p.k_sink + ((size_t)u * p.S_cap + tl) * 128;
-    return p.k_res + ((size_t)u * p.cap_k + (tl - p.n_sink - p.T_k)) * 128;
+__device__ __forceinline__ const uint16_t *krow16(const DecodeParams &p, const SeqLen &sq, int u, int64_t tl) {
+    if (tl < sq.n_sink) return p.k_sink + ((size_t)u * p.S_cap + tl) * 128;
+    return p.k_res + ((size_t)u * p.cap_k + (tl - sq.n_sink - sq.T_k)) * 128;
 }
 
-template <int KB, int VB, bool KITTY>
+template <int KB, int VB, bool KITTY, bool PG = false>
 struct MiniWarp {
     const DecodeParams &p;
     unsigned char *wbase;
@@ -914,6 +976,7 @@ struct MiniWarp {
     int u, lane;
     uint64_t *bars;
     uint32_t phase = 0, pending = 0;
+    SeqLen sq;  // lengths of sequence u
 
     // packed-key block layout in the key half of a slot
     static constexpr int MB_W = 0, MB_M = 512, MB_HI = 1024;
@@ -953,9 +1016,9 @@ struct MiniWarp {
         const int64_t tl = mt.tok0 + (i < mt.n ? i : 0);
         if (lane < 16) {
             if (!mt.kpacked) {
-                issue_copy(sK + i * kMiniRow, krow16(p, u, tl), 256, &bars[sk]);
-            } else {
-                const int64_t tk = mt.tok0 - p.n_sink, page = tk >> p.g_shift, blk = tk >> 4;
+                issue_copy(sK + i * kMiniRow, krow16(p, sq, u, tl), 256, &bars[sk]);
+            } else {  // Kitty mixed blocks (dense caches only)
+                const int64_t tk = mt.tok0 - sq.n_sink, page = tk >> p.g_shift, blk = tk >> 4;
                 if (i == 0) {
                     issue_copy(sK + MB_W, p.k_codes + ((size_t)u * (p.max_T / 16) + blk) * 128, 512, &bars[sk]);
                 } else if (i == 1) {
@@ -968,19 +1031,20 @@ struct MiniWarp {
                 }
             }
         } else {
-            issue_copy(sV + i * kMiniRow, vrow16(p, u, tl), 256, &bars[sk + 1]);
+            issue_copy(sV + i * kMiniRow, vrow16(p, sq, u, tl), 256, &bars[sk + 1]);
         }
     }
 
     __device__ void run(int uu, int64_t m0, int64_t m1, float *part) {
         u = uu;
+        sq = seq_len<PG>(p, uu);
         const int gq = lane >> 2, t = lane & 3, hq = gq >> 1;
         const bool lo_col = (gq & 1) != 0;
         const int64_t n = m1 - m0;
         uint16_t *qraw = reinterpret_cast<uint16_t *>(wbase + L.qraw);
         const QRegs qr = load_q_regs(p, u);
-        issue(mini_tile(p, u_base(m0)), 0);
-        if (n > 1) issue(mini_tile(p, u_base(m0 + 1)), 2);
+        issue(mini_tile(p, sq, u_base(m0)), 0);
+        if (n > 1) issue(mini_tile(p, sq, u_base(m0 + 1)), 2);
         store_q_warp<8>(qr, qraw, reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb = reinterpret_cast<uint16_t *>(wbase + L.pbuf);  // [4][16] p
         for (int i = lane; i < 8 * 16; i += 32) pb[i] = 0;           // heads 4..7 stay zero
@@ -995,7 +1059,7 @@ struct MiniWarp {
         bool ok = true;
         for (int64_t i = 0; i < n && ok; i++) {
             const int sk = 2 * (int)(i & 1);
-            const MiniTile mt = mini_tile(p, u_base(m0 + i));
+            const MiniTile mt = mini_tile(p, sq, u_base(m0 + i));
             ok &= wait_slot(sk);
             ok &= wait_slot(sk + 1);
             if (!ok) break;
@@ -1030,7 +1094,7 @@ struct MiniWarp {
                     uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++) wv[kk] = w[16 * sl + 4 * kk + t];
-                    FastWarp<2, 2, KITTY>::template split<Codes<2>>(wv, x, xs);
+                    FastWarp<2, 2, KITTY, false>::template split<Codes<2>>(wv, x, xs);
                     uint32_t a[4];
 #pragma unroll
                     for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;
@@ -1065,7 +1129,7 @@ struct MiniWarp {
                         uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) wv[kk] = hw[16 * s2 + 4 * kk + t];
-                        FastWarp<2, 2, KITTY>::template split<Codes<2>>(wv, x, xs);
+                        FastWarp<2, 2, KITTY, false>::template split<Codes<2>>(wv, x, xs);
                         uint32_t a[4];
 #pragma unroll
                         for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;
@@ -1116,7 +1180,7 @@ struct MiniWarp {
             }
             __syncwarp();
             fence_proxy_async();
-            if (i + 2 < n) issue(mini_tile(p, u_base(m0 + i + 2)), sk);
+            if (i + 2 < n) issue(mini_tile(p, sq, u_base(m0 + i + 2)), sk);
         }
         if (!ok) {
             for (int s = 0; s < kSlots; s++)

@@ -7,6 +7,23 @@
 
 namespace kvq {
 
+// Destination of the quant kernels' pages.  Dense (ptab null): grid unit u writes
+// page u * max_T/G + pg0 + j.  Paged: grid unit i is head h = i % H_kv of listed
+// sequence b = seq[i / H_kv]; its page j goes to physical page
+// ptab[b * ptab_stride + lp0[i / H_kv] + j], page index (that page) * H_kv + h.  Its
+// source unit is b * H_kv + h (src_by_seq) or h (a one-sequence source).
+constexpr int kMaxListSeq = 256;
+// A table entry outside [0, n_pages) is replaced by page 0 and sets the bad-state bit.
+struct PageMap {
+    const int32_t *ptab;
+    int ptab_stride, H_kv, n_seq, src_by_seq;
+    int64_t n_pages;
+    int32_t *status;
+    int32_t *lens;         // keys of a paged flush: lens[b] gets T = (lp0 + pages) * G, n_res = 0
+    int16_t seq[kMaxListSeq];
+    int32_t lp0[kMaxListSeq];
+};
+
 struct QuantKParams {
     const uint16_t *src;   // fp16 [U][*][D]
     int64_t src_ustride;   // elements between sequences
@@ -19,18 +36,20 @@ struct QuantKParams {
     uint8_t *k_bidx;
     uint16_t *k_meta;
     int32_t *status;       // device status word (may be null)
+    PageMap pm;
 };
 
 struct QuantVParams {
     const uint16_t *src;
     int64_t src_ustride, src_t0;
     int64_t n_tok;         // tokens to quantize (multiple of G)
-    int64_t tok0;          // destination packed-token index of the first one
+    int64_t tok0;          // destination packed-token index of the first one (multiple of G)
     int64_t max_T;
     int U, D, G, Gv;
     int32_t *v_codes;
     uint16_t *v_meta;
     int32_t *status;       // device status word (may be null)
+    PageMap pm;
 };
 
 struct CopyRowsParams {
@@ -45,6 +64,22 @@ struct AppendParams {
     uint16_t *k_dst, *v_dst, *v_evict;
     int64_t k_rows, k_row, v_rows, v_row, evict_rows, evict_row;  // evict_row < 0: none
     int U, D;
+};
+
+// Paged append: one CTA per batch slot; the rows follow the slot's device lengths,
+// which the CTA then advances.
+struct PagedAppendParams {
+    const uint16_t *k_new, *v_new;
+    uint16_t *k_sink, *v_sink, *k_res, *v_res;
+    int32_t *lens;         // [B][4] n_sink, T, n_res, active
+    int32_t *status;       // a full residual sets the bad-state bit (the host checks first)
+    int B, H_kv, D, S, R;
+};
+
+// Writes lens[b] = {v0, v1, v2, v3} (prefill and release of a batch slot).
+struct SetLensParams {
+    int32_t *lens;
+    int b, v0, v1, v2, v3;
 };
 
 // Decode attention schedule.  Work items of one sequence:
@@ -89,6 +124,18 @@ struct DecodeParams {
     int64_t n_mini, N_m;   // mini tiles per sequence, in all
     int64_t n_gen;         // generic tokens per sequence
     int64_t gen_chunk;     // tokens per generic chunk (multiple of 32)
+    // paged cache (tile paths, KIVI): page table and per-sequence lengths.  Items of
+    // sequence b in a pool are laid out b-major like the dense ones, each sequence with
+    // its own count; a unit range may then cross several sequences.  Segments that are
+    // neither the first nor the last of a range hold a whole sequence's items of that
+    // pool and are published by their unit alone.
+    const int32_t *ptab;   // [B][ptab_stride] physical page of logical page j (null: dense)
+    int ptab_stride;
+    int64_t n_pages;       // pool size; an entry outside [0, n_pages) reads page 0 and sets a status bit
+    const int32_t *lens;   // [B][4] n_sink, T, n_res, active (null: the lengths above)
+    int32_t *seq_slots;    // [U][smax] partial slot ids of each sequence (paged)
+    int smax;              // slot ids per sequence
+    int mid_base;          // first slot id of the middle segments: pool * U + u above it
 };
 
 constexpr int kMaxWarps = 8;
@@ -97,7 +144,10 @@ cudaError_t launch_quant_k(const QuantKParams &p, int bits, bool kitty, cudaStre
 cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
 cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st);
+cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
+cudaError_t launch_decode_paged(const DecodeParams &p, cudaStream_t st);  // p.lens set
 size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bool fast);
 int decode_warps_per_cta(int bits, int vbits, bool kitty, int n_boost, bool fast);
 

@@ -93,6 +93,27 @@ __host__ __device__ constexpr uint32_t magic_sum(int b, int n) {
 }
 
 // ------------------------------------------------------------------------------
+// Page map (see PageMap): source unit and destination page index of grid unit u.
+// ------------------------------------------------------------------------------
+__device__ __forceinline__ int map_src_unit(const PageMap &m, int u) {
+    if (!m.ptab) return u;
+    const int i = u / m.H_kv, h = u - i * m.H_kv;
+    return m.src_by_seq ? (int)m.seq[i] * m.H_kv + h : h;
+}
+// page index of page pg of the call (dense: pg0 + pg of unit u's region)
+__device__ __forceinline__ int64_t map_dst_page(const PageMap &m, int64_t max_T, int G, int64_t pg0, int u,
+                                                int64_t pg) {
+    if (!m.ptab) return (int64_t)u * (max_T / G) + pg0 + pg;
+    const int i = u / m.H_kv, h = u - i * m.H_kv;
+    int64_t e = m.ptab[(size_t)m.seq[i] * m.ptab_stride + m.lp0[i] + pg];
+    if (e < 0 || e >= m.n_pages) {
+        report(m.status, 2 /*KVQ_DEV_BAD_STATE*/);
+        e = 0;
+    }
+    return e * m.H_kv + h;
+}
+
+// ------------------------------------------------------------------------------
 // Keys: one CTA per page of G tokens.  Thread (pair pr, slice sl) holds channels
 // 2pr, 2pr+1 for TPS consecutive tokens in registers; min/max (and, for Kitty, the
 // channel scores) are combined across slices in shared memory.
@@ -115,11 +136,18 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
     const int u = blockIdx.y;
     const int64_t pg = blockIdx.x;
     const int d0 = 2 * pr;
+    if (p.pm.lens && tid == 0 && pg == 0 && u % p.pm.H_kv == 0) {  // paged flush: commit the lengths
+        const int i = u / p.pm.H_kv;
+        int32_t *ln = p.pm.lens + 4 * (size_t)p.pm.seq[i];
+        ln[1] = (int32_t)((p.pm.lp0[i] + p.n_pages) * p.G);
+        ln[2] = 0;
+    }
 
     uint32_t x[TPS];
     if (active) {
         const uint32_t *src = reinterpret_cast<const uint32_t *>(
-            p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + pg * p.G + sl * TPS) * D) + pr;
+            p.src + (size_t)map_src_unit(p.pm, u) * p.src_ustride + (size_t)(p.src_t0 + pg * p.G + sl * TPS) * D) +
+                              pr;
 #pragma unroll
         for (int i = 0; i < TPS; i++) x[i] = __ldg(src + (size_t)i * pairs);
         __half2 lo = *reinterpret_cast<__half2 *>(&x[0]), hi = lo;
@@ -195,9 +223,9 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
         gq[c] = make_group(mn, mx, max_int);
     }
 
-    const int64_t page = p.pg0 + pg;
+    const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.pg0, u, pg);  // page index
     const int64_t wrow0 = page * (p.G / FPI) + sl * NW;  // first word row of this thread
-    uint2 *dst = reinterpret_cast<uint2 *>(p.k_codes + (size_t)u * (p.max_T / FPI) * D) + pr;
+    uint2 *dst = reinterpret_cast<uint2 *>(p.k_codes) + pr;
 #pragma unroll
     for (int wi = 0; wi < NW; wi++) {
         uint32_t w0 = 0, w1 = 0, h0 = 0, h1 = 0;
@@ -215,7 +243,7 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
         }
         dst[(size_t)(wrow0 + wi) * pairs] = make_uint2(w0, w1);
         if (KITTY) {
-            int32_t *hp = p.k_hi + ((size_t)u * (p.max_T / 16) + wrow0 + wi) * p.n_boost;
+            int32_t *hp = p.k_hi + (size_t)(wrow0 + wi) * p.n_boost;
             if (slot[0] < p.n_boost) hp[slot[0]] = (int32_t)h0;
             if (slot[1] < p.n_boost) hp[slot[1]] = (int32_t)h1;
         }
@@ -224,9 +252,9 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
         uint2 m;
         m.x = (uint32_t)gq[0].s16 | ((uint32_t)gq[0].mn16 << 16);
         m.y = (uint32_t)gq[1].s16 | ((uint32_t)gq[1].mn16 << 16);
-        reinterpret_cast<uint2 *>(p.k_meta + ((size_t)u * (p.max_T / p.G) + page) * D * 2)[pr] = m;
+        reinterpret_cast<uint2 *>(p.k_meta + (size_t)page * D * 2)[pr] = m;
         if (KITTY) {
-            uint8_t *bi = p.k_bidx + ((size_t)u * (p.max_T / p.G) + page) * D;
+            uint8_t *bi = p.k_bidx + (size_t)page * D;
             bi[d0] = (uint8_t)slot[0];
             bi[d0 + 1] = (uint8_t)slot[1];
         }
@@ -244,7 +272,7 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
     const int64_t tl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // token within call
     if (tl >= p.n_tok) return;
     const uint4 *src = reinterpret_cast<const uint4 *>(
-        p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + tl) * D);
+        p.src + (size_t)map_src_unit(p.pm, u) * p.src_ustride + (size_t)(p.src_t0 + tl) * D);
     uint32_t xw[D / 2];  // the token's row as half2 words
 #pragma unroll
     for (int i = 0; i < ND; i++) {
@@ -254,10 +282,10 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
         xw[4 * i + 2] = v.z;
         xw[4 * i + 3] = v.w;
     }
-    const int64_t tau = p.tok0 + tl;  // index within the packed value region
-    const int64_t page = tau / p.G, tin = tau % p.G;
-    int32_t *vc = p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * NWORD) * p.G + tin;
-    uint32_t *vm = reinterpret_cast<uint32_t *>(p.v_meta) + ((size_t)u * p.max_T + tau) * (D / GV);
+    // tok0 is a multiple of G: page tl / G of the call, token tl % G within it
+    const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.tok0 / p.G, u, tl / p.G), tin = tl % p.G;
+    int32_t *vc = p.v_codes + ((size_t)page * NWORD) * p.G + tin;
+    uint32_t *vm = reinterpret_cast<uint32_t *>(p.v_meta) + ((size_t)page * p.G + tin) * (D / GV);
 #pragma unroll
     for (int g0 = 0; g0 < D; g0 += GV) {
         __half2 lo = *reinterpret_cast<const __half2 *>(&xw[g0 / 2]), hi = lo;
@@ -366,15 +394,15 @@ __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int6
         }
     }
     __syncthreads();
-    const int64_t tau0 = p.tok0 + tl0, page = tau0 / p.G, tin0 = tau0 % p.G;
+    // 128 tokens within one page (G is a multiple of 128 here, tok0 a multiple of G)
+    const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.tok0 / p.G, u, tl0 / p.G), tin0 = tl0 % p.G;
     for (int i = tid; i < NWORD * 32; i += 256) {
         const int m = i >> 5, q4 = i & 31;
         const uint4 v = *reinterpret_cast<const uint4 *>(&s_codes[m][4 * q4]);
-        *reinterpret_cast<uint4 *>(p.v_codes + (((size_t)u * (p.max_T / p.G) + page) * NWORD + m) * p.G + tin0 +
-                                   4 * q4) = v;
+        *reinterpret_cast<uint4 *>(p.v_codes + ((size_t)page * NWORD + m) * p.G + tin0 + 4 * q4) = v;
     }
     if (tid < 32)
-        reinterpret_cast<uint4 *>(reinterpret_cast<uint32_t *>(p.v_meta) + (size_t)u * p.max_T + tau0)[tid] =
+        reinterpret_cast<uint4 *>(reinterpret_cast<uint32_t *>(p.v_meta) + (size_t)page * p.G + tin0)[tid] =
             *reinterpret_cast<const uint4 *>(&s_meta[4 * tid]);
 }
 
@@ -383,7 +411,8 @@ template <int BITS>
 __global__ void __launch_bounds__(256) quant_v_rows(QuantVParams p) {
     const int u = blockIdx.y;
     const int64_t tl0 = (int64_t)blockIdx.x * 128;
-    quant_v_chunk<BITS>(p, u, tl0, p.src + (size_t)u * p.src_ustride + (size_t)(p.src_t0 + tl0) * 128);
+    quant_v_chunk<BITS>(p, u, tl0,
+                        p.src + (size_t)map_src_unit(p.pm, u) * p.src_ustride + (size_t)(p.src_t0 + tl0) * 128);
 }
 
 // ------------------------------------------------------------------------------
@@ -421,6 +450,50 @@ __global__ void append_kernel(AppendParams p) {
         *ev = *vd;
     }
     *vd = *vn;
+}
+
+// Paged append: CTA b moves the new key and value rows of batch slot b's H_kv heads
+// into its sink (while not full) or residual, at the slot's device lengths, and
+// advances them.  Only this CTA reads or writes lens[b].
+__global__ void paged_append_kernel(PagedAppendParams p) {
+    const int b = blockIdx.x;
+    int32_t *ln = p.lens + 4 * (size_t)b;
+    __shared__ int s_ns, s_nr, s_act;
+    if (threadIdx.x == 0) {
+        s_ns = ln[0];
+        s_nr = ln[2];
+        s_act = ln[3];
+    }
+    __syncthreads();
+    if (!s_act) return;
+    const bool to_sink = s_ns < p.S;
+    if (!to_sink && s_nr >= p.R) {  // never with the host's capacity check
+        if (threadIdx.x == 0) report(p.status, 2 /*KVQ_DEV_BAD_STATE*/);
+        return;
+    }
+    const int chunks = p.D / 8, total = p.H_kv * chunks;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int h = i / chunks, c = i - h * chunks;
+        const size_t u = (size_t)b * p.H_kv + h;
+        const uint4 kn = reinterpret_cast<const uint4 *>(p.k_new + u * p.D)[c];
+        const uint4 vn = reinterpret_cast<const uint4 *>(p.v_new + u * p.D)[c];
+        uint16_t *kd = to_sink ? p.k_sink + (u * p.S + s_ns) * p.D : p.k_res + (u * p.R + s_nr) * p.D;
+        uint16_t *vd = to_sink ? p.v_sink + (u * p.S + s_ns) * p.D : p.v_res + (u * p.R + s_nr) * p.D;
+        reinterpret_cast<uint4 *>(kd)[c] = kn;
+        reinterpret_cast<uint4 *>(vd)[c] = vn;
+    }
+    if (threadIdx.x == 0) {
+        if (to_sink) ln[0] = s_ns + 1;
+        else ln[2] = s_nr + 1;
+    }
+}
+
+__global__ void set_lens_kernel(SetLensParams p) {
+    int32_t *ln = p.lens + 4 * (size_t)p.b;
+    ln[0] = p.v0;
+    ln[1] = p.v1;
+    ln[2] = p.v2;
+    ln[3] = p.v3;
 }
 
 // ------------------------------------------------------------------------------
@@ -500,6 +573,17 @@ cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st) {
     int blocks = (int)((total + 255) / 256);
     if (blocks > 4096) blocks = 4096;
     copy_rows_kernel<<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st) {
+    if (p.B <= 0) return cudaSuccess;
+    paged_append_kernel<<<(unsigned)p.B, 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st) {
+    set_lens_kernel<<<1, 1, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -29,7 +29,8 @@
  *   - Return value: KVQ_OK or a negative kvq_status.  No entry point aborts or
  *     throws.  On an argument error nothing is enqueued and the cache is not
  *     modified.  KVQ_ERR_CUDA means a launch failed (cudaGetLastError).
- *   - Every sequence (b, h_kv) of a cache has the same length.
+ *   - Every sequence (b, h_kv) of a kvq_cache has the same length.  The paged
+ *     cache (kvq_paged, below) holds sequences of different lengths.
  */
 #ifndef KVQ_H_
 #define KVQ_H_
@@ -63,9 +64,10 @@ enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
  *   bits            : key code width, 2, 4 or 8 (Kitty: 2; its boosted key channels
  *                     reach 4 bits)
  *   v_bits          : value code width, 2, 4 or 8; 0 means the same as bits (the
- *                     K4V2 / K2V4 variants of the Kitty notes, Sec. 3.1).  Equal
- *                     widths of 2 or 4 decode on tensor-core tiles; other widths on
- *                     the CUDA-core path.
+ *                     K4V2 / K2V4 variants of the Kitty notes, Sec. 3.1).  Every
+ *                     pair of widths decodes on tensor-core tiles when D = 128,
+ *                     H_q/H_kv <= 4 and G is a multiple of the tile (256/bits
+ *                     tokens); other shapes on the CUDA-core path.
  *   S               : fp16 attention-sink tokens kept at the start (0 = none)
  *   R               : KIVI: fp16 residual capacity, a multiple of G, flushed as R/G
  *                     groups once full.  Kitty: the value local window.
@@ -209,6 +211,97 @@ int kvq_decode_attn(const kvq_config *cfg, const kvq_cache *cache, const uint16_
  * Other arguments, layouts and errors as for kvq_decode_attn. */
 int kvq_decode_attn_noalloc(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
                             uint16_t *out, void *stream);
+
+/* ---------------------------------------------------------------------------------
+ * Paged cache with per-sequence lengths (Kitty Sec. 4.1 "page-centric memory layout":
+ * every quantization group of G tokens is a page, stored apart from the fp16 sink and
+ * residual buffers, after PagedAttention; the KIVI notes name PagedAttention as the
+ * way to cut a cache into fixed blocks reached through a mapping table).
+ *
+ * Physical page p (0 <= p < n_pages) holds one group of G tokens of all H_kv heads of
+ * one sequence.  The page pools use the page-major layouts of kvq_cache with the page
+ * index (u * max_T/G + logical page) replaced by (p * H_kv + h):
+ *   k_codes  int32 [n_pages][H_kv][G/fpi_k][D]
+ *   k_meta   fp16  [n_pages][H_kv][D][2]
+ *   v_codes  int32 [n_pages][H_kv][D/fpi_v][G]
+ *   v_meta   fp16  [n_pages][H_kv][G][D/Gv][2]
+ * page_table int32 [B][max_T/G] (device) maps logical page j of sequence b to its
+ * physical page.  The caller owns the pool and the table and chooses the pages: before
+ * kvq_paged_prefill(b, L0) row b must map the packed pages of the prefill, and before
+ * kvq_paged_flush every sequence that kvq_paged_flush_plan lists must map its next R/G
+ * logical pages.  Entries must be valid page ids; a page must not be mapped twice.
+ * Per-sequence fp16 buffers keep the kvq_cache layouts ([U][S][D] sink, [U][R][D]
+ * residual; U = B*H_kv, unit b*H_kv + h).
+ * lens (device) and lens_host (host) are int32 [B][4] = {n_sink, T, n_res, active}:
+ * sink tokens, packed tokens (keys and values alike), residual tokens, and 1 if the
+ * batch slot holds a sequence.  The library keeps both; the caller only allocates
+ * them and calls kvq_paged_init once.  Sequence b's logical tokens are
+ * [sink | packed pages | residual].
+ * Supported: KIVI mode, any widths, D = 128, H_q/H_kv <= 4, G a multiple of the tile
+ * (256/bits tokens) and a power of two, B <= KVQ_PAGED_MAX_B.
+ * --------------------------------------------------------------------------------- */
+#define KVQ_PAGED_MAX_B 512
+
+typedef struct {
+    int32_t *k_codes;
+    uint16_t *k_meta;
+    int32_t *v_codes;
+    uint16_t *v_meta;
+    int64_t n_pages;
+    const int32_t *page_table;
+    uint16_t *k_sink, *v_sink;
+    uint16_t *k_res, *v_res;
+    int32_t *lens;
+    int32_t *lens_host;
+    int32_t *status;
+} kvq_paged;
+
+/* Byte size of a paged buffer: which = 0 k_codes, 3 k_meta, 4 v_codes, 5 v_meta
+ * (pools of n_pages pages), 6 k_sink (= v_sink), 7 k_res, 8 v_res, 10 lens (= lens_host),
+ * 11 page_table.  0 for an unused buffer or an unsupported cfg. */
+size_t kvq_paged_bytes(const kvq_config *cfg, int64_t n_pages, int which);
+
+/* Marks every batch slot empty (host and device lengths; cudaMemsetAsync on stream). */
+int kvq_paged_init(const kvq_config *cfg, kvq_paged *pc, void *stream);
+
+/* Prefill of batch slot b, which must be empty: k, v device fp16 [H_kv][L0][D].  The
+ * first min(S, L0) tokens go to the sink, the next floor((L0-n_sink)/G)*G are
+ * quantized (keys per channel, values per token) into the physical pages that
+ * page_table row b maps for logical pages 0.., and the rest (< G) go to the residual
+ * (KIVI Step 3).  KVQ_ERR_CAPACITY if the packed part exceeds max_T. */
+int kvq_paged_prefill(const kvq_config *cfg, kvq_paged *pc, int b, const uint16_t *k,
+                      const uint16_t *v, int64_t L0, void *stream);
+
+/* One new token for every active sequence: k_new, v_new device fp16 [B][H_kv][D]
+ * (rows of empty slots are ignored).  Into the sink while it is not full, else into
+ * the residual.  KVQ_ERR_CAPACITY if an active sequence's residual is full (flush
+ * first). */
+int kvq_paged_append(const kvq_config *cfg, kvq_paged *pc, const uint16_t *k_new,
+                     const uint16_t *v_new, void *stream);
+
+/* Host only: the sequences whose residual is full, ascending, into seqs (room for B);
+ * *n their count.  Sequence b needs logical pages [T_b/G, T_b/G + R/G) mapped before
+ * kvq_paged_flush. */
+int kvq_paged_flush_plan(const kvq_config *cfg, const kvq_paged *pc, int32_t *seqs, int *n);
+
+/* Packs the full residual of every sequence kvq_paged_flush_plan lists into its next
+ * R/G pages and empties it.  *n_flushed (may be NULL): the number of sequences.
+ * KVQ_ERR_CAPACITY if a sequence would exceed max_T. */
+int kvq_paged_flush(const kvq_config *cfg, kvq_paged *pc, int *n_flushed, void *stream);
+
+/* Empties batch slot b (its pages may then be reused by the caller). */
+int kvq_paged_release(const kvq_config *cfg, kvq_paged *pc, int b, void *stream);
+
+/* Workspace bytes kvq_paged_decode_attn needs (zero-filled once, kvq_workspace_init). */
+size_t kvq_paged_workspace_bytes(const kvq_config *cfg);
+
+/* Decode attention, as kvq_decode_attn, for every active sequence over its own
+ * length: q, out device fp16 [B][H_q][D]; rows of empty slots are not written. */
+int kvq_paged_decode_attn(const kvq_config *cfg, const kvq_paged *pc, const uint16_t *q,
+                          uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/* As kvq_read_status, for the workspace status word and pc->status. */
+int kvq_paged_read_status(const kvq_paged *pc, void *ws, int32_t *dev_status, void *stream);
 
 /* Synchronizes `stream`, then returns in *dev_status the OR of the error bits the
  * kernels wrote into the workspace status word and into cache->status (if cache is

@@ -51,6 +51,7 @@ class Workload:
     v_outlier_prob: float = 0.0
     v_outlier_scale: float = 1.0
     v_bits: int = 0   # value code width; 0: the same as bits
+    ragged: float = 0.0  # paged cache: slot lengths spread uniformly over T (1 +- ragged)
 
     @property
     def vbits(self) -> int:
@@ -97,6 +98,19 @@ WORKLOADS.update({
     "llama3_8b_gqa_k8v8": Workload("llama3_8b_gqa_k8v8", bits=8, seed=8, **_GQA),
     "llama3_8b_gqa_k2v2s": Workload("llama3_8b_gqa_k2v2s", bits=2, S=32, seed=9, **_GQA),
 })
+
+# Paged cache with per-sequence lengths: eight slots of the Llama-3-8B GQA heads whose
+# lengths spread uniformly over 32768 * (1 +- 0.75) tokens (a continuous-batching mix).
+WORKLOADS["llama3_8b_gqa_paged"] = Workload("llama3_8b_gqa_paged", bits=2, seed=10, ragged=0.75,
+                                            **dict(_GQA, B=8))
+
+
+def slot_lengths(wl: Workload) -> np.ndarray:
+    """Seeded per-slot prefill lengths of a paged workload: T * (1 + ragged * u),
+    u uniform in [-1, 1], at least one token."""
+    rng = _rng(wl, 7)
+    u = rng.uniform(-1.0, 1.0, wl.B)
+    return np.maximum(1, np.round(wl.T * (1.0 + wl.ragged * u))).astype(np.int64)
 
 
 def _rng(wl: Workload, stream: int) -> np.random.Generator:
