@@ -418,7 +418,7 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
         p.n_mini = cdiv(k->n_sink, 16) + (k->T_k - p.n_fast * tok) / 16 + cdiv(k->n_kres, 16);
         p.N_f = (int64_t)U * p.n_fast;
         p.N_m = (int64_t)U * p.n_mini;
-        split_pools(p.N_f, p.n_fast, p.N_m, p.n_mini, wpc, nsm, p.C_f, p.C_m);
+        split_pools(p.N_f, p.n_fast, p.N_m, p.n_mini, wpc, nsm, p.C_f, p.C_m, p.n_fast ? U : 0, p.n_mini ? U : 0);
     } else {
         // generic chunks of the whole sequence (CUDA cores)
         p.n_gen = L;

@@ -74,19 +74,26 @@ inline int64_t clamp_pool(int64_t want, int64_t N, int64_t n, int wpc) {
 
 // CTAs of the fast and mini pools (one wave of nsm CTAs in all) for N_f / N_m items,
 // at most n_f / n_m per sequence (dense caches; a paged cache passes the totals).
+// u_f / u_m (paged caches): sequences with items in each pool; a warp range crosses
+// about items / (N / u) of them, and each crossing restarts the warp's copy pipeline.
 inline void split_pools(int64_t N_f, int64_t n_f, int64_t N_m, int64_t n_m, int wpc, int nsm, int &C_f,
-                        int &C_m) {
+                        int &C_m, int64_t u_f = 0, int64_t u_m = 0) {
     // cost of a mini tile relative to a fast tile (bytes of 16 fp16 tokens vs a packed
-    // tile, lighter arithmetic)
-    const double kMini = 0.6;
+    // tile, lighter arithmetic); a pipeline restart costs about 1.5 tiles (measured)
+    const double kMini = u_m ? 0.8 : 0.6, kSeg = 1.5;
+    auto cost = [&](int64_t N, int64_t C, double per_item, int64_t u) -> double {
+        if (!C) return 0.0;
+        const double items = (double)cdiv(N, C * wpc);
+        const double segs = u ? items * (double)u / (double)N + 1.0 : 0.0;
+        return items * per_item + segs * kSeg;
+    };
     double best = 1e300;
     int64_t bf = 0, bm = 0;
     const int64_t cm_max = N_m > 0 ? nsm : 0;
     for (int64_t cm0 = (N_m > 0 ? 1 : 0); cm0 <= cm_max; cm0++) {
         const int64_t cm = clamp_pool(cm0, N_m, n_m, wpc);
         const int64_t cf = clamp_pool(std::max<int64_t>(1, nsm - cm), N_f, n_f, wpc);
-        const double tf = cf ? (double)cdiv(N_f, cf * wpc) : 0.0;
-        const double tm = cm ? (double)cdiv(N_m, cm * wpc) * kMini : 0.0;
+        const double tf = cost(N_f, cf, 1.0, u_f), tm = cost(N_m, cm, kMini, u_m);
         const double est = (double)cdiv(cf + cm, nsm) * std::max(tf, tm) + 1e-3 * (double)(cf + cm);
         if (est < best) {
             best = est;

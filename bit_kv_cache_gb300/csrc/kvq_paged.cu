@@ -352,13 +352,15 @@ int kvq_paged_decode_attn(const kvq_config *c, const kvq_paged *pc, const uint16
     const int wpc = decode_warps_per_cta(c->bits, vbits_of(c), false, 0, true);
     // items per batch slot: packed tiles and 16-token fp16 tiles
     std::vector<int64_t> nf(B), nm(B);
-    int64_t Sf = 0, Sm = 0;
+    int64_t Sf = 0, Sm = 0, uf = 0, um = 0;
     for (int b = 0; b < B; b++) {
         const int32_t *l = pc->lens_host + 4 * b;
         nf[b] = l[3] ? l[1] / tok : 0;
         nm[b] = l[3] ? cdiv(l[0], 16) + cdiv(l[2], 16) : 0;
         Sf += nf[b];
         Sm += nm[b];
+        uf += nf[b] ? H : 0;
+        um += nm[b] ? H : 0;
     }
     const int64_t N_f = H * Sf, N_m = H * Sm;
     if (N_f + N_m == 0) return KVQ_OK;  // no active sequence
@@ -368,7 +370,7 @@ int kvq_paged_decode_attn(const kvq_config *c, const kvq_paged *pc, const uint16
     memset(&p, 0, sizeof(p));
     p.U = U;
     p.wpc = wpc;
-    split_pools(N_f, N_f, N_m, N_m, wpc, nsm, p.C_f, p.C_m);
+    split_pools(N_f, N_f, N_m, N_m, wpc, nsm, p.C_f, p.C_m, uf, um);
     if (p.C_f + p.C_m > 2 * nsm || wpc > 8) return KVQ_ERR_UNSUPPORTED;
     // slot ids per sequence: the CTAs of both pools that hold its items
     int64_t max_slots = 0, af = 0, am = 0;
