@@ -61,7 +61,7 @@ class _Seq(ctypes.Structure):
                                              "n_local", "local_head", "local_cap")] + \
                [(n, ctypes.c_void_p) for n in ("k_sink", "v_sink", "k_codes", "k_hi", "k_bidx",
                                                "k_meta", "k_res", "v_codes", "v_meta", "v_res",
-                                               "v_local")]
+                                               "v_local")] + [("rope_base", ctypes.c_double)]
 
 
 def lib() -> ctypes.CDLL:
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.kvq_or_seq_len.argtypes = [ctypes.POINTER(_Seq)]
         L.kvq_or_seq_len.restype = Lg
         L.kvq_or_attend.argtypes = [P, I, P, P, Lg, I, P]
+        L.kvq_or_rope.argtypes = [P, Lg, I, ctypes.c_double, Lg]
         L.kvq_or_seq_attend.argtypes = [ctypes.POINTER(_Seq), P, I, P]
         L.kvq_or_seq_attend.restype = I
         _lib = L
@@ -192,6 +193,14 @@ def kitty_select(page: np.ndarray, n_boost: int):
     return score, bidx
 
 
+def rope(K: np.ndarray, base: float = 10000.0, t0: int = 0) -> np.ndarray:
+    """Rotary position embedding of K [L, D] (row i at position t0 + i), fp64: channel
+    pair (2j, 2j+1) turns by (t0 + i) * base^(-2j/D) (KVQuant notes, mechanism two)."""
+    out = np.array(K, np.float64, copy=True, order="C")
+    lib().kvq_or_rope(_p(out), out.shape[0], out.shape[1], float(base), int(t0))
+    return out
+
+
 def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     """fp64 softmax attention. q: [n_heads, D], K, V: [L, D] (any float dtype)."""
     q = np.ascontiguousarray(q, np.float64)
@@ -221,10 +230,11 @@ class OracleCache:
     """
 
     def __init__(self, B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi",
-                 max_T=None, v_bits=None):
+                 max_T=None, v_bits=None, rope_base=0.0):
         assert mode in ("kivi", "kitty")
         self.B, self.H_q, self.H_kv, self.D, self.G, self.bits = B, H_q, H_kv, D, G, bits
         self.vbits = bits if not v_bits else v_bits  # value codes may use their own width
+        self.rope_base = float(rope_base)  # > 0: keys stored before RoPE, rotated when attended
         self.S, self.R, self.n_boost, self.mode = S, (G if R is None else R), n_boost, mode
         self.Gv = min(G, D)
         self.kitty = mode == "kitty"
@@ -355,6 +365,7 @@ class OracleCache:
         s.k_res = ptr(self.k_res[b, h])
         s.v_codes, s.v_meta = ptr(self.v_codes[b, h]), ptr(self.v_meta[b, h])
         s.v_res, s.v_local = ptr(self.v_res[b, h]), ptr(self.v_local[b, h])
+        s.rope_base = self.rope_base
         return s
 
     def rows(self, b: int, h: int):

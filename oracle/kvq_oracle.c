@@ -23,7 +23,13 @@
  *     sentinel n_boost+1 ("Kitty: Accurate and Efficient 2-Bit KV Cache
  *     Quantization ...", Sec. 3.2 and Sec. 4.1, Algorithm 1);
  *   - decode attention softmax(q . K^T / sqrt(d)) . V over the dequantized cache
- *     ("BitDecoding", Sec. II, Fig. 2 caption), accumulated in fp64.
+ *     ("BitDecoding", Sec. II, Fig. 2 caption), accumulated in fp64;
+ *   - pre-RoPE keys ("KVQuant 完全拆解", mechanism two): the cache holds keys
+ *     before the rotary position embedding; attention dequantizes key t, rotates
+ *     channel pair (2i, 2i+1) by the angle t * theta_i, theta_i = base^(-2i/d)
+ *     (i = 0 .. d/2-1, the page's R_{theta,m} with its 1-based index shifted), and
+ *     only then takes the dot product with the (already rotated) query.  t is the
+ *     token's 0-based position in the sequence (sink, packed, residual order).
  *
  * Precision (the pages leave it open; this is the reading taken): min/max are
  * exact fp16 comparisons, the scale is computed in fp32 then rounded to fp16,
@@ -291,6 +297,7 @@ typedef struct {
     const uint16_t *v_meta;            /* [T_v][D/Gv][2] */
     const uint16_t *v_res;             /* [n_vres][D] */
     const uint16_t *v_local;           /* [local_cap][D] ring, oldest at local_head */
+    double rope_base;                  /* > 0: keys are stored before RoPE with this base */
 } kvq_or_seq;
 
 long kvq_or_seq_len(const kvq_or_seq *s)
@@ -390,6 +397,24 @@ void kvq_or_attend(const double *q, int n_heads, const double *K, const double *
     free(z);
 }
 
+/* RoPE of rows [0, L) of K [L][D] in place, row i at position t0 + i: channel pair
+ * (2j, 2j+1) turns by the angle (t0 + i) * base^(-2j/D) (KVQuant notes, mechanism
+ * two; fp64 throughout). */
+void kvq_or_rope(double *K, long L, int D, double base, long t0)
+{
+    for (long i = 0; i < L; i++) {
+        double *k = K + i * D;
+        double pos = (double)(t0 + i);
+        for (int j = 0; j < D / 2; j++) {
+            double theta = pow(base, -2.0 * (double)j / (double)D);
+            double c = cos(pos * theta), sn = sin(pos * theta);
+            double a = k[2 * j], b = k[2 * j + 1];
+            k[2 * j] = a * c - b * sn;
+            k[2 * j + 1] = a * sn + b * c;
+        }
+    }
+}
+
 /* Convenience: attention of the g query heads that share one (b, h_kv) sequence.
  * q16: fp16 [g][D]; out: fp64 [g][D]; scratch sized internally. */
 int kvq_or_seq_attend(const kvq_or_seq *s, const uint16_t *q16, int g, double *out)
@@ -408,6 +433,8 @@ int kvq_or_seq_attend(const kvq_or_seq *s, const uint16_t *q16, int g, double *o
     for (long i = 0; i < (long)g * D; i++)
         q[i] = kvq_or_h2f(q16[i]);
     kvq_or_seq_rows(s, Kh, Vh);
+    if (s->rope_base > 0.0)
+        kvq_or_rope(Kh, L, D, s->rope_base, 0);
     kvq_or_attend(q, g, Kh, Vh, L, D, out);
     free(Kh);
     free(Vh);
