@@ -484,7 +484,8 @@ def main():
         Kl = torch.roll(K0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
         Vl = torch.roll(V0, shifts=li * 977, dims=2)[:, :, : L0 - (wl.G - 1) + fill].contiguous()
         c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                         n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=dev, v_bits=wl.v_bits)
+                         n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=dev, v_bits=wl.v_bits,
+                         rope_base=wl.rope_base)
         c.prefill(Kl, Vl)
         caches.append(c)
         del Kl, Vl
@@ -608,7 +609,7 @@ def main():
         "data": "synthetic (seeded; shapes and outlier structure of the workload)",
         "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
                    "T": wl.T, "G": wl.G, "R": wl.R, "bits": wl.bits, "v_bits": wl.vbits, "S": wl.S,
-                   "n_boost": wl.n_boost, "mode": wl.mode,
+                   "n_boost": wl.n_boost, "mode": wl.mode, "rope_base": wl.rope_base,
                    "step": "append_token + decode_attn + flush_group (when full), one layer",
                    "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (
                        N_LAYERS, dec_bytes / 1e6, N_LAYERS * dec_bytes / 1e9),

@@ -40,7 +40,8 @@ class KvqError(RuntimeError):
 class Config(ctypes.Structure):
     """kvq_config"""
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "H_q", "H_kv", "D", "G", "bits", "S", "R",
-                                              "n_boost", "mode", "v_bits")] + [("max_T", ctypes.c_int64)]
+                                              "n_boost", "mode", "v_bits")] + [("max_T", ctypes.c_int64)] + \
+               [("rope", ctypes.c_int32), ("rope_base", ctypes.c_float)]
 
 
 class Cache(ctypes.Structure):
@@ -107,9 +108,11 @@ def _check(code: int, what: str):
 
 
 def make_config(B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi", max_T=0,
-                v_bits=0) -> Config:
+                v_bits=0, rope_base=0.0) -> Config:
+    """rope_base > 0: keys are stored before RoPE and rotated in decode attention."""
     m = {"kivi": KVQ_MODE_KIVI, "kitty": KVQ_MODE_KITTY}[mode]
-    return Config(B, H_q, H_kv, D, G, bits, S, G if R is None else R, n_boost, m, v_bits or 0, max_T)
+    return Config(B, H_q, H_kv, D, G, bits, S, G if R is None else R, n_boost, m, v_bits or 0, max_T,
+                  1 if rope_base else 0, float(rope_base or 0.0))
 
 
 class KVQCache:
@@ -120,10 +123,10 @@ class KVQCache:
     current torch stream."""
 
     def __init__(self, B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi",
-                 max_T=0, device="cuda", v_bits=0):
+                 max_T=0, device="cuda", v_bits=0, rope_base=0.0):
         import torch
         self.torch = torch
-        self.cfg = make_config(B, H_q, H_kv, D, G, bits, S, R, n_boost, mode, max_T, v_bits)
+        self.cfg = make_config(B, H_q, H_kv, D, G, bits, S, R, n_boost, mode, max_T, v_bits, rope_base)
         _check(lib.kvq_config_check(ctypes.byref(self.cfg)), "config")
         self.device = torch.device(device)
         self.c = Cache()

@@ -151,6 +151,9 @@ int kvq_config_check(const kvq_config *c) {
     if (gv != 32 && gv != 64 && gv != 128 && gv != 256) return KVQ_ERR_UNSUPPORTED;
     if (!key_slices_ok(c)) return KVQ_ERR_UNSUPPORTED;
     if (c->max_T % c->G) return KVQ_ERR_INVALID_ARG;
+    if (c->rope != 0 && c->rope != 1) return KVQ_ERR_INVALID_ARG;
+    if (!(c->rope_base >= 0.0f) || c->rope_base > 3.0e38f) return KVQ_ERR_INVALID_ARG;
+    if (c->rope && kitty(c)) return KVQ_ERR_UNSUPPORTED;
     if (!kitty(c)) {
         if (c->n_boost != 0) return KVQ_ERR_INVALID_ARG;
         if (c->R < c->G || c->R % c->G) return KVQ_ERR_INVALID_ARG;
@@ -496,6 +499,8 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.cap_v = (int)cap_v(c);
     p.R_local = kitty(c) ? c->R : 1;
     p.max_T = c->max_T;
+    p.rope = c->rope;
+    p.rope_base = c->rope_base > 0.0f ? c->rope_base : 10000.0f;
     p.n_sink = k->n_sink;
     p.T_k = k->T_k;
     p.n_kres = k->n_kres;

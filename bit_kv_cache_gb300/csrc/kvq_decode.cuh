@@ -147,9 +147,9 @@ __device__ __forceinline__ void load_v(const DecodeParams &p, int u, int64_t tl,
     for (int i = 0; i < DPL; i++) vv[i] = h2f(row[d + i]);
 }
 
-template <int DPL>
+template <int DPL, bool RP = false>
 __device__ void generic_range(const DecodeParams &p, int u, const uint16_t *q_w, int64_t a, int64_t b,
-                              GenState<DPL> &st) {
+                              GenState<DPL> &st, const float *rt = nullptr) {
     const int lane = threadIdx.x & 31, D = p.D, g = p.g;
     const float C = kLog2e * rsqrtf((float)D);
     for (int64_t base = a; base < b; base += 32) {
@@ -163,6 +163,16 @@ __device__ void generic_range(const DecodeParams &p, int u, const uint16_t *q_w,
             for (int d = 0; d < D; d += 8) {
                 float kv[8];
                 load_k8(p, u, tl, d, kv);
+                if (RP) {  // pre-RoPE keys: pairs (d + 2i, d + 2i + 1) turn by tl * theta
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int pr = d / 2 + i;
+                        const float2 cs = rope_cs((float)tl, rt[kRopeHi + pr], rt[kRopeLo + pr]);
+                        const float ka = kv[2 * i], kb = kv[2 * i + 1];
+                        kv[2 * i] = fmaf(ka, cs.x, -kb * cs.y);
+                        kv[2 * i + 1] = fmaf(ka, cs.y, kb * cs.x);
+                    }
+                }
 #pragma unroll
                 for (int h = 0; h < 8; h++) {
                     if (h < g) {
@@ -275,6 +285,18 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long
 //   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
 //      CTA resets both counters to zero for the next call.
 // ---------------------------------------------------------------------------------
+// RoPE tables passed by value to the pre-RoPE kernels (theta_j hi, lo, cos, sin;
+// layout as in shared memory); the other kernels take an empty argument.
+struct RopeTab {
+    float v[kRopeFloats];
+};
+template <bool RP>
+struct RopeArg {};
+template <>
+struct RopeArg<true> {
+    RopeTab t;
+};
+
 // A unit of sequence u in a pool: the pool's items [s0, s0 + n) are u's.
 struct Seg {
     int u, s0, n;
@@ -390,8 +412,8 @@ static __device__ void publish_whole(const DecodeParams &p, int u, int cnt, int 
     }
 }
 
-template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG>
-__global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p) {
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG, bool RP>
+__global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p, const RopeArg<RP> ra) {
     // Work units: a warp, or with PAIR (tile kernels) a warp pair -- query warp and
     // value warp -- that shares one region of shared memory.
     constexpr int NU = PAIR ? NW / 2 : NW;
@@ -415,6 +437,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     constexpr bool RG = FAST && PG;  // paged cache: per-sequence item counts
     int *s_pf = reinterpret_cast<int *>(smem + NU * wbytes);  // paged: [B + 1] fast items before slot b
     int *s_pm = s_pf + (p.B + 1);                             // paged: [B + 1] mini items before slot b
+    float *s_rt = reinterpret_cast<float *>(smem + NU * wbytes);  // pre-RoPE: the tables (never paged)
+    if constexpr (RP) {
+        for (int i = tid; i < kRopeFloats; i += NW * 32) s_rt[i] = ra.t.v[i];
+        __syncthreads();
+    }
 
     if (RG && warp == 0) {
         // per-slot item counts from the device lengths, then an exclusive scan
@@ -540,8 +567,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         // paged range may cross more sequences: a segment between the first and the
         // last holds all of its sequence's items of this pool, and its unit writes it
         // to its own pool slot and publishes it alone.
-        PairWarp<KB, VB, KITTY, RG> pw(p, wbase);
-        MiniWarp<KB, VB, KITTY, RG> mw(p, wbase, 0);
+        PairWarp<KB, VB, KITTY, RG, RP> pw(p, wbase);
+        MiniWarp<KB, VB, KITTY, RG, RP> mw(p, wbase, 0);
+        pw.rt = s_rt;
+        mw.rt = s_rt;
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
         if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // the pair's partner
         if (slot_lane >= 0 && slot_lane < nu) my_slot = take_slot();
@@ -592,7 +621,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             const int64_t b = kvq_min64(a + p.gen_chunk, p.n_gen);
             uint16_t *q_w = reinterpret_cast<uint16_t *>(wbase + part_bytes(D));
             load_q_gen(p, u, q_w);
-            generic_range<DPL>(p, u, q_w, a, b, st);
+            generic_range<DPL, RP>(p, u, q_w, a, b, st, s_rt);
             generic_store<DPL>(p, st, reinterpret_cast<float *>(wbase));
             seg1 = u;
             cnt1 = 1;
@@ -697,11 +726,34 @@ constexpr int tile_units(int kb, int vb, bool kitty, int n_boost) {
 // Tile kernels on warp pairs (query warp + value warp per unit): 4-bit keys.
 constexpr bool tile_pair(int kb, int vb) { return kb == 4 && vb == 4; }
 
-template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG = false>
+// The RoPE tables of (D, base): theta_j = base^(-2j/D) in double, kept as a two-float
+// hi + lo, and its cosine and sine (computed once per (D, base) on the host).
+static const RopeTab &rope_tables(int D, float base) {
+    static thread_local RopeTab tab;
+    static thread_local int tD = -1;
+    static thread_local float tb = -1.f;
+    if (tD != D || tb != base) {
+        for (int i = 0; i < kRopeFloats; i++) tab.v[i] = 0.f;
+        for (int j = 0; j < D / 2 && j < 128; j++) {
+            const double th = pow((double)base, -2.0 * (double)j / (double)D);
+            const float hi = (float)th;
+            tab.v[kRopeHi + j] = hi;
+            tab.v[kRopeLo + j] = (float)(th - (double)hi);
+            tab.v[kRopeC1 + j] = (float)cos(th);
+            tab.v[kRopeS1 + j] = (float)sin(th);
+        }
+        tD = D;
+        tb = base;
+    }
+    return tab;
+}
+
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG = false, bool RP = false>
 static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
     size_t smem = decode_smem_bytes(KB, VB, KITTY, p.n_boost, p.D, FAST);
     if (PG) smem += (size_t)(p.B + 1) * 8;  // paged: per-slot item prefixes
-    auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW, PG>;
+    if (RP) smem += kRopeFloats * 4;        // pre-RoPE: the tables
+    auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW, PG, RP>;
     // The dynamic shared-memory limit is raised once per device to the most any
     // configuration of this instantiation asks for (the opt-in maximum).
     static int raised[64] = {0};
@@ -716,32 +768,35 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
         if (dev >= 0 && dev < 64) raised[dev] = 1;
     }
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidValue;
-    k<<<(unsigned)(p.C_f + p.C_m + p.C_g), NW * 32, smem, st>>>(p);
+    RopeArg<RP> ra;
+    if constexpr (RP) ra.t = rope_tables(p.D, p.rope_base);
+    k<<<(unsigned)(p.C_f + p.C_m + p.C_g), NW * 32, smem, st>>>(p, ra);
     return cudaGetLastError();
 }
 
 // KIVI tiles of key width KB and value width VB; p.wpc == tile_units(KB, VB).
-template <int KB, int VB, bool PG>
+// Pre-RoPE tiles run on single warps (their QK is on the CUDA cores).
+template <int KB, int VB, bool PG, bool RP = false>
 static cudaError_t launch_tiles(const DecodeParams &p, cudaStream_t st) {
     constexpr int U = tile_units(KB, VB, false, 0);
-    constexpr bool PAIR = tile_pair(KB, VB);
+    constexpr bool PAIR = tile_pair(KB, VB) && !RP;
     if (p.wpc != U) return cudaErrorInvalidValue;
-    return launch_one<KB, VB, false, true, PAIR, 4, PAIR ? 2 * U : U, PG>(p, st);
+    return launch_one<KB, VB, false, true, PAIR, 4, PAIR ? 2 * U : U, PG, RP>(p, st);
 }
 
 // Key / value width pair of a tile launch -> its instantiation.
-template <bool PG>
+template <bool PG, bool RP = false>
 static cudaError_t launch_tiles_any(const DecodeParams &p, cudaStream_t st) {
     switch (p.bits * 16 + p.vbits) {
-        case 2 * 16 + 2: return launch_tiles<2, 2, PG>(p, st);
-        case 2 * 16 + 4: return launch_tiles<2, 4, PG>(p, st);
-        case 2 * 16 + 8: return launch_tiles<2, 8, PG>(p, st);
-        case 4 * 16 + 2: return launch_tiles<4, 2, PG>(p, st);
-        case 4 * 16 + 4: return launch_tiles<4, 4, PG>(p, st);
-        case 4 * 16 + 8: return launch_tiles<4, 8, PG>(p, st);
-        case 8 * 16 + 2: return launch_tiles<8, 2, PG>(p, st);
-        case 8 * 16 + 4: return launch_tiles<8, 4, PG>(p, st);
-        case 8 * 16 + 8: return launch_tiles<8, 8, PG>(p, st);
+        case 2 * 16 + 2: return launch_tiles<2, 2, PG, RP>(p, st);
+        case 2 * 16 + 4: return launch_tiles<2, 4, PG, RP>(p, st);
+        case 2 * 16 + 8: return launch_tiles<2, 8, PG, RP>(p, st);
+        case 4 * 16 + 2: return launch_tiles<4, 2, PG, RP>(p, st);
+        case 4 * 16 + 4: return launch_tiles<4, 4, PG, RP>(p, st);
+        case 4 * 16 + 8: return launch_tiles<4, 8, PG, RP>(p, st);
+        case 8 * 16 + 2: return launch_tiles<8, 2, PG, RP>(p, st);
+        case 8 * 16 + 4: return launch_tiles<8, 4, PG, RP>(p, st);
+        case 8 * 16 + 8: return launch_tiles<8, 8, PG, RP>(p, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -292,10 +292,30 @@ struct PageIds<true> {
     }
 };
 
+// Pre-RoPE keys (KVQuant notes, mechanism two).  The tables (shared memory, 128
+// entries each): theta_j as a two-float hi + lo, cos theta_j, sin theta_j.
+constexpr int kRopeHi = 0, kRopeLo = 128, kRopeC1 = 256, kRopeS1 = 384, kRopeFloats = 512;
+
+// (cos, sin) of pos * theta_j, the angle reduced modulo 2 pi: the product's rounding
+// error is recovered with an FMA and 2 pi is subtracted in two parts (the Cody-Waite
+// reduction), so the reduced angle stays within a few 1e-7 rad for any position
+// below 2^24; then the sine and cosine of an angle in [-pi, pi].
+__device__ __forceinline__ float2 rope_cs(float pos, float th_hi, float th_lo) {
+    const float ph = pos * th_hi;
+    const float pe = fmaf(pos, th_hi, -ph);  // pos * th_hi - ph, exactly
+    const float pl = fmaf(pos, th_lo, pe);
+    const float n = rintf(ph * 0.159154943091895336f);   // 1 / (2 pi)
+    float r = fmaf(-n, 6.28318548202514648f, ph);         // 2 pi rounded to float
+    r = fmaf(-n, -1.74845553146951720e-7f, r) + pl;       // 2 pi minus that
+    float s, c;
+    __sincosf(r, &s, &c);
+    return make_float2(c, s);
+}
+
 // ---------------------------------------------------------------------------
 // Packed tiles
 // ---------------------------------------------------------------------------
-template <int KB, int VB, bool KITTY, bool PG = false>
+template <int KB, int VB, bool KITTY, bool PG = false, bool RP = false>
 struct FastWarp {
     using T = Tile<KB, VB>;
     using CK = typename T::K;
@@ -308,6 +328,7 @@ struct FastWarp {
     uint32_t phase = 0;    // bit s: parity of the next completion of slot s
     uint32_t pending = 0;  // bit s: slot s has copies in flight
     PageIds<PG> pid;       // page index of a logical page of sequence u
+    const float *rt = nullptr;  // RP: the RoPE tables
 
     __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
         : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
@@ -544,6 +565,11 @@ struct FastWarp {
     }
         KVQ_Z(0) KVQ_Z(1) KVQ_Z(2) KVQ_Z(3) KVQ_Z(4) KVQ_Z(5) KVQ_Z(6) KVQ_Z(7)
 #undef KVQ_Z
+        softmax_max(tm, m, l, mn, a, grow);
+    }
+    // The running maximum from the tile's maximum tm of the lane's head.
+    __device__ __forceinline__ static void softmax_max(float tm, float &m, float &l, float &mn, float &a,
+                                                       bool &grow) {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
         const float nm = fmaxf(m, tm);
@@ -552,6 +578,90 @@ struct FastWarp {
         m = nm;
         l *= a;
         mn *= a;
+    }
+    // The same from logits z already in log2 units (pre-RoPE path).
+    __device__ __forceinline__ void softmax_begin_z(const float (&z)[CK::NJ][2], float &m, float &l, float &mn,
+                                                    float &a0, float &a1, bool &grow) const {
+        float tm = -INFINITY, a;
+#pragma unroll
+        for (int j = 0; j < CK::NJ; j++) tm = fmaxf(tm, fmaxf(z[j][0], z[j][1]));
+        softmax_max(tm, m, l, mn, a, grow);
+        const int t = lane & 3;
+        a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
+        a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
+    }
+
+    // Pre-RoPE keys (KVQuant notes, mechanism two): key t is dequantized in fp32, its
+    // channel pair (2j, 2j+1) turned by t * theta_j and dotted with the (already
+    // rotated) query on the CUDA cores.  Lane (g, t) takes word row g -- KFPI tokens
+    // from position pos0 on -- and the pairs j = t + 4i; its angles step from token
+    // to token by the rotation theta_j.  This call covers i in [i0, i0 + n).
+    __device__ __forceinline__ void qk_rope_part(const unsigned char *st, float pos0, int i0, int n,
+                                                 float (&acc)[CK::FPI][4]) const {
+        const int gq = lane >> 2, t = lane & 3;
+        const uint16_t *qraw = reinterpret_cast<const uint16_t *>(wbase + L.qraw);
+        constexpr uint32_t MASK = (1u << KB) - 1u;
+#pragma unroll
+        for (int ii = 0; ii < 2; ii++) {
+            if (ii >= n) break;
+            const int pr = t + 4 * (i0 + ii);
+            const uint2 w = *reinterpret_cast<const uint2 *>(st + T::OFF_K + gq * T::K_STRIDE + 8 * pr);
+            const uint2 km = *reinterpret_cast<const uint2 *>(st + T::OFF_KM + 8 * pr);
+            const float2 sa = unpack_half2(km.x), sb = unpack_half2(km.y);  // (scale, min)
+            float qa[4], qb[4];
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                const float2 qq = unpack_half2(*reinterpret_cast<const uint32_t *>(qraw + h * 128 + 2 * pr));
+                qa[h] = qq.x;
+                qb[h] = qq.y;
+            }
+            const float2 cs = rope_cs(pos0, rt[kRopeHi + pr], rt[kRopeLo + pr]);
+            const float c1 = rt[kRopeC1 + pr], s1 = rt[kRopeS1 + pr];
+            float c = cs.x, s = cs.y;
+#pragma unroll
+            for (int k = 0; k < CK::FPI; k++) {
+                const float fa = __uint_as_float(0x4B000000u | ((w.x >> (KB * k)) & MASK)) - 8388608.0f;
+                const float fb = __uint_as_float(0x4B000000u | ((w.y >> (KB * k)) & MASK)) - 8388608.0f;
+                const float ka = fmaf(fa, sa.x, sa.y), kb = fmaf(fb, sb.x, sb.y);
+                const float ra = fmaf(ka, c, -kb * s), rb = fmaf(ka, s, kb * c);
+#pragma unroll
+                for (int h = 0; h < 4; h++) acc[k][h] = fmaf(qa[h], ra, fmaf(qb[h], rb, acc[k][h]));
+                const float cn = fmaf(c, c1, -s * s1);
+                s = fmaf(s, c1, c * s1);
+                c = cn;
+            }
+        }
+    }
+    // The four lanes of a word row hold partial sums over their pairs for all heads:
+    // a reduce-scatter leaves head t in lane t; z in log2 units, in the mma path's
+    // layout (z[J][0] token KFPI g + J, z[J][1] token KFPI g + KFPI/2 + J).
+    __device__ __forceinline__ void qk_rope_finish(float (&acc)[CK::FPI][4], float (&z)[CK::NJ][2]) const {
+        const int t = lane & 3;
+        const bool b2 = (t & 2) != 0, b1 = (t & 1) != 0;
+        const float C = kLog2e * rsqrtf((float)T::D);
+        float zt[CK::FPI];
+#pragma unroll
+        for (int k = 0; k < CK::FPI; k++) {
+            const float s0 = b2 ? acc[k][0] : acc[k][2], s1 = b2 ? acc[k][1] : acc[k][3];
+            float k0 = b2 ? acc[k][2] : acc[k][0], k1 = b2 ? acc[k][3] : acc[k][1];
+            k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            const float s2 = b1 ? k0 : k1;
+            float kk = b1 ? k1 : k0;
+            kk += __shfl_xor_sync(0xffffffffu, s2, 1);
+            zt[k] = kk * C;
+        }
+#pragma unroll
+        for (int j = 0; j < CK::NJ; j++) {
+            z[j][0] = zt[j];
+            z[j][1] = zt[j + CK::FPI / 2];
+        }
+    }
+    __device__ __forceinline__ static void zero_acc(float (&acc)[CK::FPI][4]) {
+#pragma unroll
+        for (int k = 0; k < CK::FPI; k++)
+#pragma unroll
+            for (int h = 0; h < 4; h++) acc[k][h] = 0.f;
     }
 
     // Position of tile token tk in a p' row: the k index of the PV B operand under the
@@ -622,17 +732,29 @@ struct FastWarp {
             for (int e = 0; e < 4; e++) O[o][e] = 0.f;
         float acc[CK::NJ][4], cm[4];
         float z[CK::NJ][2];
+        float accr[RP ? CK::FPI : 1][4];  // RP: per-token partial dot products
+        // RP: position of the lane's first token in tile i
+        auto rpos = [&](int64_t i) { return (float)(p.n_sink + (t0 + i) * T::TOK + CK::FPI * (lane >> 2)); };
         bool ok = true;
 
         // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
         ok &= wait_slot(0);
+        if (RP) {
+            zero_acc(reinterpret_cast<float (&)[CK::FPI][4]>(accr));
 #pragma unroll
-        for (int sl = 0; sl < 8; sl++) qk_slab(sl, kslot(0), acc, cm);
-        if (KITTY && p.n_boost > 0) qk_boost(kslot(0), acc);
+            for (int sl = 0; sl < 8; sl++)
+                qk_rope_part(kslot(0), rpos(0), 2 * sl, 2, reinterpret_cast<float (&)[CK::FPI][4]>(accr));
+            qk_rope_finish(reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
+        } else {
+#pragma unroll
+            for (int sl = 0; sl < 8; sl++) qk_slab(sl, kslot(0), acc, cm);
+            if (KITTY && p.n_boost > 0) qk_boost(kslot(0), acc);
+        }
         {
             float a0, a1;
             bool grow;
-            softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
+            if (RP) softmax_begin_z(z, m, l, mn, a0, a1, grow);
+            else softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
 #pragma unroll
             for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vmslot(0), pb0, m, l, mn);
         }
@@ -649,6 +771,7 @@ struct FastWarp {
             if (!ok) break;
             const uint16_t *pb = pb0 + cur * 4 * T::PROW;
             if (more) {  // the PV steps spread evenly over the 8 key slabs
+                if (RP) zero_acc(reinterpret_cast<float (&)[CK::FPI][4]>(accr));
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
                     if (T::PV_STEPS >= 8) {
@@ -657,8 +780,13 @@ struct FastWarp {
                     } else if (sl % (8 / T::PV_STEPS) == 0) {
                         pv_step(sl / (8 / T::PV_STEPS), vslot(cur), pb, O);
                     }
-                    qk_slab(sl, kslot(nxt), acc, cm);
+                    if (RP)
+                        qk_rope_part(kslot(nxt), rpos(i + 1), 2 * sl, 2,
+                                     reinterpret_cast<float (&)[CK::FPI][4]>(accr));
+                    else
+                        qk_slab(sl, kslot(nxt), acc, cm);
                 }
+                if (RP) qk_rope_finish(reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
                 if (KITTY && p.n_boost > 0) qk_boost(kslot(nxt), acc);
             } else {
 #pragma unroll
@@ -667,7 +795,8 @@ struct FastWarp {
             if (more) {
                 float a0, a1;
                 bool grow;
-                softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
+                if (RP) softmax_begin_z(z, m, l, mn, a0, a1, grow);
+                else softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
                 if (grow) {  // O holds tiles <= i relative to the previous maximum
 #pragma unroll
                     for (int o = 0; o < 8; o++) {
@@ -735,9 +864,9 @@ struct FastWarp {
 // streams the value codes, rescales O and runs PV.  Handoff per p' buffer b:
 // "full" (query -> value) and "empty" (value -> query) mbarriers, waits bounded.
 // ---------------------------------------------------------------------------
-template <int KB, int VB, bool KITTY, bool PG = false>
-struct PairWarp : FastWarp<KB, VB, KITTY, PG> {
-    using Base = FastWarp<KB, VB, KITTY, PG>;
+template <int KB, int VB, bool KITTY, bool PG = false, bool RP = false>
+struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
+    using Base = FastWarp<KB, VB, KITTY, PG, RP>;
     using T = typename Base::T;
     using CK = typename T::K;
     using CV = typename T::V;
@@ -968,7 +1097,7 @@ __device__ __forceinline__ const uint16_t *krow16(const DecodeParams &p, const S
     return p.k_res + ((size_t)u * p.cap_k + (tl - sq.n_sink - sq.T_k)) * 128;
 }
 
-template <int KB, int VB, bool KITTY, bool PG = false>
+template <int KB, int VB, bool KITTY, bool PG = false, bool RP = false>
 struct MiniWarp {
     const DecodeParams &p;
     unsigned char *wbase;
@@ -977,6 +1106,7 @@ struct MiniWarp {
     uint64_t *bars;
     uint32_t phase = 0, pending = 0;
     SeqLen sq;  // lengths of sequence u
+    const float *rt = nullptr;  // RP: the RoPE tables
 
     // packed-key block layout in the key half of a slot
     static constexpr int MB_W = 0, MB_M = 512, MB_HI = 1024;
@@ -1078,7 +1208,27 @@ struct MiniWarp {
                         b1 = hmul2(*reinterpret_cast<const uint32_t *>(qraw + hq * 128 + 16 * sl + 8 + 2 * t),
                                    0x2C002C00u);
                     }
-                    mma_16816(s, a[0], a[1], a[2], a[3], b0, b1);
+                    if (RP) {
+                        // register r: channel pair 8 sl + t (+4 for r >= 2) of token tok0 + g
+                        // (+8 for odd r), turned by its position in fp32, then split into
+                        // fp16 hi + lo (two mmas, 22 significant bits)
+                        uint32_t ah[4], al[4];
+#pragma unroll
+                        for (int r = 0; r < 4; r++) {
+                            const int pr = 8 * sl + t + 4 * (r >> 1);
+                            const float pos = (float)(mt.tok0 + gq + 8 * (r & 1));
+                            const float2 cs = rope_cs(pos, rt[kRopeHi + pr], rt[kRopeLo + pr]);
+                            const float2 kv = unpack_half2(a[r]);
+                            const float rx = fmaf(kv.x, cs.x, -kv.y * cs.y), ry = fmaf(kv.x, cs.y, kv.y * cs.x);
+                            ah[r] = pack_half2(rx, ry);
+                            const float2 hv = unpack_half2(ah[r]);
+                            al[r] = pack_half2(rx - hv.x, ry - hv.y);
+                        }
+                        mma_16816(s, ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma_16816(s, al[0], al[1], al[2], al[3], b0, b1);
+                    } else {
+                        mma_16816(s, a[0], a[1], a[2], a[3], b0, b1);
+                    }
                 }
             } else {
                 // Kitty mixed block: 16 tokens of packed keys, rows g / g+8 <-> tokens g / g+8
@@ -1094,7 +1244,7 @@ struct MiniWarp {
                     uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++) wv[kk] = w[16 * sl + 4 * kk + t];
-                    FastWarp<2, 2, KITTY, false>::template split<Codes<2>>(wv, x, xs);
+                    FastWarp<2, 2, KITTY, false, false>::template split<Codes<2>>(wv, x, xs);
                     uint32_t a[4];
 #pragma unroll
                     for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;
@@ -1129,7 +1279,7 @@ struct MiniWarp {
                         uint32_t wv[4], x[4], xs[4];
 #pragma unroll
                         for (int kk = 0; kk < 4; kk++) wv[kk] = hw[16 * s2 + 4 * kk + t];
-                        FastWarp<2, 2, KITTY, false>::template split<Codes<2>>(wv, x, xs);
+                        FastWarp<2, 2, KITTY, false, false>::template split<Codes<2>>(wv, x, xs);
                         uint32_t a[4];
 #pragma unroll
                         for (int r = 0; r < 4; r++) a[r] = (x[r] >> (2 * gq)) & 0x00030003u;

@@ -97,6 +97,8 @@ struct DecodeParams {
     int B, H_kv, g, D, G, bits, vbits, Gv, n_boost, kitty;  // bits: keys, vbits: values
     int S_cap, cap_k, cap_v, R_local;
     int64_t max_T;
+    int rope;              // keys stored before RoPE: rotate key t by t * theta_j
+    float rope_base;
     // lengths
     int64_t n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head, L;
     // buffers
@@ -148,6 +150,7 @@ cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st);
 cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
 cudaError_t launch_decode_paged(const DecodeParams &p, cudaStream_t st);  // p.lens set
+cudaError_t launch_decode_rope(const DecodeParams &p, bool fast, cudaStream_t st);  // p.rope set
 size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bool fast);
 int decode_warps_per_cta(int bits, int vbits, bool kitty, int n_boost, bool fast);
 

@@ -51,7 +51,7 @@ PagedWs paged_ws_layout(const kvq_config *c) {
 int paged_cfg_check(const kvq_config *c) {
     const int e = kvq_config_check(c);
     if (e) return e;
-    if (kitty(c) || !fast_supported(c) || c->B > KVQ_PAGED_MAX_B) return KVQ_ERR_UNSUPPORTED;
+    if (kitty(c) || c->rope || !fast_supported(c) || c->B > KVQ_PAGED_MAX_B) return KVQ_ERR_UNSUPPORTED;
     if (c->max_T / c->G < 1) return KVQ_ERR_INVALID_ARG;
     return KVQ_OK;
 }

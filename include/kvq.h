@@ -74,12 +74,22 @@ enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
  *   n_boost         : Kitty: key channels per page kept at INT4 (0..min(D,254)).
  *                     Must be 0 in KIVI mode.
  *   mode            : KVQ_MODE_KIVI or KVQ_MODE_KITTY
- *   max_T           : packed-token capacity per sequence, a multiple of G       */
+ *   max_T           : packed-token capacity per sequence, a multiple of G
+ *   rope            : 0: keys are attended as stored.  1: keys are stored before
+ *                     the rotary position embedding and decode attention rotates
+ *                     each one by its position (KVQuant notes, mechanism two:
+ *                     pre-RoPE quantization); the query is passed already rotated.
+ *                     Channel pair (2j, 2j+1) of the key at position t (its 0-based
+ *                     index in [sink | packed | residual]) turns by
+ *                     t * rope_base^(-2j/D).  KIVI mode, dense cache only.
+ *   rope_base       : the RoPE base (10000 if 0)                                */
 typedef struct {
     int32_t B, H_q, H_kv, D, G, bits;
     int32_t S, R, n_boost, mode;
     int32_t v_bits;
     int64_t max_T;
+    int32_t rope;
+    float rope_base;
 } kvq_config;
 
 /* Caller-owned device buffers and host-side lengths of one layer's cache.
@@ -126,7 +136,8 @@ const char *kvq_status_str(int status);
 /* Validates a configuration.  KVQ_OK, KVQ_ERR_INVALID_ARG (H_q % H_kv, G % fpi,
  * D % fpi, Gv | D, R % G (KIVI), n_boost range, max_T % G, non-positive sizes) or
  * KVQ_ERR_UNSUPPORTED (bits or v_bits not 2/4/8, Kitty with bits != 2, D not 64,
- * 128 or 256, more than 8 query heads per KV head). */
+ * 128 or 256, more than 8 query heads per KV head, rope with Kitty; rope not 0/1 or
+ * a negative or non-finite rope_base is KVQ_ERR_INVALID_ARG). */
 int kvq_config_check(const kvq_config *cfg);
 
 /* Byte size of each cache buffer for cfg: which = 0 k_codes, 1 k_hi, 2 k_bidx,
@@ -238,7 +249,7 @@ int kvq_decode_attn_noalloc(const kvq_config *cfg, const kvq_cache *cache, const
  * them and calls kvq_paged_init once.  Sequence b's logical tokens are
  * [sink | packed pages | residual].
  * Supported: KIVI mode, any widths, D = 128, H_q/H_kv <= 4, G a multiple of the tile
- * (256/bits tokens) and a power of two, B <= KVQ_PAGED_MAX_B.
+ * (256/bits tokens) and a power of two, B <= KVQ_PAGED_MAX_B, rope = 0.
  * --------------------------------------------------------------------------------- */
 #define KVQ_PAGED_MAX_B 512
 

@@ -52,6 +52,7 @@ class Workload:
     v_outlier_scale: float = 1.0
     v_bits: int = 0   # value code width; 0: the same as bits
     ragged: float = 0.0  # paged cache: slot lengths spread uniformly over T (1 +- ragged)
+    rope_base: float = 0.0  # > 0: keys cached before RoPE (rotated in decode attention)
 
     @property
     def vbits(self) -> int:
@@ -103,6 +104,11 @@ WORKLOADS.update({
 # lengths spread uniformly over 32768 * (1 +- 0.75) tokens (a continuous-batching mix).
 WORKLOADS["llama3_8b_gqa_paged"] = Workload("llama3_8b_gqa_paged", bits=2, seed=10, ragged=0.75,
                                             **dict(_GQA, B=8))
+
+
+# Pre-RoPE keys (KVQuant notes, mechanism two) on the Llama-3-8B GQA layer, with
+# Llama-3's RoPE base.
+WORKLOADS["llama3_8b_gqa_rope"] = Workload("llama3_8b_gqa_rope", bits=2, seed=11, rope_base=500000.0, **_GQA)
 
 
 def slot_lengths(wl: Workload) -> np.ndarray:

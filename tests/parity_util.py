@@ -11,9 +11,10 @@ TOL_REL = 2e-3
 def make_pair(wl, max_T, device):
     import bit_kv_cache_gb300 as kvq
     gpu = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                       n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=device, v_bits=wl.v_bits)
+                       n_boost=wl.n_boost, mode=wl.mode, max_T=max_T, device=device, v_bits=wl.v_bits,
+                       rope_base=wl.rope_base)
     ora = oracle.OracleCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
-                             n_boost=wl.n_boost, mode=wl.mode, v_bits=wl.v_bits)
+                             n_boost=wl.n_boost, mode=wl.mode, v_bits=wl.v_bits, rope_base=wl.rope_base)
     return gpu, ora
 
 

@@ -46,6 +46,16 @@ SMALL = {
     # G = 32: 8-bit keys fill one 32-token tile per page; 2-bit keys take the CUDA-core path
     "tiny_k8v2": (WORKLOADS["tiny_kivi"].replace(bits=8, v_bits=2), 256 + 31, 3),
     "tiny_k2v4": (WORKLOADS["tiny_kivi"].replace(v_bits=4), 256 + 31, 3),
+    # pre-RoPE keys: the tile path (fp32 rotated QK on the CUDA cores, rotated fp16
+    # tokens on tensor cores), widths, sinks, one query head per KV head, and the
+    # CUDA-core path (G = 32 below a 2-bit tile)
+    "rope_k2v2": (WORKLOADS["llama3_8b_gqa_rope"].replace(B=2, H_q=16, H_kv=4, T=1024), 1024 + 100, 4),
+    "rope_k4v4_sink": (WORKLOADS["llama3_8b_gqa_rope"].replace(B=2, H_q=16, H_kv=4, T=512, bits=4, S=8,
+                                                             rope_base=10000.0), 8 + 512 + 70, 3),
+    "rope_k8v2": (WORKLOADS["llama3_8b_gqa_rope"].replace(B=2, H_q=16, H_kv=4, T=512, bits=8, v_bits=2),
+                  512 + 70, 3),
+    "rope_mha": (WORKLOADS["llama7b_mha"].replace(B=2, H_q=8, H_kv=8, T=512, rope_base=10000.0), 512 + 77, 3),
+    "rope_tiny": (WORKLOADS["tiny_kivi"].replace(rope_base=10000.0), 256 + 31, 3),
 }
 
 
@@ -64,7 +74,7 @@ def test_prefill_state_and_attention(name):
     assert gpu.read_status() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi"])
+@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi", "rope_k2v2"])
 def test_decode_loop_crosses_flushes(name):
     """Enough steps that every buffer fills and is flushed at least once."""
     wl, L0, _ = SMALL[name]
@@ -187,5 +197,23 @@ def test_full_size_sampled(name):
     U = [(b, h) for b in range(wl.B) for h in range(wl.H_kv)]
     units = [U[i] for i in sorted(rng.choice(len(U), size=min(4, len(U)), replace=False))]
     assert_state_equal(gpu, ora)          # every code, scale, min: bit-exact
+    run_steps(gpu, ora, wl, 2, DEV, units=units)
+    assert gpu.read_status() == 0
+
+
+@pytest.mark.parametrize("wl", [WORKLOADS["llama3_8b_gqa_rope"],
+                                WORKLOADS["long_128k"].replace(rope_base=500000.0)],
+                         ids=["gqa_rope_32k", "rope_128k"])
+def test_full_size_pre_rope_sampled(wl):
+    """Pre-RoPE keys at full size: positions up to 131K, where an angle t * theta
+    evaluated in plain fp32 would be off by ~1e-2 rad."""
+    L0 = wl.T + 64
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    gpu, ora = make_pair(wl, max_T=wl.T + 2 * wl.G + wl.R, device=DEV)
+    prefill_both(gpu, ora, K, V, DEV)
+    del K, V
+    rng = np.random.default_rng(1)
+    U = [(b, h) for b in range(wl.B) for h in range(wl.H_kv)]
+    units = [U[i] for i in sorted(rng.choice(len(U), size=min(3, len(U)), replace=False))]
     run_steps(gpu, ora, wl, 2, DEV, units=units)
     assert gpu.read_status() == 0
