@@ -657,6 +657,15 @@ struct FastWarp {
             z[j][1] = zt[j + CK::FPI / 2];
         }
     }
+    // The whole pre-RoPE QK of a key half: a rolled loop over groups of two pairs (the
+    // unrolled form overflows the instruction cache).
+    __device__ __forceinline__ void qk_rope(const unsigned char *st, float pos0, float (&acc)[CK::FPI][4],
+                                            float (&z)[CK::NJ][2]) const {
+        zero_acc(acc);
+#pragma unroll 1
+        for (int i0 = 0; i0 < T::D / 8; i0 += 2) qk_rope_part(st, pos0, i0, 2, acc);
+        qk_rope_finish(acc, z);
+    }
     __device__ __forceinline__ static void zero_acc(float (&acc)[CK::FPI][4]) {
 #pragma unroll
         for (int k = 0; k < CK::FPI; k++)
@@ -740,11 +749,7 @@ struct FastWarp {
         // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
         ok &= wait_slot(0);
         if (RP) {
-            zero_acc(reinterpret_cast<float (&)[CK::FPI][4]>(accr));
-#pragma unroll
-            for (int sl = 0; sl < 8; sl++)
-                qk_rope_part(kslot(0), rpos(0), 2 * sl, 2, reinterpret_cast<float (&)[CK::FPI][4]>(accr));
-            qk_rope_finish(reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
+            qk_rope(kslot(0), rpos(0), reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
         } else {
 #pragma unroll
             for (int sl = 0; sl < 8; sl++) qk_slab(sl, kslot(0), acc, cm);
@@ -770,8 +775,11 @@ struct FastWarp {
             ok &= wait_slot(2 + cur);        // V(i): codes of i, (scale, min) of i+1
             if (!ok) break;
             const uint16_t *pb = pb0 + cur * 4 * T::PROW;
-            if (more) {  // the PV steps spread evenly over the 8 key slabs
-                if (RP) zero_acc(reinterpret_cast<float (&)[CK::FPI][4]>(accr));
+            if (RP && more) {  // PV of tile i, then the CUDA-core QK of tile i+1 (a rolled loop)
+#pragma unroll
+                for (int s = 0; s < T::PV_STEPS; s++) pv_step(s, vslot(cur), pb, O);
+                qk_rope(kslot(nxt), rpos(i + 1), reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
+            } else if (more) {  // the PV steps spread evenly over the 8 key slabs
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
                     if (T::PV_STEPS >= 8) {
@@ -780,13 +788,8 @@ struct FastWarp {
                     } else if (sl % (8 / T::PV_STEPS) == 0) {
                         pv_step(sl / (8 / T::PV_STEPS), vslot(cur), pb, O);
                     }
-                    if (RP)
-                        qk_rope_part(kslot(nxt), rpos(i + 1), 2 * sl, 2,
-                                     reinterpret_cast<float (&)[CK::FPI][4]>(accr));
-                    else
-                        qk_slab(sl, kslot(nxt), acc, cm);
+                    qk_slab(sl, kslot(nxt), acc, cm);
                 }
-                if (RP) qk_rope_finish(reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
                 if (KITTY && p.n_boost > 0) qk_boost(kslot(nxt), acc);
             } else {
 #pragma unroll
