@@ -79,7 +79,7 @@ def decode_bytes_struct(wl, st) -> int:
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in ("kvq_decode.cu", "kvq_decode.cuh", "kvq_decode_fast.cuh", "kvq_device.cuh", "kvq_internal.h",
-              "kvq_api.cu", "kvq_host.h"):
+              "kvq_api.cu", "kvq_host.h", "kvq_paged.cu", "kvq_decode_paged.cu", "kvq_decode_rope.cu"):
         with open(os.path.join(ROOT, "bit_kv_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -420,7 +420,7 @@ def paged_main(args, wl, baseline, rank, world, dev):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel (paged)", "us_per_launch": dec_avg_ms * 1e3,
-                     "algorithmic_bytes_per_launch": dec_bytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": dec_bytes, "traffic": profiled_traffic(wl.name)},
         "gpu_launches": launches,
         "clocks": clk.summary(w0, w1),
         "e2e": {"value": e_bytes / e_dt / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
