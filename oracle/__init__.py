@@ -84,6 +84,14 @@ def lib() -> ctypes.CDLL:
         L.kvq_or_rope.argtypes = [P, Lg, I, ctypes.c_double, Lg]
         L.kvq_or_seq_attend.argtypes = [ctypes.POINTER(_Seq), P, I, P]
         L.kvq_or_seq_attend.restype = I
+        D_ = ctypes.c_double
+        L.kvq_or_small_float_value.argtypes = [I, I, I, I]
+        L.kvq_or_small_float_value.restype = D_
+        L.kvq_or_small_float_code.argtypes = [D_, I, I, I, D_]
+        L.kvq_or_small_float_code.restype = I
+        L.kvq_or_nvfp4_page_k.argtypes = [P, I, I, P, P, P]
+        L.kvq_or_nvfp4_page_v.argtypes = [P, I, I, P, P, P]
+        L.kvq_or_nvfp4_dequant.argtypes = [P, P, ctypes.c_float, I, I, I, P]
         _lib = L
     return _lib
 
@@ -201,6 +209,47 @@ def rope(K: np.ndarray, base: float = 10000.0, t0: int = 0) -> np.ndarray:
     return out
 
 
+# --------------------------------------------------------------------------- #
+# NVFP4 pages (see kvq_oracle.c for the reading of the format)                 #
+# --------------------------------------------------------------------------- #
+
+def small_float_value(code: int, ebits: int, mbits: int, bias: int) -> float:
+    return lib().kvq_or_small_float_value(int(code), ebits, mbits, bias)
+
+
+def small_float_code(x: float, ebits: int, mbits: int, bias: int, maxv: float) -> int:
+    return lib().kvq_or_small_float_code(float(x), ebits, mbits, bias, float(maxv))
+
+
+def e2m1_code(x: float) -> int:
+    return small_float_code(x, 2, 1, 1, 6.0)
+
+
+def e4m3_code(x: float) -> int:
+    return small_float_code(x, 4, 3, 7, 448.0)
+
+
+def nvfp4_page(x: np.ndarray, values: bool):
+    """One page fp16 [G][D] -> (codes uint8 [G][D/2], scales uint8 ([G][D/16] for keys,
+    [G/16][D] for values), S float32)."""
+    x = np.ascontiguousarray(_u16(x))
+    G, D = x.shape
+    codes = np.zeros((G, D // 2), np.uint8)
+    scales = np.zeros((G // 16, D) if values else (G, D // 16), np.uint8)
+    S = ctypes.c_float(0.0)
+    fn = lib().kvq_or_nvfp4_page_v if values else lib().kvq_or_nvfp4_page_k
+    fn(_p(x), G, D, _p(codes), _p(scales), ctypes.byref(S))
+    return codes, scales, np.float32(S.value)
+
+
+def nvfp4_dequant(codes: np.ndarray, scales: np.ndarray, S: float, values: bool) -> np.ndarray:
+    G, D = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((G, D), np.float64)
+    lib().kvq_or_nvfp4_dequant(_p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
+                               float(S), G, D, int(values), _p(out))
+    return out
+
+
 def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     """fp64 softmax attention. q: [n_heads, D], K, V: [L, D] (any float dtype)."""
     q = np.ascontiguousarray(q, np.float64)
@@ -231,7 +280,9 @@ class OracleCache:
 
     def __init__(self, B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi",
                  max_T=None, v_bits=None, rope_base=0.0):
-        assert mode in ("kivi", "kitty")
+        assert mode in ("kivi", "kitty", "nvfp4")
+        self.nvfp4 = mode == "nvfp4"
+        assert not self.nvfp4 or (bits == 4 and (not v_bits or v_bits == 4)), "NVFP4 codes are 4-bit"
         self.B, self.H_q, self.H_kv, self.D, self.G, self.bits = B, H_q, H_kv, D, G, bits
         self.vbits = bits if not v_bits else v_bits  # value codes may use their own width
         self.rope_base = float(rope_base)  # > 0: keys stored before RoPE, rotated when attended
@@ -255,11 +306,42 @@ class OracleCache:
         self.v_meta = np.zeros(U + (0, D // self.Gv, 2), np.float16)
         self.n_sink = self.T_k = self.n_kres = self.T_v = self.n_vres = 0
         self.n_local = self.local_head = 0
+        if self.nvfp4:  # codes [T][D/2]; key scales [T][D/16], value scales [T/16][D]; S per page
+            self.k_codes = np.zeros(U + (0, D // 2), np.uint8)
+            self.k_scales = np.zeros(U + (0, D // 16), np.uint8)
+            self.k_S = np.zeros(U + (0,), np.float32)
+            self.v_codes = np.zeros(U + (0, D // 2), np.uint8)
+            self.v_scales = np.zeros(U + (0, D), np.uint8)
+            self.v_S = np.zeros(U + (0,), np.float32)
 
     # -- packing helpers ---------------------------------------------------- #
+    def _pack_nvfp4(self, src: np.ndarray, values: bool):
+        B, H, n, D = src.shape
+        G = self.G
+        c = np.zeros((B, H, n, D // 2), np.uint8)
+        sc = np.zeros((B, H, n // 16, D) if values else (B, H, n, D // 16), np.uint8)
+        S = np.zeros((B, H, n // G), np.float32)
+        for b in range(B):
+            for h in range(H):
+                for j in range(n // G):
+                    cc, ss, S[b, h, j] = nvfp4_page(src[b, h, j * G:(j + 1) * G], values)
+                    c[b, h, j * G:(j + 1) * G] = cc
+                    if values:
+                        sc[b, h, j * G // 16:(j + 1) * G // 16] = ss
+                    else:
+                        sc[b, h, j * G:(j + 1) * G] = ss
+        return c, sc, S
+
     def _pack_k(self, src: np.ndarray):
         """Quantize src fp16 [B,H,n*G,D] as n key groups appended at the tail."""
         if src.shape[2] == 0:
+            return
+        if self.nvfp4:
+            c, sc, S = self._pack_nvfp4(src, False)
+            self.k_codes = np.concatenate([self.k_codes, c], 2)
+            self.k_scales = np.concatenate([self.k_scales, sc], 2)
+            self.k_S = np.concatenate([self.k_S, S], 2)
+            self.T_k += src.shape[2]
             return
         if self.kitty:
             lo, hi, bi, mt = quant_k_kitty(src, self.G, self.n_boost)
@@ -274,6 +356,13 @@ class OracleCache:
 
     def _pack_v(self, src: np.ndarray):
         if src.shape[2] == 0:
+            return
+        if self.nvfp4:
+            c, sc, S = self._pack_nvfp4(src, True)
+            self.v_codes = np.concatenate([self.v_codes, c], 2)
+            self.v_scales = np.concatenate([self.v_scales, sc], 2)
+            self.v_S = np.concatenate([self.v_S, S], 2)
+            self.T_v += src.shape[2]
             return
         c, mt = quant_v(src, self.Gv, self.vbits)
         self.v_codes = np.concatenate([self.v_codes, c], 2)
@@ -368,8 +457,23 @@ class OracleCache:
         s.rope_base = self.rope_base
         return s
 
+    def _nvfp4_rows(self, b: int, h: int):
+        G, D = self.G, self.D
+        parts_k = [self.k_sink[b, h, :self.n_sink].astype(np.float64)]
+        parts_v = [self.v_sink[b, h, :self.n_sink].astype(np.float64)]
+        for j in range(self.T_k // G):
+            parts_k.append(nvfp4_dequant(self.k_codes[b, h, j * G:(j + 1) * G],
+                                         self.k_scales[b, h, j * G:(j + 1) * G], self.k_S[b, h, j], False))
+            parts_v.append(nvfp4_dequant(self.v_codes[b, h, j * G:(j + 1) * G],
+                                         self.v_scales[b, h, j * G // 16:(j + 1) * G // 16], self.v_S[b, h, j], True))
+        parts_k.append(self.k_res[b, h, :self.n_kres].astype(np.float64))
+        parts_v.append(self.v_res[b, h, :self.n_vres].astype(np.float64))
+        return np.concatenate(parts_k, 0), np.concatenate(parts_v, 0)
+
     def rows(self, b: int, h: int):
         """Dequantized fp64 keys and values [L, D] of one sequence, logical order."""
+        if self.nvfp4:
+            return self._nvfp4_rows(b, h)
         keep: List = []
         s = self._seq(b, h, keep)
         Kh = np.zeros((self.L, self.D), np.float64)
@@ -384,6 +488,12 @@ class OracleCache:
         if units is None:
             units = [(b, h) for b in range(self.B) for h in range(self.H_kv)]
         for b, h in units:
+            if self.nvfp4:
+                Kh, Vh = self._nvfp4_rows(b, h)
+                if self.rope_base > 0:
+                    Kh = rope(Kh, self.rope_base, 0)
+                out[b, h * g:(h + 1) * g] = attend(q[b, h * g:(h + 1) * g].astype(np.float64), Kh, Vh)
+                continue
             keep: List = []
             s = self._seq(b, h, keep)
             qh = np.ascontiguousarray(_u16(q[b, h * g:(h + 1) * g]))

@@ -454,3 +454,169 @@ void kvq_or_f2h_array(const float *f, uint16_t *h, long n)
     for (long i = 0; i < n; i++)
         h[i] = kvq_or_f2h(f[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 pages (BitDecoding notes, Sec. V-D: Blackwell's native low-precision  */
+/* formats mxfp4 / nvfp4; the pages name the formats only).  Reading taken:    */
+/* elements are e2m1 (1 sign, 2 exponent bits, bias 1, 1 mantissa bit: the    */
+/* magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6); every block of 16 elements along   */
+/* the dimension a product contracts (channels of a key, tokens of a value)   */
+/* has an e4m3 scale (4 exponent bits, bias 7, 3 mantissa bits, largest 448); */
+/* each page (G tokens of one sequence) has an fp32 scale S.  In fp32 with    */
+/* IEEE operations:                                                           */
+/*   S = amax(page) / 2688 (= 6 * 448);                                       */
+/*   s = e4m3( amax(block) / 6 / S ), rounded to nearest even, saturating;    */
+/*   d = s * S;  code = e2m1( x / d ), nearest even, saturating at 6, signed;  */
+/*   an all-zero page has S = 0, and a zero d gives code 0;                   */
+/* dequant x^ = e2m1(code) * s * S.                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Value of a small float code with ebits exponent bits (bias), mbits mantissa bits
+ * and a sign bit above them; exponent field 0 is subnormal. */
+double kvq_or_small_float_value(int code, int ebits, int mbits, int bias)
+{
+    int mag = code & ((1 << (ebits + mbits)) - 1);
+    int sign = (code >> (ebits + mbits)) & 1;
+    int e = mag >> mbits, m = mag & ((1 << mbits) - 1);
+    double v = e == 0 ? ldexp((double)m, 1 - bias - mbits)
+                      : ldexp(1.0 + ldexp((double)m, -mbits), e - bias);
+    return sign ? -v : v;
+}
+
+/* Code of the representable value nearest to x (ties to the even code), with
+ * magnitudes above the largest finite value `maxv` taken as maxv (saturation).
+ * Written from the format: for each exponent field e the values are spaced by
+ * 2^(max(e,1) - bias - mbits), so x is rounded on that grid in its binade. */
+int kvq_or_small_float_code(double x, int ebits, int mbits, int bias, double maxv)
+{
+    int sign = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    if (a >= maxv)
+        a = maxv;
+    /* the binade: largest e with 2^(e - bias) <= a (normal), else subnormal */
+    int emax_field = (1 << ebits) - 1, e = 0;
+    for (int f = emax_field; f >= 1; f--) {
+        if (a >= ldexp(1.0, f - bias)) {
+            e = f;
+            break;
+        }
+    }
+    double q = ldexp(1.0, (e > 0 ? e : 1) - bias - mbits);  /* spacing in this binade */
+    double n = a / q;                                         /* exact: q is a power of 2 */
+    double r = floor(n);
+    double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    /* r counts spacings from 0 (subnormal) or from 2^(e-bias) (normal) */
+    int mag;
+    if (e == 0) {
+        mag = (int)r;  /* may carry into the first normal code: r == 2^mbits */
+    } else {
+        long steps = (long)r - (1L << mbits);  /* mantissa, may carry into the next binade */
+        mag = (e << mbits) + (int)steps;
+    }
+    int magmax = (1 << (ebits + mbits)) - 1;
+    if (mag > magmax)
+        mag = magmax;
+    return (sign << (ebits + mbits)) | mag;
+}
+
+static double fp32_div(double a, double b) { return (double)((float)a / (float)b); }
+
+static int e2m1_code(float x) { return kvq_or_small_float_code((double)x, 2, 1, 1, 6.0); }
+static int e4m3_code(float x) { return kvq_or_small_float_code((double)x, 4, 3, 7, 448.0); }
+static float e4m3_value(int c) { return (float)kvq_or_small_float_value(c, 4, 3, 7); }
+double kvq_or_e2m1_value(int c) { return kvq_or_small_float_value(c, 2, 1, 1); }
+
+/* One NVFP4 block of n elements x[0], x[stride], ...: its scale code and its codes
+ * (code i into codes[i]).  S: the page scale. */
+static void nvfp4_block(const float *x, long stride, int n, float S, uint8_t *scale, uint8_t *codes)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; i++) {
+        float a = fabsf(x[i * stride]);
+        if (a > amax)
+            amax = a;
+    }
+    if (S == 0.0f) {
+        *scale = 0;
+        for (int i = 0; i < n; i++)
+            codes[i] = 0;
+        return;
+    }
+    float sb = (float)fp32_div(fp32_div(amax, 6.0), S);
+    int sc = e4m3_code(sb);
+    *scale = (uint8_t)sc;
+    volatile float d = e4m3_value(sc) * S;   /* fp32 product, rounded once */
+    for (int i = 0; i < n; i++) {
+        if (d == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        volatile float r = x[i * stride] / d;
+        codes[i] = (uint8_t)e2m1_code(r);
+    }
+}
+
+static float page_scale(const uint16_t *x, long n)
+{
+    float amax = 0.0f;
+    for (long i = 0; i < n; i++) {
+        float a = fabsf(kvq_or_h2f(x[i]));
+        if (a > amax)
+            amax = a;
+    }
+    return (float)fp32_div(amax, 2688.0);
+}
+
+/* Keys: page k [G][D] fp16 -> codes [G][D/2] (channel 2i low nibble, 2i+1 high),
+ * scales [G][D/16] (blocks of 16 channels of a token), *S. */
+void kvq_or_nvfp4_page_k(const uint16_t *k, int G, int D, uint8_t *codes, uint8_t *scales, float *S_out)
+{
+    float S = page_scale(k, (long)G * D);
+    float x[16];
+    uint8_t c[16];
+    for (int t = 0; t < G; t++) {
+        for (int b = 0; b < D / 16; b++) {
+            for (int i = 0; i < 16; i++)
+                x[i] = kvq_or_h2f(k[(long)t * D + 16 * b + i]);
+            nvfp4_block(x, 1, 16, S, &scales[(long)t * (D / 16) + b], c);
+            for (int i = 0; i < 8; i++)
+                codes[(long)t * (D / 2) + 8 * b + i] = (uint8_t)(c[2 * i] | (c[2 * i + 1] << 4));
+        }
+    }
+    *S_out = S;
+}
+
+/* Values: page v [G][D] fp16 -> codes [G][D/2] (token-major, as keys), scales
+ * [G/16][D] (blocks of 16 tokens of a channel), *S. */
+void kvq_or_nvfp4_page_v(const uint16_t *v, int G, int D, uint8_t *codes, uint8_t *scales, float *S_out)
+{
+    float S = page_scale(v, (long)G * D);
+    float x[16];
+    uint8_t c[16];
+    memset(codes, 0, (size_t)G * D / 2);
+    for (int tb = 0; tb < G / 16; tb++) {
+        for (int ch = 0; ch < D; ch++) {
+            for (int i = 0; i < 16; i++)
+                x[i] = kvq_or_h2f(v[(long)(16 * tb + i) * D + ch]);
+            nvfp4_block(x, 1, 16, S, &scales[(long)tb * D + ch], c);
+            for (int i = 0; i < 16; i++)
+                codes[(long)(16 * tb + i) * (D / 2) + ch / 2] |= (uint8_t)(c[i] << (4 * (ch & 1)));
+        }
+    }
+    *S_out = S;
+}
+
+/* Dequantized page [G][D] fp64 of either layout (value_blocks: blocks run along tokens). */
+void kvq_or_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, float S, int G, int D, int value_blocks,
+                          double *out)
+{
+    for (int t = 0; t < G; t++) {
+        for (int ch = 0; ch < D; ch++) {
+            int c = (codes[(long)t * (D / 2) + ch / 2] >> (4 * (ch & 1))) & 15;
+            int sc = value_blocks ? scales[(long)(t / 16) * D + ch] : scales[(long)t * (D / 16) + ch / 16];
+            out[(long)t * D + ch] = kvq_or_e2m1_value(c) * (double)e4m3_value(sc) * (double)S;
+        }
+    }
+}
