@@ -60,6 +60,10 @@ def decode_bytes(wl, lengths) -> int:
     Gv = min(G, D)
     kb = 2 if wl.mode == "kitty" else wl.bits
     T_k, T_v = lengths["T_k"], lengths["T_v"]
+    if wl.mode == "nvfp4":   # 4-bit codes, one e4m3 scale per 16 elements, 16-byte page records
+        b = U * (T_k + T_v) * D // 2 + U * (T_k + T_v) * D // 16 + U * (T_k // G + T_v // G) * 16
+        n16 = lengths["n_sink"] * 2 + lengths["n_kres"] + lengths["n_vres"]
+        return b + U * n16 * D * 2 + 2 * wl.B * wl.H_q * D * 2
     b = U * T_k * D * kb // 8 + U * (T_k // G) * D * 4              # key codes + (scale, min)
     if wl.mode == "kitty" and wl.n_boost:
         b += U * T_k * wl.n_boost * 2 // 8 + U * (T_k // G) * D      # high plane + boost index
@@ -181,7 +185,7 @@ def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
     sub = wl.replace(B=1, H_kv=n_units, H_q=n_units * wl.g)
     K, V = kvq_synth.prefill_kv(wl.replace(B=1, H_kv=min(wl.H_kv, n_units)), L0)
     ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S, R=sub.R,
-                             n_boost=sub.n_boost, mode=sub.mode, v_bits=sub.v_bits)
+                             n_boost=sub.n_boost, mode=sub.mode, v_bits=sub.v_bits, rope_base=sub.rope_base)
     ora.prefill(K, V)
     q = kvq_synth.queries(sub, 1)[0]
     lengths = dict(n_sink=ora.n_sink, T_k=ora.T_k, n_kres=ora.n_kres, T_v=ora.T_v,

@@ -15,7 +15,7 @@ from typing import Optional, Tuple
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
-KVQ_MODE_KIVI, KVQ_MODE_KITTY = 0, 1
+KVQ_MODE_KIVI, KVQ_MODE_KITTY, KVQ_MODE_NVFP4 = 0, 1, 2
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
           -3: "capacity exceeded", -4: "workspace missing or too small", -5: "CUDA error",
           -6: "device-side error reported"}
@@ -110,7 +110,7 @@ def _check(code: int, what: str):
 def make_config(B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi", max_T=0,
                 v_bits=0, rope_base=0.0) -> Config:
     """rope_base > 0: keys are stored before RoPE and rotated in decode attention."""
-    m = {"kivi": KVQ_MODE_KIVI, "kitty": KVQ_MODE_KITTY}[mode]
+    m = {"kivi": KVQ_MODE_KIVI, "kitty": KVQ_MODE_KITTY, "nvfp4": KVQ_MODE_NVFP4}[mode]
     return Config(B, H_q, H_kv, D, G, bits, S, G if R is None else R, n_boost, m, v_bits or 0, max_T,
                   1 if rope_base else 0, float(rope_base or 0.0))
 
@@ -231,6 +231,13 @@ class KVQCache:
         cfg = self.cfg
         U, D, T, G = cfg.B * cfg.H_kv, cfg.D, cfg.max_T, cfg.G
         kitty = cfg.mode == KVQ_MODE_KITTY
+        if cfg.mode == KVQ_MODE_NVFP4:  # codes [B][H][T][D/2]; page records of 16 + G*D/16 bytes
+            b = self.buf[name]
+            ms = 16 + G * D // 16
+            if name in ("k_codes", "v_codes"):
+                return b[: U * T * D // 2].view(cfg.B, cfg.H_kv, T, D // 2)
+            if name in ("k_meta", "v_meta"):
+                return b[: U * (T // G) * ms].view(cfg.B, cfg.H_kv, T // G, ms)
         kfpi = 16 if kitty else 32 // cfg.bits
         vfpi = 32 // (cfg.v_bits or cfg.bits)
         Gv = min(G, D)

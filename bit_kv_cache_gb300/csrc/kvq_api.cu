@@ -101,6 +101,43 @@ QuantVParams qv_params(const kvq_config *c, kvq_cache *k) {
     return p;
 }
 
+// Key / value page quantization of either format: the KIVI / Kitty quantizers, or the
+// NVFP4 page kernel with the same source rows and destination pages.
+cudaError_t launch_keys(const kvq_config *c, kvq_cache *k, const QuantKParams &p, cudaStream_t st) {
+    if (!nvfp4(c)) return launch_quant_k(p, c->bits, kitty(c), st);
+    QuantNvParams q;
+    q.src = p.src;
+    q.src_ustride = p.src_ustride;
+    q.src_t0 = p.src_t0;
+    q.n_pages = p.n_pages;
+    q.pg0 = p.pg0;
+    q.max_T = c->max_T;
+    q.U = (int)units(c);
+    q.D = c->D;
+    q.G = c->G;
+    q.ms = (int)nvfp4_page_bytes(c);
+    q.codes = reinterpret_cast<uint8_t *>(k->k_codes);
+    q.meta = reinterpret_cast<uint8_t *>(k->k_meta);
+    return launch_nvfp4(q, false, st);
+}
+cudaError_t launch_values(const kvq_config *c, kvq_cache *k, const QuantVParams &p, cudaStream_t st) {
+    if (!nvfp4(c)) return launch_quant_v(p, vbits_of(c), st);
+    QuantNvParams q;
+    q.src = p.src;
+    q.src_ustride = p.src_ustride;
+    q.src_t0 = p.src_t0;
+    q.n_pages = p.n_tok / c->G;
+    q.pg0 = p.tok0 / c->G;
+    q.max_T = c->max_T;
+    q.U = (int)units(c);
+    q.D = c->D;
+    q.G = c->G;
+    q.ms = (int)nvfp4_page_bytes(c);
+    q.codes = reinterpret_cast<uint8_t *>(k->v_codes);
+    q.meta = reinterpret_cast<uint8_t *>(k->v_meta);
+    return launch_nvfp4(q, true, st);
+}
+
 cudaError_t copy_rows(const kvq_config *c, const uint16_t *src, int64_t src_rows, int64_t src_r0, uint16_t *dst,
                       int64_t dst_rows, int64_t dst_r0, int64_t n, cudaStream_t st) {
     CopyRowsParams p;
@@ -138,7 +175,12 @@ int kvq_config_check(const kvq_config *c) {
     if (c->B <= 0 || c->H_q <= 0 || c->H_kv <= 0 || c->D <= 0 || c->G <= 0 || c->max_T < 0 || c->S < 0 ||
         c->R < 0 || c->n_boost < 0)
         return KVQ_ERR_INVALID_ARG;
-    if (c->mode != KVQ_MODE_KIVI && c->mode != KVQ_MODE_KITTY) return KVQ_ERR_INVALID_ARG;
+    if (c->mode != KVQ_MODE_KIVI && c->mode != KVQ_MODE_KITTY && c->mode != KVQ_MODE_NVFP4)
+        return KVQ_ERR_INVALID_ARG;
+    if (nvfp4(c)) {
+        if (c->bits != 4 || (c->v_bits != 0 && c->v_bits != 4)) return KVQ_ERR_UNSUPPORTED;
+        if (c->G % 16 || c->D % 16 || c->G > 256) return KVQ_ERR_UNSUPPORTED;
+    }
     if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KVQ_ERR_UNSUPPORTED;
     if (c->v_bits != 0 && c->v_bits != 2 && c->v_bits != 4 && c->v_bits != 8) return KVQ_ERR_UNSUPPORTED;
     if (kitty(c) && c->bits != 2) return KVQ_ERR_UNSUPPORTED;
@@ -149,7 +191,7 @@ int kvq_config_check(const kvq_config *c) {
     const int gv = gv_of(c);
     if (c->D % gv) return KVQ_ERR_INVALID_ARG;
     if (gv != 32 && gv != 64 && gv != 128 && gv != 256) return KVQ_ERR_UNSUPPORTED;
-    if (!key_slices_ok(c)) return KVQ_ERR_UNSUPPORTED;
+    if (!nvfp4(c) && !key_slices_ok(c)) return KVQ_ERR_UNSUPPORTED;
     if (c->max_T % c->G) return KVQ_ERR_INVALID_ARG;
     if (c->rope != 0 && c->rope != 1) return KVQ_ERR_INVALID_ARG;
     if (!(c->rope_base >= 0.0f) || c->rope_base > 3.0e38f) return KVQ_ERR_INVALID_ARG;
@@ -167,6 +209,15 @@ int kvq_config_check(const kvq_config *c) {
 size_t kvq_buffer_bytes(const kvq_config *c, int which) {
     if (kvq_config_check(c) != KVQ_OK) return 0;
     const size_t U = (size_t)units(c), D = c->D, T = (size_t)c->max_T, G = c->G;
+    if (nvfp4(c)) {
+        switch (which) {
+            case 0: case 4: return U * T * D / 2;
+            case 3: case 5: return U * (T / G) * (size_t)nvfp4_page_bytes(c);
+            case 6: return U * (size_t)c->S * D * 2;
+            case 7: case 8: return U * (size_t)c->R * D * 2;
+        }
+        return 0;
+    }
     switch (which) {
         case 0: return U * (T / kfpi(c)) * D * 4;
         case 1: return kitty(c) && c->n_boost ? U * (T / 16) * c->n_boost * 4 : 0;
@@ -203,7 +254,7 @@ int kvq_quant_pack_k(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
         p.src_t0 = ns;
         p.n_pages = tk / c->G;
         p.pg0 = 0;
-        ce = launch_quant_k(p, c->bits, kitty(c), st);
+        ce = launch_keys(c, k, p, st);
     }
     if (ce == cudaSuccess && kres > 0) ce = copy_rows(c, src, L0, ns + tk, k->k_res, cap_k(c), 0, kres, st);
     if (ce != cudaSuccess) return KVQ_ERR_CUDA;
@@ -240,7 +291,7 @@ int kvq_quant_pack_v(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
         p.src_t0 = ns;
         p.n_tok = tv;
         p.tok0 = 0;
-        ce = launch_quant_v(p, vbits_of(c), st);
+        ce = launch_values(c, k, p, st);
     }
     if (ce == cudaSuccess && vres > 0) ce = copy_rows(c, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres, st);
     if (ce == cudaSuccess && nl > 0) ce = copy_rows(c, src, L0, ns + older, k->v_local, c->R, 0, nl, st);
@@ -323,7 +374,7 @@ int kvq_flush_group(const kvq_config *c, kvq_cache *k, int *flushed_k, int *flus
         p.src_t0 = 0;
         p.n_pages = cap_k(c) / c->G;
         p.pg0 = k->T_k / c->G;
-        if (launch_quant_k(p, c->bits, kitty(c), st) != cudaSuccess) return KVQ_ERR_CUDA;
+        if (launch_keys(c, k, p, st) != cudaSuccess) return KVQ_ERR_CUDA;
         k->T_k += cap_k(c);
         k->n_kres = 0;
     }
@@ -334,7 +385,7 @@ int kvq_flush_group(const kvq_config *c, kvq_cache *k, int *flushed_k, int *flus
         p.src_t0 = 0;
         p.n_tok = cap_v(c);
         p.tok0 = k->T_v;
-        if (launch_quant_v(p, vbits_of(c), st) != cudaSuccess) return KVQ_ERR_CUDA;
+        if (launch_values(c, k, p, st) != cudaSuccess) return KVQ_ERR_CUDA;
         k->T_v += cap_v(c);
         k->n_vres = 0;
     }
@@ -501,6 +552,8 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.max_T = c->max_T;
     p.rope = c->rope;
     p.rope_base = c->rope_base > 0.0f ? c->rope_base : 10000.0f;
+    p.nvfp4 = nvfp4(c) ? 1 : 0;
+    p.nv_kms = p.nv_vms = (int)nvfp4_page_bytes(c);
     p.n_sink = k->n_sink;
     p.T_k = k->T_k;
     p.n_kres = k->n_kres;

@@ -81,6 +81,21 @@ __device__ __forceinline__ void load_k8(const DecodeParams &p, int u, int64_t tl
         return;
     }
     int64_t tk = tl - p.n_sink;
+    if (tk < p.T_k && p.nvfp4) {  // NVFP4: 8 codes of token tk, e4m3 scale of their block, page scale
+        const uint8_t *codes = reinterpret_cast<const uint8_t *>(p.k_codes);
+        const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.k_meta) +
+                             ((size_t)u * (p.max_T / p.G) + tk / p.G) * p.nv_kms;
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + ((size_t)u * p.max_T + tk) * (D / 2) + d / 2);
+        const float S = *reinterpret_cast<const float *>(rec);
+        const float s = unpack_half2(e4m3x2_to_f16x2(rec[16 + (tk % p.G) * (D / 16) + d / 16])).x * S;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 f = unpack_half2(e2m1x2_to_f16x2((w >> (8 * i)) & 0xFFu));
+            kv[2 * i] = f.x * s;
+            kv[2 * i + 1] = f.y * s;
+        }
+        return;
+    }
     if (tk < p.T_k) {
         const int kb = p.kitty ? 2 : p.bits, fpi = 32 / kb;
         const int64_t page = tk / p.G;
@@ -122,6 +137,20 @@ __device__ __forceinline__ void load_v(const DecodeParams &p, int u, int64_t tl,
         row = p.v_sink + ((size_t)u * p.S_cap + tl) * D;
     } else {
         int64_t tv = tl - p.n_sink;
+        if (tv < p.T_v && p.nvfp4) {  // NVFP4 values: codes of channels d.., scales of their blocks
+            const uint8_t *codes = reinterpret_cast<const uint8_t *>(p.v_codes) + ((size_t)u * p.max_T + tv) * (D / 2);
+            const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.v_meta) +
+                                 ((size_t)u * (p.max_T / p.G) + tv / p.G) * p.nv_vms;
+            const float S = *reinterpret_cast<const float *>(rec);
+            const uint8_t *sc = rec + 16 + ((tv % p.G) / 16) * D;
+#pragma unroll
+            for (int i = 0; i < DPL; i += 2) {
+                const float2 f = unpack_half2(e2m1x2_to_f16x2(codes[(d + i) / 2]));
+                vv[i] = f.x * unpack_half2(e4m3x2_to_f16x2(sc[d + i])).x * S;
+                vv[i + 1] = f.y * unpack_half2(e4m3x2_to_f16x2(sc[d + i + 1])).x * S;
+            }
+            return;
+        }
         if (tv < p.T_v) {
             const int fpi = 32 / p.vbits;
             const int64_t page = tv / p.G, tin = tv % p.G;

@@ -116,6 +116,30 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
+// Blackwell FP4 / FP8 conversions: two e2m1 codes of a byte -> f16x2 (low nibble ->
+// low half); two e4m3 codes of a 16-bit word -> f16x2; float pairs -> codes, rounded
+// to nearest even with saturation (the second argument becomes the low code).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{.reg .b8 c;\n cvt.u8.u32 c, %1;\n cvt.rn.f16x2.e2m1x2 %0, c;}" : "=r"(r) : "r"(byte));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t word) {
+    uint32_t r;
+    asm("{.reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;}" : "=r"(r) : "r"(word));
+    return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float hi, float lo) {
+    uint32_t r;
+    asm("{.reg .b8 c;\n cvt.rn.satfinite.e2m1x2.f32 c, %1, %2;\n cvt.u32.u8 %0, c;}" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+    return r & 0xFFu;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);

@@ -21,6 +21,8 @@ inline int kfpi(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY ? 16 : 3
 inline int vfpi(const kvq_config *c) { return 32 / vbits_of(c); }
 inline int gv_of(const kvq_config *c) { return std::min(c->G, c->D); }
 inline bool kitty(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY; }
+inline bool nvfp4(const kvq_config *c) { return c->mode == KVQ_MODE_NVFP4; }
+inline int64_t nvfp4_page_bytes(const kvq_config *c) { return 16 + (int64_t)c->G * c->D / 16; }
 inline int64_t cap_k(const kvq_config *c) { return kitty(c) ? c->G : c->R; }
 inline int64_t cap_v(const kvq_config *c) { return kitty(c) ? c->G : c->R; }
 inline int64_t units(const kvq_config *c) { return (int64_t)c->B * c->H_kv; }
@@ -53,6 +55,7 @@ inline int num_sms() {
 
 inline bool fast_supported(const kvq_config *c) {
     const int tok = 256 / c->bits;  // a tile holds 8 key word rows
+    if (nvfp4(c)) return false;     // NVFP4 pages decode on the CUDA-core path
     // tiles: any key and value widths of 2, 4, 8 bits (Kitty: 2-bit planes, 2-bit values)
     if (kitty(c) && vbits_of(c) != 2) return false;
     if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4

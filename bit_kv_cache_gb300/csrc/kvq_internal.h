@@ -52,6 +52,18 @@ struct QuantVParams {
     PageMap pm;
 };
 
+// NVFP4 pages: one CTA per page of G tokens (fp16 [G][D] at src rows src_t0 + j G of
+// unit u) -> codes uint8 [U][max_T][D/2] (token-major) and a page record of `ms`
+// bytes at meta + (u * max_T/G + pg0 + j) * ms: fp32 scale S, 12 bytes of padding,
+// then e4m3 block scales ([G][D/16] for keys, [G/16][D] for values).
+struct QuantNvParams {
+    const uint16_t *src;
+    int64_t src_ustride, src_t0;
+    int64_t n_pages, pg0, max_T;
+    int U, D, G, ms;
+    uint8_t *codes, *meta;
+};
+
 struct CopyRowsParams {
     const uint16_t *src;
     uint16_t *dst;
@@ -99,6 +111,7 @@ struct DecodeParams {
     int64_t max_T;
     int rope;              // keys stored before RoPE: rotate key t by t * theta_j
     float rope_base;
+    int nvfp4, nv_kms, nv_vms;  // NVFP4 pages (CUDA-core path): page record bytes of keys, values
     // lengths
     int64_t n_sink, T_k, n_kres, T_v, n_vres, n_local, local_head, L;
     // buffers
@@ -144,6 +157,7 @@ constexpr int kMaxWarps = 8;
 
 cudaError_t launch_quant_k(const QuantKParams &p, int bits, bool kitty, cudaStream_t st);
 cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
+cudaError_t launch_nvfp4(const QuantNvParams &p, bool values, cudaStream_t st);
 cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st);

@@ -452,6 +452,114 @@ __global__ void append_kernel(AppendParams p) {
     *vd = *vn;
 }
 
+// ------------------------------------------------------------------------------
+// NVFP4 pages (BitDecoding notes, Sec. V-D: Blackwell's native mxfp4 / nvfp4
+// formats).  One CTA per page of G tokens: the fp16 page is staged in shared memory,
+// its amax gives the page scale S = amax / 2688 (6 * 448); every block of 16 elements
+// along the contracted dimension (a key's channels, a value's tokens) gets the e4m3
+// scale of (amax_block / 6) / S and its elements the e2m1 codes of x / (s * S), both
+// by the hardware conversions (nearest even, saturating); IEEE divisions throughout.
+// Codes leave token-major ([token][D/2], channel 2i in the low nibble).
+// ------------------------------------------------------------------------------
+template <bool VALUES>
+__global__ void __launch_bounds__(256) nvfp4_page_kernel(QuantNvParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int G = p.G, D = p.D, tid = threadIdx.x;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);             // [G][D] fp16
+    uint8_t *cs = smem + (size_t)G * D * 2;                        // [G][D/2] codes
+    uint8_t *ss = cs + (size_t)G * D / 2;                          // block scales
+    __shared__ float s_red[8];
+    const int u = blockIdx.y;
+    const int64_t pg = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.src + (size_t)u * p.src_ustride +
+                                                       (size_t)(p.src_t0 + pg * G) * D);
+    const int n16 = G * D / 8;  // uint4 chunks of the page
+    float amax = 0.f;
+    for (int i = tid; i < n16; i += 256) {
+        const uint4 v = __ldg(src + i);
+        reinterpret_cast<uint4 *>(xs)[i] = v;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const float2 f = unpack_half2(w[k]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((tid & 31) == 0) s_red[tid >> 5] = amax;
+    __syncthreads();
+    float pmax = s_red[0];
+#pragma unroll
+    for (int w = 1; w < 8; w++) pmax = fmaxf(pmax, s_red[w]);
+    const float S = __fdiv_rn(pmax, 2688.0f);
+    auto xval = [&](int t, int c) { return __half2float(__ushort_as_half(xs[t * D + c])); };
+    // one 16-element block: its scale code and the divisor d = s * S (0: all codes 0)
+    auto block_scale = [&](float bmax, uint32_t &sc) {
+        if (S == 0.0f) {
+            sc = 0;
+            return 0.0f;
+        }
+        sc = f32_to_e4m3(__fdiv_rn(__fdiv_rn(bmax, 6.0f), S));
+        const float sd = unpack_half2(e4m3x2_to_f16x2(sc)).x;
+        return __fmul_rn(sd, S);
+    };
+    if (!VALUES) {
+        // task = (token t, channel block b): 16 channels, 8 code bytes, 1 scale
+        for (int i = tid; i < G * (D / 16); i += 256) {
+            const int t = i / (D / 16), b = i - t * (D / 16);
+            float bmax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; k++) bmax = fmaxf(bmax, fabsf(xval(t, 16 * b + k)));
+            uint32_t sc;
+            const float d = block_scale(bmax, sc);
+            uint32_t lo = 0, hi = 0;
+            if (d != 0.0f) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(xval(t, 16 * b + 2 * k + 1), d),
+                                                          __fdiv_rn(xval(t, 16 * b + 2 * k), d));
+                    if (k < 4) lo |= byte << (8 * k);
+                    else hi |= byte << (8 * (k - 4));
+                }
+            }
+            *reinterpret_cast<uint2 *>(cs + (size_t)t * (D / 2) + 8 * b) = make_uint2(lo, hi);
+            ss[t * (D / 16) + b] = (uint8_t)sc;
+        }
+    } else {
+        // task = (token block tb, channel pair j): 16 tokens of channels 2j, 2j+1
+        for (int i = tid; i < (G / 16) * (D / 2); i += 256) {
+            const int tb = i / (D / 2), j = i - tb * (D / 2);
+            float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; k++) {
+                m0 = fmaxf(m0, fabsf(xval(16 * tb + k, 2 * j)));
+                m1 = fmaxf(m1, fabsf(xval(16 * tb + k, 2 * j + 1)));
+            }
+            uint32_t sc0, sc1;
+            const float d0 = block_scale(m0, sc0), d1 = block_scale(m1, sc1);
+#pragma unroll
+            for (int k = 0; k < 16; k++) {
+                const int t = 16 * tb + k;
+                const uint32_t c0 = d0 != 0.0f ? f32x2_to_e2m1x2(0.0f, __fdiv_rn(xval(t, 2 * j), d0)) & 15u : 0u;
+                const uint32_t c1 = d1 != 0.0f ? f32x2_to_e2m1x2(__fdiv_rn(xval(t, 2 * j + 1), d1), 0.0f) >> 4 : 0u;
+                cs[(size_t)t * (D / 2) + j] = (uint8_t)(c0 | (c1 << 4));
+            }
+            ss[tb * D + 2 * j] = (uint8_t)sc0;
+            ss[tb * D + 2 * j + 1] = (uint8_t)sc1;
+        }
+    }
+    __syncthreads();
+    const int64_t page = p.pg0 + pg;
+    uint4 *dc = reinterpret_cast<uint4 *>(p.codes + ((size_t)u * p.max_T + (size_t)page * G) * (D / 2));
+    for (int i = tid; i < G * D / 32; i += 256) dc[i] = reinterpret_cast<const uint4 *>(cs)[i];
+    uint8_t *rec = p.meta + ((size_t)u * (p.max_T / G) + page) * p.ms;
+    const int nsc = G * D / 16;
+    for (int i = tid; i < nsc / 16; i += 256)
+        reinterpret_cast<uint4 *>(rec + 16)[i] = reinterpret_cast<const uint4 *>(ss)[i];
+    if (tid == 0) *reinterpret_cast<float4 *>(rec) = make_float4(S, 0.f, 0.f, 0.f);
+}
+
 // Paged append: CTA b moves the new key and value rows of batch slot b's H_kv heads
 // into its sink (while not full) or residual, at the slot's device lengths, and
 // advances them.  Only this CTA reads or writes lens[b].
@@ -573,6 +681,19 @@ cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st) {
     int blocks = (int)((total + 255) / 256);
     if (blocks > 4096) blocks = 4096;
     copy_rows_kernel<<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4(const QuantNvParams &p, bool values, cudaStream_t st) {
+    if (p.n_pages <= 0) return cudaSuccess;
+    const size_t smem = (size_t)p.G * p.D * 2 + (size_t)p.G * p.D / 2 + (size_t)p.G * p.D / 16;
+    dim3 grid((unsigned)p.n_pages, (unsigned)p.U);
+    auto k = values ? nvfp4_page_kernel<true> : nvfp4_page_kernel<false>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    k<<<grid, 256, smem, st>>>(p);
     return cudaGetLastError();
 }
 

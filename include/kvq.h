@@ -52,7 +52,7 @@ typedef enum {
     KVQ_ERR_DEVICE = -6        /* a kernel reported an error in the status word   */
 } kvq_status;
 
-enum { KVQ_MODE_KIVI = 0, KVQ_MODE_KITTY = 1 };
+enum { KVQ_MODE_KIVI = 0, KVQ_MODE_KITTY = 1, KVQ_MODE_NVFP4 = 2 };
 
 /* Device status bits (see kvq_read_status). */
 enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
@@ -73,7 +73,7 @@ enum { KVQ_DEV_TIMEOUT = 1, KVQ_DEV_BAD_STATE = 2 };
  *                     groups once full.  Kitty: the value local window.
  *   n_boost         : Kitty: key channels per page kept at INT4 (0..min(D,254)).
  *                     Must be 0 in KIVI mode.
- *   mode            : KVQ_MODE_KIVI or KVQ_MODE_KITTY
+ *   mode            : KVQ_MODE_KIVI, KVQ_MODE_KITTY or KVQ_MODE_NVFP4 (below)
  *   max_T           : packed-token capacity per sequence, a multiple of G
  *   rope            : 0: keys are attended as stored.  1: keys are stored before
  *                     the rotary position embedding and decode attention rotates
@@ -113,6 +113,19 @@ typedef struct {
  *   v_local  fp16  [U][R][D]             Kitty local window (ring, oldest at
  *                                        local_head); NULL in KIVI mode.
  *   status   int32 device word that kernels OR error bits into (may be NULL).
+ * KVQ_MODE_NVFP4 (BitDecoding notes, Sec. V-D: Blackwell's native mxfp4 / nvfp4
+ * formats; bits = 4, v_bits 0 or 4, G and D multiples of 16, G <= 256, R as KIVI):
+ * pages hold e2m1 codes with an e4m3 scale per block of 16 elements along the
+ * dimension each product contracts and an fp32 scale per page,
+ *   S = amax(page) / 2688,  s = e4m3((amax(block) / 6) / S),  code = e2m1(x / (s S)),
+ * rounded to nearest even with saturation, in fp32 IEEE arithmetic (S = 0 for an
+ * all-zero page; a zero s S gives code 0).  Buffers in this mode:
+ *   k_codes, v_codes  uint8 [U][max_T][D/2]  token-major; channel 2i in the low nibble
+ *   k_meta  bytes [U][max_T/G][16 + G*D/16]  per page: fp32 S, 12 bytes padding, e4m3
+ *                                            key scales [G][D/16] (16 channels of a token)
+ *   v_meta  bytes [U][max_T/G][16 + G*D/16]  the same with value scales [G/16][D]
+ *                                            (16 tokens of a channel)
+ *   k_hi, k_bidx, v_local unused.  Decode attention runs on the CUDA-core path.
  * Lengths: n_sink sink tokens, T_k / T_v packed key / value tokens, n_kres keys in
  * k_res, n_vres values in v_res, n_local values in v_local.  A fresh cache has all
  * lengths 0.  Logical token order: keys [sink | packed | k_res], values

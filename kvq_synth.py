@@ -110,6 +110,9 @@ WORKLOADS["llama3_8b_gqa_paged"] = Workload("llama3_8b_gqa_paged", bits=2, seed=
 # Llama-3's RoPE base.
 WORKLOADS["llama3_8b_gqa_rope"] = Workload("llama3_8b_gqa_rope", bits=2, seed=11, rope_base=500000.0, **_GQA)
 
+# NVFP4 pages (BitDecoding notes, Sec. V-D) on the Llama-3-8B GQA layer.
+WORKLOADS["llama3_8b_gqa_nvfp4"] = Workload("llama3_8b_gqa_nvfp4", bits=4, seed=12, mode="nvfp4", **_GQA)
+
 
 def slot_lengths(wl: Workload) -> np.ndarray:
     """Seeded per-slot prefill lengths of a paged workload: T * (1 + ragged * u),

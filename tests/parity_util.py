@@ -43,6 +43,25 @@ def _u16(a):
     return np.ascontiguousarray(a).view(np.uint16)
 
 
+def _assert_nvfp4_state(gpu, ora, pick):
+    cfg = gpu.cfg
+    T, G, D = ora.T_k, cfg.G, cfg.D
+    assert ora.T_v == T
+    for side in ("k", "v"):
+        codes = _np(gpu.view(side + "_codes")[:, :, :T])
+        assert np.array_equal(pick(codes), pick(getattr(ora, side + "_codes"))), side + " codes differ"
+        rec = _np(gpu.view(side + "_meta")[:, :, : T // G])                     # [B,H,P,16 + G*D/16]
+        S = np.ascontiguousarray(rec[..., :4]).view(np.float32)[..., 0]
+        assert np.array_equal(pick(S).view(np.uint32), pick(getattr(ora, side + "_S")).view(np.uint32)), \
+            side + " page scales differ"
+        sc = rec[..., 16:]
+        if side == "k":
+            sc = sc.reshape(cfg.B, cfg.H_kv, T, D // 16)
+        else:
+            sc = sc.reshape(cfg.B, cfg.H_kv, T // 16, D)
+        assert np.array_equal(pick(sc), pick(getattr(ora, side + "_scales"))), side + " block scales differ"
+
+
 def assert_state_equal(gpu, ora, units=None):
     """Bit-exact comparison of every cache buffer (optionally for some (b, h) only)."""
     assert_lengths(gpu, ora)
@@ -57,6 +76,14 @@ def assert_state_equal(gpu, ora, units=None):
         return np.stack([a[b, h] for b, h in units])
 
     T_k, T_v, G = ora.T_k, ora.T_v, cfg.G
+    if getattr(ora, "nvfp4", False):
+        _assert_nvfp4_state(gpu, ora, pick)
+        for name, n in (("k_res", ora.n_kres), ("v_res", ora.n_vres), ("k_sink", ora.n_sink),
+                        ("v_sink", ora.n_sink)):
+            if n:
+                assert np.array_equal(pick(_u16(_np(gpu.view(name)[:, :, :n]))),
+                                      pick(_u16(getattr(ora, name)[:, :, :n]))), name + " differs"
+        return
     kc = _np(gpu.view("k_codes")[:, :, : T_k // kfpi])
     assert np.array_equal(pick(kc), pick(ora.k_codes)), "key codes differ"
     km = _u16(_np(gpu.view("k_meta")[:, :, : T_k // G]))

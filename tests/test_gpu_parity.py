@@ -56,6 +56,12 @@ SMALL = {
                   512 + 70, 3),
     "rope_mha": (WORKLOADS["llama7b_mha"].replace(B=2, H_q=8, H_kv=8, T=512, rope_base=10000.0), 512 + 77, 3),
     "rope_tiny": (WORKLOADS["tiny_kivi"].replace(rope_base=10000.0), 256 + 31, 3),
+    # NVFP4 pages (e2m1 codes, e4m3 block scales, fp32 page scale), CUDA-core decode
+    "nvfp4": (WORKLOADS["llama3_8b_gqa_nvfp4"].replace(B=2, H_q=16, H_kv=4, T=256), 256 + 70, 3),
+    "nvfp4_sink_g32": (WORKLOADS["llama3_8b_gqa_nvfp4"].replace(B=1, H_q=8, H_kv=2, T=128, G=32, R=64, S=4),
+                       4 + 128 + 40, 3),
+    "nvfp4_rope": (WORKLOADS["llama3_8b_gqa_nvfp4"].replace(B=1, H_q=8, H_kv=2, T=256, rope_base=10000.0),
+                   256 + 50, 2),
 }
 
 
@@ -74,7 +80,7 @@ def test_prefill_state_and_attention(name):
     assert gpu.read_status() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi", "rope_k2v2"])
+@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi", "rope_k2v2", "nvfp4_sink_g32"])
 def test_decode_loop_crosses_flushes(name):
     """Enough steps that every buffer fills and is flushed at least once."""
     wl, L0, _ = SMALL[name]
@@ -216,4 +222,18 @@ def test_full_size_pre_rope_sampled(wl):
     U = [(b, h) for b in range(wl.B) for h in range(wl.H_kv)]
     units = [U[i] for i in sorted(rng.choice(len(U), size=min(3, len(U)), replace=False))]
     run_steps(gpu, ora, wl, 2, DEV, units=units)
+    assert gpu.read_status() == 0
+
+
+def test_full_size_nvfp4_sampled():
+    """NVFP4 pages at the Llama-3-8B GQA shape (32K tokens): every code, block scale and
+    page scale bit-exact; attention of sampled sequences."""
+    wl = WORKLOADS["llama3_8b_gqa_nvfp4"]
+    L0 = wl.T + 64
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    gpu, ora = make_pair(wl, max_T=wl.T + 2 * wl.G + wl.R, device=DEV)
+    prefill_both(gpu, ora, K, V, DEV)
+    del K, V
+    assert_state_equal(gpu, ora)
+    run_steps(gpu, ora, wl, 2, DEV, units=[(0, 1), (3, 6)])
     assert gpu.read_status() == 0
