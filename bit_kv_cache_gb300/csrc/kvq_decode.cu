@@ -17,6 +17,7 @@ size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bo
 
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st) {
     if (p.rope) return launch_decode_rope(p, fast, st);
+    if (p.nvfp4 && fast) return launch_decode_nvfp4(p, st);
     if (fast) {  // p.wpc units of one warp, or of a warp pair
         if (p.kitty) {
             if (p.wpc == 8) return launch_one<2, 2, true, true, false, 4, 8>(p, st);

@@ -85,7 +85,10 @@ __device__ __forceinline__ void load_k8(const DecodeParams &p, int u, int64_t tl
         const uint8_t *codes = reinterpret_cast<const uint8_t *>(p.k_codes);
         const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.k_meta) +
                              ((size_t)u * (p.max_T / p.G) + tk / p.G) * p.nv_kms;
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + ((size_t)u * p.max_T + tk) * (D / 2) + d / 2);
+        // key page [D/32][G][16]: channels d .. d+7 of token tk are 4 bytes of its group row
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(
+            codes + ((size_t)u * (p.max_T / p.G) + tk / p.G) * ((size_t)p.G * D / 2) +
+            ((size_t)(d / 32) * p.G + tk % p.G) * 16 + (d % 32) / 2);
         const float S = *reinterpret_cast<const float *>(rec);
         const float s = unpack_half2(e4m3x2_to_f16x2(rec[16 + (tk % p.G) * (D / 16) + d / 16])).x * S;
 #pragma unroll
@@ -138,16 +141,19 @@ __device__ __forceinline__ void load_v(const DecodeParams &p, int u, int64_t tl,
     } else {
         int64_t tv = tl - p.n_sink;
         if (tv < p.T_v && p.nvfp4) {  // NVFP4 values: codes of channels d.., scales of their blocks
-            const uint8_t *codes = reinterpret_cast<const uint8_t *>(p.v_codes) + ((size_t)u * p.max_T + tv) * (D / 2);
+            // value page [G/32][D][16]: token t of channel c is nibble t & 1 of byte (t % 32) / 2
+            const int64_t t = tv % p.G;
+            const uint8_t *codes = reinterpret_cast<const uint8_t *>(p.v_codes) +
+                                   ((size_t)u * (p.max_T / p.G) + tv / p.G) * ((size_t)p.G * D / 2) +
+                                   (size_t)(t / 32) * D * 16 + (t % 32) / 2;
             const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.v_meta) +
                                  ((size_t)u * (p.max_T / p.G) + tv / p.G) * p.nv_vms;
             const float S = *reinterpret_cast<const float *>(rec);
             const uint8_t *sc = rec + 16 + ((tv % p.G) / 16) * D;
 #pragma unroll
-            for (int i = 0; i < DPL; i += 2) {
-                const float2 f = unpack_half2(e2m1x2_to_f16x2(codes[(d + i) / 2]));
-                vv[i] = f.x * unpack_half2(e4m3x2_to_f16x2(sc[d + i])).x * S;
-                vv[i + 1] = f.y * unpack_half2(e4m3x2_to_f16x2(sc[d + i + 1])).x * S;
+            for (int i = 0; i < DPL; i++) {
+                const float2 f = unpack_half2(e2m1x2_to_f16x2(codes[(d + i) * 16]));
+                vv[i] = ((t & 1) ? f.y : f.x) * unpack_half2(e4m3x2_to_f16x2(sc[d + i])).x * S;
             }
             return;
         }
@@ -441,7 +447,7 @@ static __device__ void publish_whole(const DecodeParams &p, int u, int cnt, int 
     }
 }
 
-template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG, bool RP>
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG, bool RP, bool F4 = false>
 __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p, const RopeArg<RP> ra) {
     // Work units: a warp, or with PAIR (tile kernels) a warp pair -- query warp and
     // value warp -- that shares one region of shared memory.
@@ -596,8 +602,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         // paged range may cross more sequences: a segment between the first and the
         // last holds all of its sequence's items of this pool, and its unit writes it
         // to its own pool slot and publishes it alone.
+        // one object per unit for all its segments: each keeps its mbarrier phases
         PairWarp<KB, VB, KITTY, RG, RP> pw(p, wbase);
         MiniWarp<KB, VB, KITTY, RG, RP> mw(p, wbase, 0);
+        F4Warp<RG> fw(p, wbase);
         pw.rt = s_rt;
         mw.rt = s_rt;
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
@@ -614,7 +622,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             const int id = p.mid_base + (fastpool ? 0 : p.U) + u;
             float *dst = whole ? p.partials + (size_t)id * 4 * prow(D)
                                : reinterpret_cast<float *>(wbase + (last ? 0 : part0_off));
-            if (fastpool) {
+            if (F4 && fastpool) {
+                fw.run(u, x - sg.s0, end - sg.s0, dst);
+            } else if (fastpool) {
                 if (!PAIR) pw.run(u, x - sg.s0, end - sg.s0, dst);
                 else if (role == 0) pw.run_q(u, x - sg.s0, end - sg.s0);
                 else pw.run_p(u, x - sg.s0, end - sg.s0, dst);
@@ -777,12 +787,13 @@ static const RopeTab &rope_tables(int D, float base) {
     return tab;
 }
 
-template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG = false, bool RP = false>
+template <int KB, int VB, bool KITTY, bool FAST, bool PAIR, int DPL, int NW, bool PG = false, bool RP = false,
+          bool F4 = false>
 static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
     size_t smem = decode_smem_bytes(KB, VB, KITTY, p.n_boost, p.D, FAST);
     if (PG) smem += (size_t)(p.B + 1) * 8;  // paged: per-slot item prefixes
     if (RP) smem += kRopeFloats * 4;        // pre-RoPE: the tables
-    auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW, PG, RP>;
+    auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW, PG, RP, F4>;
     // The dynamic shared-memory limit is raised once per device to the most any
     // configuration of this instantiation asks for (the opt-in maximum).
     static int raised[64] = {0};

@@ -1057,6 +1057,303 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
 };
 
 // ---------------------------------------------------------------------------
+// NVFP4 tiles (BitDecoding notes, Sec. V-D: Blackwell's mxfp4 / nvfp4 formats): 64
+// tokens of e2m1 codes with e4m3 scales per 16 elements along each product's
+// contracted dimension and an fp32 scale per page.  The hardware conversion turns a
+// code byte -- the two elements one mma register takes, by the page layouts -- into
+// an exact f16x2; times its block scale it stays exact (a 2-bit by 4-bit significand).
+// The fp16 query is the QK B operand as it is (even columns; odd columns zero) and the
+// page scale S_K multiplies the logits; p' = p * S_V is the PV B operand, in natural
+// token order.  Symmetric scales: no min terms.
+//   QK: ldmatrix row = token, 16 bytes = 32 channels: lane (g, t) gets channels
+//       32 grp + 8t .. 8t+7; k pairs (2t, 2t+1 | 2t+8, 2t+9) <- bytes (0 | 1) for the first
+//       mma of a group, (2 | 3) for the second, and the query likewise.
+//   PV: ldmatrix row = channel, 16 bytes = 32 tokens: lane (g, t) gets tokens
+//       32 tg + 8t .. 8t+7, the same k pairing, and p' of those tokens (one 16-byte load).
+// ---------------------------------------------------------------------------
+template <bool PG = false>
+struct F4Warp {
+    static constexpr int D = 128, TOK = 64;
+    static constexpr int K_CODES = 0, K_SCALES = 4096, K_HDR = 4608, V_HDR = 4624, K_STAGE = 4736;
+    static constexpr int V_CODES = 0, V_SCALES = 4096, V_STAGE = 4608;
+    static constexpr int PROW = TOK + 8;  // p' row (halves), padded
+    const DecodeParams &p;
+    unsigned char *wbase;
+    WarpSmem L;  // the 4-bit tile layout: the stages below fit its tile region exactly
+    int u, lane;
+    uint64_t *bars;
+    uint32_t phase = 0, pending = 0;
+    uint32_t qb[16];  // query B registers: group grp, mma m, register r at [4 grp + 2 m + r]
+
+    __device__ F4Warp(const DecodeParams &pp, unsigned char *wb)
+        : p(pp), wbase(wb), L(4, 4, false, 0), u(0), lane(threadIdx.x & 31) {
+        bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
+    }
+    __device__ unsigned char *kslot(int s) const { return wbase + L.k0 + s * K_STAGE; }
+    __device__ unsigned char *vslot(int s) const { return wbase + 2 * K_STAGE + s * V_STAGE; }
+    __device__ bool wait_slot(int s) {
+        const bool ok = mbar_wait(&bars[s], (phase >> s) & 1u, p.status);
+        phase ^= 1u << s;
+        pending &= ~(1u << s);
+        return ok;
+    }
+    // page record and codes of the page holding tile ti
+    __device__ const uint8_t *krec(int64_t pg) const {
+        return reinterpret_cast<const uint8_t *>(p.k_meta) + ((size_t)u * (p.max_T / p.G) + pg) * p.nv_kms;
+    }
+    __device__ const uint8_t *vrec(int64_t pg) const {
+        return reinterpret_cast<const uint8_t *>(p.v_meta) + ((size_t)u * (p.max_T / p.G) + pg) * p.nv_vms;
+    }
+    __device__ const uint8_t *kcodes(int64_t pg) const {
+        return reinterpret_cast<const uint8_t *>(p.k_codes) + ((size_t)u * (p.max_T / p.G) + pg) * ((size_t)p.G * D / 2);
+    }
+    __device__ const uint8_t *vcodes(int64_t pg) const {
+        return reinterpret_cast<const uint8_t *>(p.v_codes) + ((size_t)u * (p.max_T / p.G) + pg) * ((size_t)p.G * D / 2);
+    }
+
+    // Batch K(j): key codes (4 groups x 1 KB), key scales, both page headers -> key stage
+    // j & 1, barrier j & 1.  Batch V(j): value codes (4 KB), value scales -> value stage,
+    // barrier 2 + (j & 1).
+    __device__ void issue_k(int64_t t0, int j) {
+        const int s = j & 1;
+        const int64_t ti = t0 + j, pg = ti >> p.tpp_shift;
+        const int tok0 = (int)(ti & ((1 << p.tpp_shift) - 1)) * TOK;
+        pending |= 1u << s;
+        unsigned char *st = kslot(s);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], 4096 + 512 + 16 + 16);
+        __syncwarp();
+        if (lane < 4) {
+            issue_copy(st + K_CODES + 1024 * lane, kcodes(pg) + ((size_t)lane * p.G + tok0) * 16, 1024, &bars[s]);
+        } else if (lane == 4) {
+            issue_copy(st + K_SCALES, krec(pg) + 16 + (size_t)tok0 * (D / 16), 512, &bars[s]);
+        } else if (lane == 5) {
+            issue_copy(st + K_HDR, krec(pg), 16, &bars[s]);
+        } else if (lane == 6) {
+            issue_copy(st + V_HDR, vrec(pg), 16, &bars[s]);
+        }
+    }
+    __device__ void issue_v(int64_t t0, int j) {
+        const int s = 2 + (j & 1);
+        const int64_t ti = t0 + j, pg = ti >> p.tpp_shift;
+        const int tok0 = (int)(ti & ((1 << p.tpp_shift) - 1)) * TOK;
+        pending |= 1u << s;
+        unsigned char *st = vslot(j & 1);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], 4096 + 512);
+        __syncwarp();
+        if (lane == 0) {
+            issue_copy(st + V_CODES, vcodes(pg) + (size_t)(tok0 / 32) * D * 16, 4096, &bars[s]);
+        } else if (lane == 1) {
+            issue_copy(st + V_SCALES, vrec(pg) + 16 + (size_t)(tok0 / 16) * D, 512, &bars[s]);
+        }
+    }
+
+    // f16x2 (s, s) of the e4m3 scale byte `sc`
+    __device__ __forceinline__ static uint32_t scale2(uint32_t sc) {
+        const uint32_t h = e4m3x2_to_f16x2(sc & 0xFFu);
+        return prmt(h, h, 0x1010);
+    }
+    __device__ __forceinline__ static uint32_t deq(uint32_t w, int byte, uint32_t s2) {
+        return hmul2(e2m1x2_to_f16x2((w >> (8 * byte)) & 0xFFu), s2);
+    }
+
+    // Query B registers (once per run): the fp16 query of head g >> 1 in even columns.
+    __device__ void load_qb() {
+        const int gq = lane >> 2, t = lane & 3;
+        const uint16_t *qraw = reinterpret_cast<const uint16_t *>(wbase + L.qraw);
+#pragma unroll
+        for (int grp = 0; grp < 4; grp++)
+#pragma unroll
+            for (int m = 0; m < 2; m++)
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    const int ch = 32 * grp + 8 * t + 4 * m + 2 * r;
+                    qb[4 * grp + 2 * m + r] =
+                        (gq & 1) ? 0u : *reinterpret_cast<const uint32_t *>(qraw + (gq >> 1) * 128 + ch);
+                }
+    }
+
+    // QK of the key stage st: acc[rs] for tokens 16 rs + g (c0, c1), 16 rs + 8 + g (c2, c3)
+    __device__ __forceinline__ void qk(const unsigned char *st, float (&acc)[4][4]) const {
+        const int gq = lane >> 2, t = lane & 3;
+        const uint32_t cb = smem_u32(st + K_CODES);
+#pragma unroll
+        for (int rs = 0; rs < 4; rs++) {
+            const int tk0 = 16 * rs + gq, tk1 = tk0 + 8;
+            const uint2 sw0 = *reinterpret_cast<const uint2 *>(st + K_SCALES + tk0 * 8);
+            const uint2 sw1 = *reinterpret_cast<const uint2 *>(st + K_SCALES + tk1 * 8);
+#pragma unroll
+            for (int gp = 0; gp < 2; gp++) {  // groups 2 gp, 2 gp + 1
+                uint32_t w[4];
+                const int L8 = lane & 7, m8 = (lane >> 3) & 1, g2 = (lane >> 4) & 1;
+                ldmatrix_x4(w, cb + (2 * gp + g2) * 1024 + (16 * rs + 8 * m8 + L8) * 16);
+#pragma unroll
+                for (int gg = 0; gg < 2; gg++) {
+                    const int grp = 2 * gp + gg, blk = 2 * grp + (t >> 1);  // this lane's 16-channel block
+                    const uint32_t s0 = scale2((blk < 4 ? sw0.x : sw0.y) >> (8 * (blk & 3)));
+                    const uint32_t s1 = scale2((blk < 4 ? sw1.x : sw1.y) >> (8 * (blk & 3)));
+                    const uint32_t wa = w[2 * gg], wb = w[2 * gg + 1];  // rows g, g+8
+#pragma unroll
+                    for (int m = 0; m < 2; m++)
+                        mma_16816(acc[rs], deq(wa, 2 * m, s0), deq(wb, 2 * m, s1), deq(wa, 2 * m + 1, s0),
+                                  deq(wb, 2 * m + 1, s1), qb[4 * grp + 2 * m], qb[4 * grp + 2 * m + 1]);
+                }
+            }
+        }
+    }
+
+    // PV of the value stage st with p' buffer pb: O[cs] rows = channels 16 cs + g, + 8
+    __device__ __forceinline__ void pv(const unsigned char *st, const uint16_t *pb, float (&O)[8][4]) const {
+        const int gq = lane >> 2, t = lane & 3;
+        const uint32_t cb = smem_u32(st + V_CODES);
+        uint4 bp[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (gq < 4) {
+#pragma unroll
+            for (int tg = 0; tg < 2; tg++)
+                bp[tg] = *reinterpret_cast<const uint4 *>(pb + gq * PROW + 32 * tg + 8 * t);
+        }
+#pragma unroll
+        for (int cs = 0; cs < 8; cs++) {
+            uint32_t w[4];
+            const int L8 = lane & 7, m8 = (lane >> 3) & 1, g2 = (lane >> 4) & 1;
+            ldmatrix_x4(w, cb + g2 * 2048 + (16 * cs + 8 * m8 + L8) * 16);
+            const int c0 = 16 * cs + gq, c1 = c0 + 8;
+#pragma unroll
+            for (int tg = 0; tg < 2; tg++) {
+                const int tb = 2 * tg + (t >> 1);  // this lane's 16-token block
+                const uint32_t s0 = scale2(st[V_SCALES + tb * D + c0]), s1 = scale2(st[V_SCALES + tb * D + c1]);
+                const uint32_t wa = w[2 * tg], wb = w[2 * tg + 1];
+                mma_16816(O[cs], deq(wa, 0, s0), deq(wb, 0, s1), deq(wa, 1, s0), deq(wb, 1, s1), bp[tg].x, bp[tg].y);
+                mma_16816(O[cs], deq(wa, 2, s0), deq(wb, 2, s1), deq(wa, 3, s0), deq(wb, 3, s1), bp[tg].z, bp[tg].w);
+            }
+        }
+    }
+
+    // Softmax of a tile: logits from acc (times S_K), running maximum, then p' = p S_V
+    // into pb (natural token order, heads 0..3 = rows).
+    __device__ __forceinline__ void softmax(const float (&acc)[4][4], const unsigned char *ks, uint16_t *pb,
+                                            float &m, float &l, float &a0, float &a1, bool &grow) const {
+        const int gq = lane >> 2, t = lane & 3;
+        const float SK = *reinterpret_cast<const float *>(ks + K_HDR), SV = *reinterpret_cast<const float *>(ks + V_HDR);
+        const float C = kLog2e * rsqrtf((float)D) * SK;
+        float z[4][2], tm = -INFINITY;
+#pragma unroll
+        for (int rs = 0; rs < 4; rs++) {
+            z[rs][0] = (acc[rs][0] + acc[rs][1]) * C;
+            z[rs][1] = (acc[rs][2] + acc[rs][3]) * C;
+            tm = fmaxf(tm, fmaxf(z[rs][0], z[rs][1]));
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+        const float nm = fmaxf(m, tm);
+        const float a = exp2f(m - nm);
+        grow = __any_sync(0xffffffffu, nm > m);
+        m = nm;
+        l *= a;
+        a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
+        a1 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t + 1) & 3));
+        uint16_t *row = pb + t * PROW;
+#pragma unroll
+        for (int rs = 0; rs < 4; rs++) {
+            const float p0 = exp2f(z[rs][0] - m), p1 = exp2f(z[rs][1] - m);
+            l += p0 + p1;
+            row[16 * rs + gq] = __half_as_ushort(__float2half_rn(p0 * SV));
+            row[16 * rs + 8 + gq] = __half_as_ushort(__float2half_rn(p1 * SV));
+        }
+    }
+
+    // Tiles [t0, t1) of sequence uu; the warp's partial [4][D+4] to `part`.  Pipeline as
+    // the packed-code tiles: PV of tile i with QK of tile i+1, copies two tiles ahead.
+    __device__ void run(int uu, int64_t t0, int64_t t1, float *part) {
+        u = uu;
+        const int64_t n = t1 - t0;
+        const QRegs qr = load_q_regs(p, u);
+        issue_k(t0, 0);
+        issue_v(t0, 0);
+        if (n > 1) issue_k(t0, 1);
+        store_q_warp<4>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw), reinterpret_cast<uint2 *>(wbase + L.qpair));
+        load_qb();
+        uint16_t *pb0 = reinterpret_cast<uint16_t *>(wbase + L.pbuf);
+        for (int i = lane; i < 4 * PROW; i += 32) reinterpret_cast<uint32_t *>(pb0)[i] = 0u;
+        __syncwarp();
+        float m = -INFINITY, l = 0.f, O[8][4], acc[4][4];
+#pragma unroll
+        for (int o = 0; o < 8; o++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) O[o][e] = 0.f;
+        bool ok = wait_slot(0);
+        if (ok) {
+#pragma unroll
+            for (int rs = 0; rs < 4; rs++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) acc[rs][e] = 0.f;
+            qk(kslot(0), acc);
+            float a0, a1;
+            bool grow;
+            softmax(acc, kslot(0), pb0, m, l, a0, a1, grow);
+        }
+        __syncwarp();
+        fence_proxy_async();
+        if (n > 2) issue_k(t0, 2);
+        if (n > 1) issue_v(t0, 1);
+        for (int64_t i = 0; i < n && ok; i++) {
+            const int cur = (int)(i & 1), nxt = cur ^ 1;
+            const bool more = i + 1 < n;
+            if (more) ok &= wait_slot(nxt);  // K(i+1)
+            ok &= wait_slot(2 + cur);        // V(i)
+            if (!ok) break;
+            const uint16_t *pb = pb0 + cur * 4 * PROW;
+            pv(vslot(cur), pb, O);
+            if (more) {
+#pragma unroll
+                for (int rs = 0; rs < 4; rs++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) acc[rs][e] = 0.f;
+                qk(kslot(nxt), acc);
+                float a0, a1;
+                bool grow;
+                softmax(acc, kslot(nxt), pb0 + nxt * 4 * PROW, m, l, a0, a1, grow);
+                if (grow) {
+#pragma unroll
+                    for (int o = 0; o < 8; o++) {
+                        O[o][0] *= a0;
+                        O[o][2] *= a0;
+                        O[o][1] *= a1;
+                        O[o][3] *= a1;
+                    }
+                }
+            }
+            __syncwarp();
+            fence_proxy_async();
+            if (i + 3 < n) issue_k(t0, (int)i + 3);
+            if (i + 2 < n) issue_v(t0, (int)i + 2);
+        }
+        if (!ok) {
+            for (int s = 0; s < kSlots; s++)
+                if (pending & (1u << s)) wait_slot(s);
+        }
+        // partial: heads 0..3 (lanes t < 2 hold heads 2t, 2t+1 of channels g, g+8 per set)
+        const int gq = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        __syncwarp();
+        if (t < 2) {
+#pragma unroll
+            for (int cs = 0; cs < 8; cs++) {
+                const int ch = 16 * cs + gq;
+                part[(2 * t) * (D + 4) + ch] = O[cs][0];
+                part[(2 * t + 1) * (D + 4) + ch] = O[cs][1];
+                part[(2 * t) * (D + 4) + ch + 8] = O[cs][2];
+                part[(2 * t + 1) * (D + 4) + ch + 8] = O[cs][3];
+            }
+        }
+        if (gq == 0) {
+            part[t * (D + 4) + D] = m;
+            part[t * (D + 4) + D + 1] = l;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Mini tiles: 16 tokens with fp16 values
 // ---------------------------------------------------------------------------
 // Mini tile mi of a sequence: [sink tiles][packed-key blocks][fp16-buffer tiles].

@@ -55,7 +55,9 @@ inline int num_sms() {
 
 inline bool fast_supported(const kvq_config *c) {
     const int tok = 256 / c->bits;  // a tile holds 8 key word rows
-    if (nvfp4(c)) return false;     // NVFP4 pages decode on the CUDA-core path
+    if (nvfp4(c) && (c->rope || c->D != 128 || c->H_q / c->H_kv > 4 || c->G % 64 || (c->G & (c->G - 1))))
+        return false;               // NVFP4 tiles: 64 tokens, D = 128; else the CUDA-core path
+    if (nvfp4(c)) return true;
     // tiles: any key and value widths of 2, 4, 8 bits (Kitty: 2-bit planes, 2-bit values)
     if (kitty(c) && vbits_of(c) != 2) return false;
     if (c->D != 128 || c->H_q / c->H_kv > 4) return false;  // hi/lo q' columns need g <= 4

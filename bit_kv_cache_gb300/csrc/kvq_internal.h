@@ -165,6 +165,7 @@ cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);
 cudaError_t launch_decode_paged(const DecodeParams &p, cudaStream_t st);  // p.lens set
 cudaError_t launch_decode_rope(const DecodeParams &p, bool fast, cudaStream_t st);  // p.rope set
+cudaError_t launch_decode_nvfp4(const DecodeParams &p, cudaStream_t st);            // NVFP4 tiles
 size_t decode_smem_bytes(int bits, int vbits, bool kitty, int n_boost, int D, bool fast);
 int decode_warps_per_cta(int bits, int vbits, bool kitty, int n_boost, bool fast);
 

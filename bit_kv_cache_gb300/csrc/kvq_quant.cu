@@ -459,14 +459,16 @@ __global__ void append_kernel(AppendParams p) {
 // along the contracted dimension (a key's channels, a value's tokens) gets the e4m3
 // scale of (amax_block / 6) / S and its elements the e2m1 codes of x / (s * S), both
 // by the hardware conversions (nearest even, saturating); IEEE divisions throughout.
-// Codes leave token-major ([token][D/2], channel 2i in the low nibble).
+// Code bytes pair the two elements one mma register takes: keys leave as [D/32][G][16]
+// (byte = channels 2i, 2i+1 of a token, low nibble first), values as [G/32][D][16]
+// (byte = tokens 2m, 2m+1 of a channel).
 // ------------------------------------------------------------------------------
 template <bool VALUES>
 __global__ void __launch_bounds__(256) nvfp4_page_kernel(QuantNvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int G = p.G, D = p.D, tid = threadIdx.x;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);             // [G][D] fp16
-    uint8_t *cs = smem + (size_t)G * D * 2;                        // [G][D/2] codes
+    uint8_t *cs = smem + (size_t)G * D * 2;                        // codes: keys [G][D/2], values [D][G/2]
     uint8_t *ss = cs + (size_t)G * D / 2;                          // block scales
     __shared__ float s_red[8];
     const int u = blockIdx.y;
@@ -527,32 +529,42 @@ __global__ void __launch_bounds__(256) nvfp4_page_kernel(QuantNvParams p) {
             ss[t * (D / 16) + b] = (uint8_t)sc;
         }
     } else {
-        // task = (token block tb, channel pair j): 16 tokens of channels 2j, 2j+1
-        for (int i = tid; i < (G / 16) * (D / 2); i += 256) {
-            const int tb = i / (D / 2), j = i - tb * (D / 2);
-            float m0 = 0.f, m1 = 0.f;
+        // task = (token block tb, channel c): 16 tokens, 8 code bytes, 1 scale
+        for (int i = tid; i < (G / 16) * D; i += 256) {
+            const int tb = i / D, c = i - tb * D;
+            float bmax = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; k++) {
-                m0 = fmaxf(m0, fabsf(xval(16 * tb + k, 2 * j)));
-                m1 = fmaxf(m1, fabsf(xval(16 * tb + k, 2 * j + 1)));
-            }
-            uint32_t sc0, sc1;
-            const float d0 = block_scale(m0, sc0), d1 = block_scale(m1, sc1);
+            for (int k = 0; k < 16; k++) bmax = fmaxf(bmax, fabsf(xval(16 * tb + k, c)));
+            uint32_t sc;
+            const float d = block_scale(bmax, sc);
+            uint32_t lo = 0, hi = 0;
+            if (d != 0.0f) {
 #pragma unroll
-            for (int k = 0; k < 16; k++) {
-                const int t = 16 * tb + k;
-                const uint32_t c0 = d0 != 0.0f ? f32x2_to_e2m1x2(0.0f, __fdiv_rn(xval(t, 2 * j), d0)) & 15u : 0u;
-                const uint32_t c1 = d1 != 0.0f ? f32x2_to_e2m1x2(__fdiv_rn(xval(t, 2 * j + 1), d1), 0.0f) >> 4 : 0u;
-                cs[(size_t)t * (D / 2) + j] = (uint8_t)(c0 | (c1 << 4));
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(xval(16 * tb + 2 * k + 1, c), d),
+                                                          __fdiv_rn(xval(16 * tb + 2 * k, c), d));
+                    if (k < 4) lo |= byte << (8 * k);
+                    else hi |= byte << (8 * (k - 4));
+                }
             }
-            ss[tb * D + 2 * j] = (uint8_t)sc0;
-            ss[tb * D + 2 * j + 1] = (uint8_t)sc1;
+            *reinterpret_cast<uint2 *>(cs + (size_t)c * (G / 2) + 8 * tb) = make_uint2(lo, hi);
+            ss[tb * D + c] = (uint8_t)sc;
         }
     }
     __syncthreads();
     const int64_t page = p.pg0 + pg;
-    uint4 *dc = reinterpret_cast<uint4 *>(p.codes + ((size_t)u * p.max_T + (size_t)page * G) * (D / 2));
-    for (int i = tid; i < G * D / 32; i += 256) dc[i] = reinterpret_cast<const uint4 *>(cs)[i];
+    uint4 *dc = reinterpret_cast<uint4 *>(p.codes + ((size_t)u * (p.max_T / G) + (size_t)page) * ((size_t)G * D / 2));
+    if (!VALUES) {  // chunk i = (group i / G, token i % G) <- staging row token, bytes 16 group ..
+        for (int i = tid; i < G * D / 32; i += 256) {
+            const int grp = i / G, t = i - grp * G;
+            dc[i] = *reinterpret_cast<const uint4 *>(cs + (size_t)t * (D / 2) + 16 * grp);
+        }
+    } else {        // chunk i = (token group i / D, channel i % D) <- staging row channel, bytes 16 tg ..
+        for (int i = tid; i < G * D / 32; i += 256) {
+            const int tg = i / D, c = i - tg * D;
+            dc[i] = *reinterpret_cast<const uint4 *>(cs + (size_t)c * (G / 2) + 16 * tg);
+        }
+    }
     uint8_t *rec = p.meta + ((size_t)u * (p.max_T / G) + page) * p.ms;
     const int nsc = G * D / 16;
     for (int i = tid; i < nsc / 16; i += 256)

@@ -120,7 +120,10 @@ typedef struct {
  *   S = amax(page) / 2688,  s = e4m3((amax(block) / 6) / S),  code = e2m1(x / (s S)),
  * rounded to nearest even with saturation, in fp32 IEEE arithmetic (S = 0 for an
  * all-zero page; a zero s S gives code 0).  Buffers in this mode:
- *   k_codes, v_codes  uint8 [U][max_T][D/2]  token-major; channel 2i in the low nibble
+ *   k_codes  uint8 [U][max_T/G][D/32][G][16]  per page, per 32-channel group, per token:
+ *                                            byte i = channels 2i, 2i+1 (low nibble first)
+ *   v_codes  uint8 [U][max_T/G][G/32][D][16]  per page, per 32-token group, per channel:
+ *                                            byte m = tokens 2m, 2m+1 (low nibble first)
  *   k_meta  bytes [U][max_T/G][16 + G*D/16]  per page: fp32 S, 12 bytes padding, e4m3
  *                                            key scales [G][D/16] (16 channels of a token)
  *   v_meta  bytes [U][max_T/G][16 + G*D/16]  the same with value scales [G/16][D]

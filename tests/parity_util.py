@@ -47,8 +47,18 @@ def _assert_nvfp4_state(gpu, ora, pick):
     cfg = gpu.cfg
     T, G, D = ora.T_k, cfg.G, cfg.D
     assert ora.T_v == T
-    for side in ("k", "v"):
-        codes = _np(gpu.view(side + "_codes")[:, :, :T])
+    P = T // G
+    raw = {s: _np(gpu.view(s + "_codes")).reshape(cfg.B, cfg.H_kv, -1)[:, :, : P * G * D // 2]
+           for s in ("k", "v")}
+    # keys: [P][D/32][G][16] -> token-major [T][D/2]
+    kc = raw["k"].reshape(cfg.B, cfg.H_kv, P, D // 32, G, 16).transpose(0, 1, 2, 4, 3, 5)
+    kc = kc.reshape(cfg.B, cfg.H_kv, T, D // 2)
+    # values: [P][G/32][D][16] (byte = tokens 2m, 2m+1 of a channel) -> token-major [T][D/2]
+    vr = raw["v"].reshape(cfg.B, cfg.H_kv, P, G // 32, D, 16)
+    nib = np.stack([vr & 15, vr >> 4], axis=-1)                               # [.., tg, c, m, 2]
+    nib = nib.transpose(0, 1, 2, 3, 5, 6, 4).reshape(cfg.B, cfg.H_kv, T, D)     # token-major nibbles
+    vc = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    for side, codes in (("k", kc), ("v", vc)):
         assert np.array_equal(pick(codes), pick(getattr(ora, side + "_codes"))), side + " codes differ"
         rec = _np(gpu.view(side + "_meta")[:, :, : T // G])                     # [B,H,P,16 + G*D/16]
         S = np.ascontiguousarray(rec[..., :4]).view(np.float32)[..., 0]

@@ -62,6 +62,10 @@ SMALL = {
                        4 + 128 + 40, 3),
     "nvfp4_rope": (WORKLOADS["llama3_8b_gqa_nvfp4"].replace(B=1, H_q=8, H_kv=2, T=256, rope_base=10000.0),
                    256 + 50, 2),
+    # three sequences of 20 tiles over ~56 warps: ranges cross sequences after odd
+    # tile counts, so a unit's second segment starts with its mbarriers mid-phase
+    "nvfp4_cross": (WORKLOADS["llama3_8b_gqa_nvfp4"].replace(B=3, H_q=4, H_kv=1, T=1280), 1280 + 30, 3),
+    "k4v4_cross": (WORKLOADS["llama3_8b_gqa_b4"].replace(B=3, H_q=4, H_kv=1, T=1280), 1280 + 30, 3),
 }
 
 
@@ -80,7 +84,7 @@ def test_prefill_state_and_attention(name):
     assert gpu.read_status() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi", "rope_k2v2", "nvfp4_sink_g32"])
+@pytest.mark.parametrize("name", ["gqa_b2", "kitty", "tiny_kivi", "rope_k2v2", "nvfp4_sink_g32", "nvfp4"])
 def test_decode_loop_crosses_flushes(name):
     """Enough steps that every buffer fills and is flushed at least once."""
     wl, L0, _ = SMALL[name]
