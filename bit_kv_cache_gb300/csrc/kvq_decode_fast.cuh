@@ -312,6 +312,34 @@ __device__ __forceinline__ float2 rope_cs(float pos, float th_hi, float th_lo) {
     return make_float2(c, s);
 }
 
+// Packed fp32 pairs (Blackwell's f32x2 arithmetic): two lanes of fp32, each rounded as
+// the scalar operation would be.
+__device__ __forceinline__ uint64_t f2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2x(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // Packed tiles
 // ---------------------------------------------------------------------------
@@ -601,6 +629,8 @@ struct FastWarp {
         const int gq = lane >> 2, t = lane & 3;
         const uint16_t *qraw = reinterpret_cast<const uint16_t *>(wbase + L.qraw);
         constexpr uint32_t MASK = (1u << KB) - 1u;
+        // tokens 2k and 2k+1 of the lane's row share each f32x2 operation
+        uint64_t *acc2 = reinterpret_cast<uint64_t *>(&acc[0][0]);  // [FPI/2][4]: (token 2k, 2k+1)
 #pragma unroll
         for (int ii = 0; ii < 2; ii++) {
             if (ii >= n) break;
@@ -608,27 +638,36 @@ struct FastWarp {
             const uint2 w = *reinterpret_cast<const uint2 *>(st + T::OFF_K + gq * T::K_STRIDE + 8 * pr);
             const uint2 km = *reinterpret_cast<const uint2 *>(st + T::OFF_KM + 8 * pr);
             const float2 sa = unpack_half2(km.x), sb = unpack_half2(km.y);  // (scale, min)
-            float qa[4], qb[4];
+            const uint64_t SA = f2(sa.x, sa.x), MA = f2(sa.y, sa.y), SB = f2(sb.x, sb.x), MB = f2(sb.y, sb.y);
+            uint64_t QA[4], QB[4];
 #pragma unroll
             for (int h = 0; h < 4; h++) {
                 const float2 qq = unpack_half2(*reinterpret_cast<const uint32_t *>(qraw + h * 128 + 2 * pr));
-                qa[h] = qq.x;
-                qb[h] = qq.y;
+                QA[h] = f2(qq.x, qq.x);
+                QB[h] = f2(qq.y, qq.y);
             }
             const float2 cs = rope_cs(pos0, rt[kRopeHi + pr], rt[kRopeLo + pr]);
             const float c1 = rt[kRopeC1 + pr], s1 = rt[kRopeS1 + pr];
-            float c = cs.x, s = cs.y;
+            // angles of tokens 0 and 1, and the two-token step (2 theta)
+            uint64_t C = f2(cs.x, fmaf(cs.x, c1, -cs.y * s1)), Sn = f2(cs.y, fmaf(cs.y, c1, cs.x * s1));
+            const float c2 = fmaf(c1, c1, -s1 * s1), s2 = 2.0f * c1 * s1;
+            const uint64_t C2 = f2(c2, c2), S2 = f2(s2, s2), NS2 = f2(-s2, -s2);
+            const uint64_t MAGIC = f2(-8388608.0f, -8388608.0f);
 #pragma unroll
-            for (int k = 0; k < CK::FPI; k++) {
-                const float fa = __uint_as_float(0x4B000000u | ((w.x >> (KB * k)) & MASK)) - 8388608.0f;
-                const float fb = __uint_as_float(0x4B000000u | ((w.y >> (KB * k)) & MASK)) - 8388608.0f;
-                const float ka = fmaf(fa, sa.x, sa.y), kb = fmaf(fb, sb.x, sb.y);
-                const float ra = fmaf(ka, c, -kb * s), rb = fmaf(ka, s, kb * c);
+            for (int k = 0; k < CK::FPI; k += 2) {
+                const uint64_t fa = add2(f2(__uint_as_float(0x4B000000u | ((w.x >> (KB * k)) & MASK)),
+                                            __uint_as_float(0x4B000000u | ((w.x >> (KB * k + KB)) & MASK))), MAGIC);
+                const uint64_t fb = add2(f2(__uint_as_float(0x4B000000u | ((w.y >> (KB * k)) & MASK)),
+                                            __uint_as_float(0x4B000000u | ((w.y >> (KB * k + KB)) & MASK))), MAGIC);
+                const uint64_t ka = fma2(fa, SA, MA), kb = fma2(fb, SB, MB);
+                const float2 sv = f2x(Sn);
+                const uint64_t NSv = f2(-sv.x, -sv.y);
+                const uint64_t ra = fma2(ka, C, mul2(kb, NSv)), rb = fma2(ka, Sn, mul2(kb, C));
 #pragma unroll
-                for (int h = 0; h < 4; h++) acc[k][h] = fmaf(qa[h], ra, fmaf(qb[h], rb, acc[k][h]));
-                const float cn = fmaf(c, c1, -s * s1);
-                s = fmaf(s, c1, c * s1);
-                c = cn;
+                for (int h = 0; h < 4; h++) acc2[(k / 2) * 4 + h] = fma2(QA[h], ra, fma2(QB[h], rb, acc2[(k / 2) * 4 + h]));
+                const uint64_t Cn = fma2(C, C2, mul2(Sn, NS2));
+                Sn = fma2(Sn, C2, mul2(C, S2));
+                C = Cn;
             }
         }
     }
@@ -640,10 +679,14 @@ struct FastWarp {
         const bool b2 = (t & 2) != 0, b1 = (t & 1) != 0;
         const float C = kLog2e * rsqrtf((float)T::D);
         float zt[CK::FPI];
+        // acc holds (token 2k, token 2k+1) pairs per head: entry [2k + e][h] is at pair
+        // (k, h), element e
+        const float *af = &acc[0][0];
+        auto A = [&](int tk, int h) { return af[((tk >> 1) * 4 + h) * 2 + (tk & 1)]; };
 #pragma unroll
         for (int k = 0; k < CK::FPI; k++) {
-            const float s0 = b2 ? acc[k][0] : acc[k][2], s1 = b2 ? acc[k][1] : acc[k][3];
-            float k0 = b2 ? acc[k][2] : acc[k][0], k1 = b2 ? acc[k][3] : acc[k][1];
+            const float s0 = b2 ? A(k, 0) : A(k, 2), s1 = b2 ? A(k, 1) : A(k, 3);
+            float k0 = b2 ? A(k, 2) : A(k, 0), k1 = b2 ? A(k, 3) : A(k, 1);
             k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
             k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
             const float s2 = b1 ? k0 : k1;
