@@ -452,6 +452,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     // Work units: a warp, or with PAIR (tile kernels) a warp pair -- query warp and
     // value warp -- that shares one region of shared memory.
     constexpr int NU = PAIR ? NW / 2 : NW;
+    // A CTA merges up to 2 * NU sequences, and lanes 16.. of its last warp take their
+    // slots: one lane per sequence.
+    static_assert(2 * NU <= 16, "more merged sequences than slot-taking lanes");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_seg[NU][2];   // sequence of the first / last segment of each unit (-1: none)
     __shared__ int s_cnt[NU][2];   // items of those segments
