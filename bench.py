@@ -83,7 +83,8 @@ def decode_bytes_struct(wl, st) -> int:
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in ("kvq_decode.cu", "kvq_decode.cuh", "kvq_decode_fast.cuh", "kvq_device.cuh", "kvq_internal.h",
-              "kvq_api.cu", "kvq_host.h", "kvq_paged.cu", "kvq_decode_paged.cu", "kvq_decode_rope.cu"):
+              "kvq_api.cu", "kvq_host.h", "kvq_paged.cu", "kvq_decode_paged.cu", "kvq_decode_rope.cu",
+              "kvq_decode_nvfp4.cu"):
         with open(os.path.join(ROOT, "bit_kv_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
