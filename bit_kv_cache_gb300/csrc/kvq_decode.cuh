@@ -320,10 +320,10 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long
 //   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
 //      CTA resets both counters to zero for the next call.
 // ---------------------------------------------------------------------------------
-// RoPE tables passed by value to the pre-RoPE kernels (theta_j hi, lo, cos, sin;
-// layout as in shared memory); the other kernels take an empty argument.
+// theta_j (hi, lo), passed by value to the pre-RoPE kernels (the first kRopeArgFloats
+// of their shared-memory tables); the other kernels take an empty argument.
 struct RopeTab {
-    float v[kRopeFloats];
+    float v[kRopeArgFloats];
 };
 template <bool RP>
 struct RopeArg {};
@@ -477,8 +477,21 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     int *s_pm = s_pf + (p.B + 1);                             // paged: [B + 1] mini items before slot b
     float *s_rt = reinterpret_cast<float *>(smem + NU * wbytes);  // pre-RoPE: the tables (never paged)
     if constexpr (RP) {
-        for (int i = tid; i < kRopeFloats; i += NW * 32) s_rt[i] = ra.t.v[i];
+        for (int i = tid; i < kRopeArgFloats; i += NW * 32) s_rt[i] = ra.t.v[i];
         __syncthreads();
+        if (FAST) {  // the in-row turns of the packed tiles: k theta_j for k = 2m, 2m + 1
+            for (int i = tid; i < 8 * 64; i += NW * 32) {
+                const int m = i >> 6, j = i & 63;
+                const float th = s_rt[kRopeHi + j], tl = s_rt[kRopeLo + j];
+                const float k0 = (float)(2 * m), k1 = k0 + 1.f;
+                float s0, c0, s1, c1;
+                sincosf(fmaf(k0, th, k0 * tl), &s0, &c0);
+                sincosf(fmaf(k1, th, k1 * tl), &s1, &c1);
+                reinterpret_cast<float4 *>(s_rt + kRopeCS)[i] = make_float4(c0, c1, s0, s1);
+                reinterpret_cast<float2 *>(s_rt + kRopeNS)[i] = make_float2(-s0, -s1);
+            }
+            __syncthreads();
+        }
     }
 
     if (RG && warp == 0) {
@@ -768,21 +781,19 @@ constexpr int tile_units(int kb, int vb, bool kitty, int n_boost) {
 // Tile kernels on warp pairs (query warp + value warp per unit): 4-bit keys.
 constexpr bool tile_pair(int kb, int vb) { return kb == 4 && vb == 4; }
 
-// The RoPE tables of (D, base): theta_j = base^(-2j/D) in double, kept as a two-float
-// hi + lo, and its cosine and sine (computed once per (D, base) on the host).
+// theta_j = base^(-2j/D) of (D, base) in double, kept as a two-float hi + lo (computed
+// once per (D, base) on the host).
 static const RopeTab &rope_tables(int D, float base) {
     static thread_local RopeTab tab;
     static thread_local int tD = -1;
     static thread_local float tb = -1.f;
     if (tD != D || tb != base) {
-        for (int i = 0; i < kRopeFloats; i++) tab.v[i] = 0.f;
+        for (int i = 0; i < kRopeArgFloats; i++) tab.v[i] = 0.f;
         for (int j = 0; j < D / 2 && j < 128; j++) {
             const double th = pow((double)base, -2.0 * (double)j / (double)D);
             const float hi = (float)th;
             tab.v[kRopeHi + j] = hi;
             tab.v[kRopeLo + j] = (float)(th - (double)hi);
-            tab.v[kRopeC1 + j] = (float)cos(th);
-            tab.v[kRopeS1 + j] = (float)sin(th);
         }
         tD = D;
         tb = base;

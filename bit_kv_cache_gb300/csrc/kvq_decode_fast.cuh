@@ -292,9 +292,13 @@ struct PageIds<true> {
     }
 };
 
-// Pre-RoPE keys (KVQuant notes, mechanism two).  The tables (shared memory, 128
-// entries each): theta_j as a two-float hi + lo, cos theta_j, sin theta_j.
-constexpr int kRopeHi = 0, kRopeLo = 128, kRopeC1 = 256, kRopeS1 = 384, kRopeFloats = 512;
+// Pre-RoPE keys (KVQuant notes, mechanism two).  The tables in shared memory:
+//   - theta_j as a two-float hi + lo, 128 entries each (the kernel argument);
+//   - for the packed tiles, the turns by k theta_j within a word row (k < 16, j < 64):
+//     one float4 (cos, cos, sin, sin) of k = 2m, 2m + 1 per (m, j) at kRopeCS, and one
+//     float2 of their negated sines at kRopeNS (index m * 64 + j).
+constexpr int kRopeHi = 0, kRopeLo = 128, kRopeArgFloats = 256;
+constexpr int kRopeCS = kRopeArgFloats, kRopeNS = kRopeCS + 8 * 64 * 4, kRopeFloats = kRopeNS + 8 * 64 * 2;
 
 // (cos, sin) of pos * theta_j, the angle reduced modulo 2 pi: the product's rounding
 // error is recovered with an FMA and 2 pi is subtracted in two parts (the Cody-Waite
@@ -620,15 +624,25 @@ struct FastWarp {
     }
 
     // Pre-RoPE keys (KVQuant notes, mechanism two): key t is dequantized in fp32, its
-    // channel pair (2j, 2j+1) turned by t * theta_j and dotted with the (already
-    // rotated) query on the CUDA cores.  Lane (g, t) takes word row g -- KFPI tokens
-    // from position pos0 on -- and the pairs j = t + 4i; its angles step from token
-    // to token by the rotation theta_j.  This call covers i in [i0, i0 + n).
+    // channel pair (2j, 2j+1) turned by t * theta_j and dotted with the query on the
+    // CUDA cores.  Lane (g, t) takes word row g -- KFPI tokens at positions pos0 + k --
+    // and the pairs j = t + 4i.  The turn by (pos0 + k) theta_j is split in two: the
+    // query turns back by pos0 theta_j once per pair (q . R(a + b) k = (R(a)^T q) .
+    // (R(b) k)), the key by k theta_j from the in-row table.  This call covers i in
+    // [i0, i0 + n).
+    //
+    // Codes become floats with one LOP3 each: code c at bit offset o (o + KB <= 16) of
+    // a word, OR-ed into the mantissa of 2^(23 - o), is the float 2^(23 - o) + c, so
+    // one subtraction leaves c exactly.  Tokens of the upper half-word come from the
+    // word shifted right by 16.
     __device__ __forceinline__ void qk_rope_part(const unsigned char *st, float pos0, int i0, int n,
                                                  float (&acc)[CK::FPI][4]) const {
         const int gq = lane >> 2, t = lane & 3;
         const uint16_t *qraw = reinterpret_cast<const uint16_t *>(wbase + L.qraw);
+        constexpr int HALF = CK::FPI / 2;
         constexpr uint32_t MASK = (1u << KB) - 1u;
+        const float4 *tcs = reinterpret_cast<const float4 *>(rt + kRopeCS);
+        const float2 *tns = reinterpret_cast<const float2 *>(rt + kRopeNS);
         // tokens 2k and 2k+1 of the lane's row share each f32x2 operation
         uint64_t *acc2 = reinterpret_cast<uint64_t *>(&acc[0][0]);  // [FPI/2][4]: (token 2k, 2k+1)
 #pragma unroll
@@ -639,35 +653,35 @@ struct FastWarp {
             const uint2 km = *reinterpret_cast<const uint2 *>(st + T::OFF_KM + 8 * pr);
             const float2 sa = unpack_half2(km.x), sb = unpack_half2(km.y);  // (scale, min)
             const uint64_t SA = f2(sa.x, sa.x), MA = f2(sa.y, sa.y), SB = f2(sb.x, sb.x), MB = f2(sb.y, sb.y);
+            // the query of each head turned back by pos0 theta_j
+            const float2 cs = rope_cs(pos0, rt[kRopeHi + pr], rt[kRopeLo + pr]);
             uint64_t QA[4], QB[4];
 #pragma unroll
             for (int h = 0; h < 4; h++) {
                 const float2 qq = unpack_half2(*reinterpret_cast<const uint32_t *>(qraw + h * 128 + 2 * pr));
-                QA[h] = f2(qq.x, qq.x);
-                QB[h] = f2(qq.y, qq.y);
+                const float a = fmaf(qq.x, cs.x, qq.y * cs.y), b = fmaf(qq.y, cs.x, -(qq.x * cs.y));
+                QA[h] = f2(a, a);
+                QB[h] = f2(b, b);
             }
-            const float2 cs = rope_cs(pos0, rt[kRopeHi + pr], rt[kRopeLo + pr]);
-            const float c1 = rt[kRopeC1 + pr], s1 = rt[kRopeS1 + pr];
-            // angles of tokens 0 and 1, and the two-token step (2 theta)
-            uint64_t C = f2(cs.x, fmaf(cs.x, c1, -cs.y * s1)), Sn = f2(cs.y, fmaf(cs.y, c1, cs.x * s1));
-            const float c2 = fmaf(c1, c1, -s1 * s1), s2 = 2.0f * c1 * s1;
-            const uint64_t C2 = f2(c2, c2), S2 = f2(s2, s2), NS2 = f2(-s2, -s2);
-            const uint64_t MAGIC = f2(-8388608.0f, -8388608.0f);
+            const uint32_t xs[2] = {w.x, w.x >> 16}, ys[2] = {w.y, w.y >> 16};
 #pragma unroll
             for (int k = 0; k < CK::FPI; k += 2) {
-                const uint64_t fa = add2(f2(__uint_as_float(0x4B000000u | ((w.x >> (KB * k)) & MASK)),
-                                            __uint_as_float(0x4B000000u | ((w.x >> (KB * k + KB)) & MASK))), MAGIC);
-                const uint64_t fb = add2(f2(__uint_as_float(0x4B000000u | ((w.y >> (KB * k)) & MASK)),
-                                            __uint_as_float(0x4B000000u | ((w.y >> (KB * k + KB)) & MASK))), MAGIC);
+                const int o0 = KB * (k % HALF), o1 = KB * ((k + 1) % HALF);
+                const uint32_t e0 = (uint32_t)(150 - o0) << 23, e1 = (uint32_t)(150 - o1) << 23;
+                const uint32_t sx = xs[k / HALF], sy = ys[k / HALF];
+                const uint64_t MAGIC = f2(-__uint_as_float(e0), -__uint_as_float(e1));
+                const uint64_t fa = add2(f2(__uint_as_float((sx & (MASK << o0)) | e0),
+                                            __uint_as_float((sx & (MASK << o1)) | e1)), MAGIC);
+                const uint64_t fb = add2(f2(__uint_as_float((sy & (MASK << o0)) | e0),
+                                            __uint_as_float((sy & (MASK << o1)) | e1)), MAGIC);
                 const uint64_t ka = fma2(fa, SA, MA), kb = fma2(fb, SB, MB);
-                const float2 sv = f2x(Sn);
-                const uint64_t NSv = f2(-sv.x, -sv.y);
-                const uint64_t ra = fma2(ka, C, mul2(kb, NSv)), rb = fma2(ka, Sn, mul2(kb, C));
+                // turn by k theta_j: (ka, kb) -> (ka cos - kb sin, ka sin + kb cos)
+                const float4 cs4 = tcs[(k / 2) * 64 + pr];
+                const float2 ns2 = tns[(k / 2) * 64 + pr];
+                const uint64_t C = f2(cs4.x, cs4.y), S = f2(cs4.z, cs4.w), NS = f2(ns2.x, ns2.y);
+                const uint64_t ra = fma2(ka, C, mul2(kb, NS)), rb = fma2(ka, S, mul2(kb, C));
 #pragma unroll
                 for (int h = 0; h < 4; h++) acc2[(k / 2) * 4 + h] = fma2(QA[h], ra, fma2(QB[h], rb, acc2[(k / 2) * 4 + h]));
-                const uint64_t Cn = fma2(C, C2, mul2(Sn, NS2));
-                Sn = fma2(Sn, C2, mul2(C, S2));
-                C = Cn;
             }
         }
     }
