@@ -11,8 +11,9 @@ tokens (same distribution, different pages); residual fills are staggered.
 value  = effective packed-KV bandwidth: algorithmic bytes of all timed steps
          (codes + fp16 scales/mins + fp16 sink/residual + q + out, summed per step
          from the cache state) / device time.  Whole job: summed over ranks.
-e2e    = the same through host buffers: per step, pinned q / k_new / v_new copied
-         in, the step run, out copied back, stream synchronized.
+e2e    = the same through host buffers: per step one kvq_decode_step_host call (pinned
+         q / k_new / v_new copied in, the step run, out copied back), then a stream
+         synchronize.
 roofline: the decode kernel, CUDA events on its stream, against the measured HBM
          copy bandwidth.
 
@@ -72,6 +73,24 @@ def decode_bytes(wl, lengths) -> int:
     b += U * n16 * D * 2                                           # fp16 sink / buffers
     b += 2 * wl.B * wl.H_q * D * 2                                 # q in, out
     return b
+
+
+def after_append(wl, lengths) -> dict:
+    """Cache lengths after one kvq_append_token (its rule, on the host-side lengths):
+    sink first, then the key residual and the value residual (KIVI) or the local
+    window, whose oldest value moves to the value buffer once it is full (Kitty)."""
+    n = dict(lengths)
+    if n["n_sink"] < wl.S:
+        n["n_sink"] += 1
+        return n
+    n["n_kres"] += 1
+    if wl.mode != "kitty":
+        n["n_vres"] += 1
+    elif n["n_local"] < wl.R:
+        n["n_local"] += 1
+    else:
+        n["n_vres"] += 1
+    return n
 
 
 def decode_bytes_struct(wl, st) -> int:
@@ -371,6 +390,10 @@ def paged_main(args, wl, baseline, rank, world, dev):
     clk.stop()
     ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(bb) for a, bb in evs]
+    # tens of thousands of live events slow down later runtime calls on the host
+    # (one host-buffer step went from about 42 to 226 us of host time): free them
+    # before the end-to-end leg
+    del evs
     st = sum(c.read_status() for c in caches)
     if st != 0:
         print("device status %d" % st, file=sys.stderr)
@@ -559,20 +582,22 @@ def main():
     clk.stop()
     ms = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(bb) for a, bb in evs]
+    # tens of thousands of live events slow down later runtime calls on the host
+    # (one host-buffer step went from about 42 to 226 us of host time): free them
+    # before the end-to-end leg
+    del evs
     st = sum(c.read_status() for c in caches)
     if st != 0:
         print("device status %d" % st, file=sys.stderr)
     launches = 2 * K + flushes
     ms_max, bytes_all = reduce_over_ranks(ms, float(total_bytes), world, dev)
 
-    # ---- end to end through host buffers (public API, pinned memory) ----
+    # ---- end to end through host buffers: one kvq_decode_step_host call per step
+    # (copies in, append, attend, flush, copy out; pinned memory), then a stream sync ----
     kn_h = torch.from_numpy(kn).pin_memory()
     vn_h = torch.from_numpy(vn).pin_memory()
     q_h = torch.from_numpy(qs).pin_memory()
     out_h = torch.empty((wl.B, wl.H_q, wl.D), dtype=torch.float16).pin_memory()
-    kn_s = torch.empty_like(kn_d[0])
-    vn_s = torch.empty_like(vn_d[0])
-    q_s = torch.empty_like(q_d[0])
     Ke = max(1, min(K, args.e2e_steps))
     e_bytes = 0
     for i in range(Ke + 3):
@@ -582,18 +607,12 @@ def main():
             e_bytes = 0
         c = caches[i % N_LAYERS]
         j = i % 64
-        kn_s.copy_(kn_h[j], non_blocking=True)
-        vn_s.copy_(vn_h[j], non_blocking=True)
-        q_s.copy_(q_h[j], non_blocking=True)
-        c.append_token(kn_s, vn_s)
-        e_bytes += decode_bytes(wl, c.lengths)
-        c.decode_attn(q_s, out)
-        c.flush_group()
-        out_h.copy_(out, non_blocking=True)
+        e_bytes += decode_bytes(wl, after_append(wl, c.lengths))
+        c.step_host(q_h[j], kn_h[j], vn_h[j], out_h)
         stream.synchronize()
     e_dt = time.perf_counter() - t0
-    h2d = (kn_s.numel() + vn_s.numel() + q_s.numel()) * 2
-    d2h = out.numel() * 2
+    h2d = (kn_h[0].numel() + vn_h[0].numel() + q_h[0].numel()) * 2
+    d2h = out_h.numel() * 2
 
     if rank != 0:
         if world > 1:

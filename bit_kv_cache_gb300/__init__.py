@@ -24,7 +24,8 @@ BUFFERS = ("k_codes", "k_hi", "k_bidx", "k_meta", "v_codes", "v_meta", "k_sink",
 EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_pack_k",
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
-           "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_paged_bytes", "kvq_paged_init",
+           "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_step_io_bytes", "kvq_decode_step_host",
+           "kvq_paged_bytes", "kvq_paged_init",
            "kvq_paged_prefill", "kvq_paged_append", "kvq_paged_flush_plan", "kvq_paged_flush",
            "kvq_paged_release", "kvq_paged_workspace_bytes", "kvq_paged_decode_attn",
            "kvq_paged_read_status")
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_decode_attn": ([CP, KP, P, P, P, Sz, P], I),
         "kvq_read_status": ([KP, P, ctypes.POINTER(ctypes.c_int32), P], I),
         "kvq_decode_attn_noalloc": ([CP, KP, P, P, P], I),
+        "kvq_step_io_bytes": ([CP], Sz),
+        "kvq_decode_step_host": ([CP, KP, P, P, P, P, P, Sz, P, Sz, IP, IP, P], I),
         "kvq_paged_bytes": ([CP, I64, I], Sz),
         "kvq_paged_init": ([CP, PP, P], I),
         "kvq_paged_prefill": ([CP, PP, I, P, P, I64, P], I),
@@ -143,6 +146,9 @@ class KVQCache:
         self.c.status = self.status.data_ptr()
         wsb = lib.kvq_decode_attn_workspace_bytes(ctypes.byref(self.cfg))
         self.ws = torch.zeros(wsb, dtype=torch.uint8, device=self.device)  # zero-filled
+        # staging of kvq_decode_step_host (q, k_new, v_new, out of one step)
+        self.io = torch.empty(lib.kvq_step_io_bytes(ctypes.byref(self.cfg)), dtype=torch.uint8,
+                              device=self.device)
 
     # -- helpers ------------------------------------------------------------- #
     @staticmethod
@@ -218,6 +224,29 @@ class KVQCache:
         out = self.decode_attn(q, out)
         self.flush_group()
         return out
+
+    def step_host(self, q, k_new, v_new, out):
+        """One decode step from host tensors (kvq_decode_step_host): q, out [B, H_q, D],
+        k_new, v_new [B, H_kv, D], contiguous float16 on the CPU (page-locked for the
+        copies to be asynchronous).  Enqueued on the current stream; out holds the
+        result once the stream is synchronized.  Returns (flushed_k, flushed_v)."""
+        torch = self.torch
+        for t, shp, what in ((q, (self.cfg.B, self.cfg.H_q, self.cfg.D), "q"),
+                             (out, (self.cfg.B, self.cfg.H_q, self.cfg.D), "out"),
+                             (k_new, (self.cfg.B, self.cfg.H_kv, self.cfg.D), "k_new"),
+                             (v_new, (self.cfg.B, self.cfg.H_kv, self.cfg.D), "v_new")):
+            if t.device.type != "cpu" or t.dtype != torch.float16 or not t.is_contiguous() or \
+                    tuple(t.shape) != shp:
+                raise ValueError("%s must be a contiguous float16 CPU tensor of shape %s" % (what, shp))
+        fk, fv = ctypes.c_int(0), ctypes.c_int(0)
+        _check(lib.kvq_decode_step_host(ctypes.byref(self.cfg), ctypes.byref(self.c),
+                                        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
+                                        ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                        ctypes.c_void_p(self.io.data_ptr()), self.io.numel(),
+                                        ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+                                        ctypes.byref(fk), ctypes.byref(fv), self._stream()),
+               "kvq_decode_step_host")
+        return bool(fk.value), bool(fv.value)
 
     def read_status(self) -> int:
         st = ctypes.c_int32(0)

@@ -601,4 +601,38 @@ int kvq_read_status(const kvq_cache *k, void *ws, int32_t *dev_status, void *str
     return acc ? KVQ_ERR_DEVICE : KVQ_OK;
 }
 
+// Staging layout of kvq_decode_step_host: q, k_new, v_new, out, each 256-byte aligned.
+static size_t step_io_part(size_t n) { return (n + 255) & ~(size_t)255; }
+
+size_t kvq_step_io_bytes(const kvq_config *c) {
+    if (kvq_config_check(c) != KVQ_OK) return 0;
+    const size_t nq = (size_t)c->B * c->H_q * c->D * 2, nk = (size_t)c->B * c->H_kv * c->D * 2;
+    return 2 * step_io_part(nq) + 2 * step_io_part(nk);
+}
+
+int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, const uint16_t *k_new,
+                         const uint16_t *v_new, uint16_t *out, void *io, size_t io_bytes, void *ws,
+                         size_t ws_bytes, int *flushed_k, int *flushed_v, void *stream) {
+    int e = kvq_config_check(c);
+    if (e) return e;
+    if (!k || !q || !k_new || !v_new || !out || !io || ((uintptr_t)io & 255)) return KVQ_ERR_INVALID_ARG;
+    if (io_bytes < kvq_step_io_bytes(c)) return KVQ_ERR_WORKSPACE;
+    const size_t nq = (size_t)c->B * c->H_q * c->D * 2, nk = (size_t)c->B * c->H_kv * c->D * 2;
+    char *d = static_cast<char *>(io);
+    uint16_t *dq = reinterpret_cast<uint16_t *>(d);
+    uint16_t *dk = reinterpret_cast<uint16_t *>(d + step_io_part(nq));
+    uint16_t *dv = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + step_io_part(nk));
+    uint16_t *dout = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + 2 * step_io_part(nk));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(dk, k_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
+        cudaMemcpyAsync(dq, q, nq, cudaMemcpyDefault, st) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    if ((e = kvq_append_token(c, k, dk, dv, stream))) return e;
+    if ((e = kvq_decode_attn(c, k, dq, dout, ws, ws_bytes, stream))) return e;
+    if ((e = kvq_flush_group(c, k, flushed_k, flushed_v, stream))) return e;
+    if (cudaMemcpyAsync(out, dout, nq, cudaMemcpyDefault, st) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
 }  // extern "C"

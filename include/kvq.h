@@ -214,6 +214,31 @@ int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream);
 int kvq_decode_attn(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
                     uint16_t *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Bytes of the device staging buffer of kvq_decode_step_host for cfg (0 if cfg is
+ * invalid): q, k_new, v_new and out of one step, each 256-byte aligned. */
+size_t kvq_step_io_bytes(const kvq_config *cfg);
+
+/* One whole decode step from host memory: the three stages of the decode pipeline in
+ * order (Kitty Sec. 4.3), with the copies in and out.
+ *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) are copied
+ *      into the device staging buffer io, one cudaMemcpyAsync each;
+ *   2. kvq_append_token, kvq_decode_attn (output into io), kvq_flush_group;
+ *   3. the attention output is copied into out (host fp16 [B][H_q][D]).
+ * Everything is enqueued on `stream` and nothing is synchronized: out holds the result
+ * once the stream has passed this point (cudaStreamSynchronize or an event), and the
+ * host inputs must stay unchanged until then.  The copies are asynchronous only from
+ * and to page-locked host memory.
+ * io: device buffer of io_bytes >= kvq_step_io_bytes(cfg), 256-byte aligned, owned by
+ * the caller (KVQ_ERR_WORKSPACE if too small); ws, ws_bytes as for kvq_decode_attn;
+ * flushed_k, flushed_v as for kvq_flush_group.
+ * Returns KVQ_OK or the status of the first stage that fails; the stages before it
+ * have taken effect, as if called one by one (a refused append leaves the cache as it
+ * was; only the copies into io were enqueued). */
+int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *q,
+                         const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, void *io,
+                         size_t io_bytes, void *ws, size_t ws_bytes, int *flushed_k,
+                         int *flushed_v, void *stream);
+
 /* Size of the library's own decode scratch region (16 MiB per device). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

@@ -131,3 +131,27 @@ def test_workspace_size_grows_with_sequences(kvq):
     a = kvq.lib.kvq_decode_attn_workspace_bytes(ctypes.byref(_cfg(kvq, B=1)))
     b = kvq.lib.kvq_decode_attn_workspace_bytes(ctypes.byref(_cfg(kvq, B=8)))
     assert 0 < a < b
+
+
+def test_step_io_bytes_and_refusals_before_any_copy(kvq):
+    c = _cfg(kvq)                                   # B=2, H_q=8, H_kv=2, D=128
+    nq, nk = 2 * 8 * 128 * 2, 2 * 2 * 128 * 2       # q / out and k_new / v_new bytes
+    r256 = lambda n: (n + 255) // 256 * 256
+    assert kvq.lib.kvq_step_io_bytes(ctypes.byref(c)) == 2 * r256(nq) + 2 * r256(nk)
+    odd = _cfg(kvq, B=3, H_q=3, H_kv=1, D=64, G=32, R=32)
+    assert kvq.lib.kvq_step_io_bytes(ctypes.byref(odd)) == 2 * r256(3 * 3 * 64 * 2) + 2 * r256(3 * 64 * 2)
+    assert kvq.lib.kvq_step_io_bytes(ctypes.byref(_cfg(kvq, H_q=7))) == 0
+    need = kvq.lib.kvq_step_io_bytes(ctypes.byref(c))
+    f = kvq.lib.kvq_decode_step_host
+    P = ctypes.c_void_p
+    cache = kvq.Cache()
+    host = P(0x1000)                                # never dereferenced: every case is refused first
+    io = P(0x10000)
+
+    def call(q=host, io_=io, io_bytes=need, cfg=c):
+        return f(ctypes.byref(cfg), ctypes.byref(cache), q, host, host, host, io_, io_bytes, P(0x20000),
+                 1 << 20, None, None, None)
+    assert call(q=P(0)) == -1                       # a missing host buffer
+    assert call(io_=P(0x10010)) == -1               # staging not 256-byte aligned
+    assert call(io_bytes=need - 1) == -4            # staging too small
+    assert call(cfg=_cfg(kvq, H_q=7)) == -1         # invalid configuration

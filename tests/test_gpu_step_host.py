@@ -1,0 +1,66 @@
+"""kvq_decode_step_host (one decode step from host buffers: copies in, append,
+attend, flush, copy out) against the same steps through the device-buffer calls,
+over steps that cross a flush of the residual."""
+import numpy as np
+import pytest
+
+import kvq_synth
+from kvq_synth import WORKLOADS
+from parity_util import TOL_ABS, TOL_REL, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+CASES = {
+    # prefill leaves R - 3 tokens in the residual: the fourth step flushes it
+    "gqa_b2": (WORKLOADS["llama3_8b_gqa_b2"].replace(B=2, H_q=16, H_kv=4, T=1024), 1024 + 128 - 3),
+    "kitty": (WORKLOADS["kitty"].replace(B=2, H_q=16, H_kv=4, T=1024), 32 + 1024 + 128 + 125),
+    "tiny_kivi": (WORKLOADS["tiny_kivi"], 256 + 29),
+}
+STEPS = 6
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_kv_cache_gb300 as m
+    return m
+
+
+def _cache(kvq, wl, K, V):
+    c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R, n_boost=wl.n_boost,
+                     mode=wl.mode, max_T=wl.T + 4 * wl.G, device=DEV)
+    c.prefill(to_dev(K, DEV), to_dev(V, DEV))
+    return c
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_host_step_matches_device_steps(kvq, name):
+    import torch
+    wl, L0 = CASES[name]
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    kn, vn = kvq_synth.decode_tokens(wl, STEPS)
+    qs = kvq_synth.queries(wl, STEPS, replica=3)
+    dev, host = _cache(kvq, wl, K, V), _cache(kvq, wl, K, V)
+    flushes = 0
+    for i in range(STEPS):
+        dev.append_token(to_dev(kn[i], DEV), to_dev(vn[i], DEV))
+        ref = dev.decode_attn(to_dev(qs[i], DEV))
+        fd = dev.flush_group()
+        out = torch.full(tuple(qs[i].shape), float("nan"), dtype=torch.float16).pin_memory()
+        fh = host.step_host(torch.from_numpy(qs[i]).pin_memory(), torch.from_numpy(kn[i]).pin_memory(),
+                            torch.from_numpy(vn[i]).pin_memory(), out)
+        torch.cuda.synchronize()
+        assert fh == fd
+        flushes += fd[0] or fd[1]
+        a = out.numpy().astype(np.float64)
+        r = ref.cpu().numpy().astype(np.float64)
+        err = np.abs(a - r)
+        assert np.isfinite(a).all() and (err <= TOL_ABS + TOL_REL * np.abs(r)).all(), float(err.max())
+        assert host.lengths == dev.lengths
+    assert flushes >= 1
+    for name_ in host.buf:                                # packed state and buffers: bit-exact
+        assert torch.equal(host.buf[name_], dev.buf[name_]), name_
+    assert host.read_status() == 0 and dev.read_status() == 0
