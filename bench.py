@@ -2,8 +2,9 @@
 
 Default workload: the Llama-3-8B-shaped GQA layer (B=4, H_q=32, H_kv=8, D=128,
 T=32768 packed 2-bit tokens, G=R=128).  One step = one decode step of one layer
-in the Kitty pipeline order: append the new token (kvq_append_token), attend
-(kvq_decode_attn), quantize the residual when it is full (kvq_flush_group).  The
+in the Kitty pipeline order: append the new token and attend (kvq_append_decode:
+one launch for KIVI caches on the packed-tile path, else kvq_append_token then
+kvq_decode_attn), quantize the residual when it is full (kvq_flush_group).  The
 benchmark rotates through 16 layer caches (16 x 77.7 MB > 2 x L2), so no step
 finds its cache in L2.  Layer l's prefill is the seeded draw rolled by l*977
 tokens (same distribution, different pages); residual fills are staggered.
@@ -542,16 +543,34 @@ def main():
     fk, fv = ctypes.c_int(0), ctypes.c_int(0)
     fkr, fvr = ctypes.byref(fk), ctypes.byref(fv)
 
+    # KIVI caches on the packed-tile path insert and attend in one launch
+    # (kvq_append_decode); the others append, then attend, so that the events around
+    # the attention time the decode kernel alone
+    tok = 256 // wl.bits
+    one_launch = wl.mode != "kitty" and wl.D == 128 and wl.H_q // wl.H_kv <= 4 and wl.G % tok == 0
+    fused = ctypes.c_int(0)
+    fusedr = ctypes.byref(fused)
+
     def step(i, ev=None):
         cfg, cc, ws, wsb, st = layer_args[i % N_LAYERS]
         j = i % 64
-        rc = lib.kvq_append_token(cfg, cc, knp[j], vnp[j], sp)
-        b = decode_bytes_struct(wl, st)
-        if ev is not None:
-            ev[0].record(stream)
-        rc |= lib.kvq_decode_attn(cfg, cc, qp[j], outp, ws, wsb, sp)
-        if ev is not None:
-            ev[1].record(stream)
+        if one_launch:
+            b = decode_bytes(wl, after_append(wl, caches[i % N_LAYERS].lengths))
+            if ev is not None:
+                ev[0].record(stream)
+            rc = lib.kvq_append_decode(cfg, cc, knp[j], vnp[j], qp[j], outp, ws, wsb, fusedr, sp)
+            if ev is not None:
+                ev[1].record(stream)
+            if not fused.value:
+                raise RuntimeError("step %d was not one launch" % i)
+        else:
+            rc = lib.kvq_append_token(cfg, cc, knp[j], vnp[j], sp)
+            b = decode_bytes_struct(wl, st)
+            if ev is not None:
+                ev[0].record(stream)
+            rc |= lib.kvq_decode_attn(cfg, cc, qp[j], outp, ws, wsb, sp)
+            if ev is not None:
+                ev[1].record(stream)
         rc |= lib.kvq_flush_group(cfg, cc, fkr, fvr, sp)
         if rc:
             raise RuntimeError("libkvq call failed in step %d" % i)
@@ -589,7 +608,7 @@ def main():
     st = sum(c.read_status() for c in caches)
     if st != 0:
         print("device status %d" % st, file=sys.stderr)
-    launches = 2 * K + flushes
+    launches = (1 if one_launch else 2) * K + flushes
     ms_max, bytes_all = reduce_over_ranks(ms, float(total_bytes), world, dev)
 
     # ---- end to end through host buffers: one kvq_decode_step_host call per step
@@ -634,7 +653,8 @@ def main():
         "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
                    "T": wl.T, "G": wl.G, "R": wl.R, "bits": wl.bits, "v_bits": wl.vbits, "S": wl.S,
                    "n_boost": wl.n_boost, "mode": wl.mode, "rope_base": wl.rope_base,
-                   "step": "append_token + decode_attn + flush_group (when full), one layer",
+                   "step": ("append_decode (one launch)" if one_launch else "append_token + decode_attn")
+                           + " + flush_group (when full), one layer",
                    "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (
                        N_LAYERS, dec_bytes / 1e6, N_LAYERS * dec_bytes / 1e9),
                    "parallelism": "independent replicas per GPU" if world > 1 else "single GPU"},

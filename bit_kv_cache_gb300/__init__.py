@@ -25,6 +25,7 @@ EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
            "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_step_io_bytes", "kvq_decode_step_host",
+           "kvq_append_decode",
            "kvq_paged_bytes", "kvq_paged_init",
            "kvq_paged_prefill", "kvq_paged_append", "kvq_paged_flush_plan", "kvq_paged_flush",
            "kvq_paged_release", "kvq_paged_workspace_bytes", "kvq_paged_decode_attn",
@@ -83,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_read_status": ([KP, P, ctypes.POINTER(ctypes.c_int32), P], I),
         "kvq_decode_attn_noalloc": ([CP, KP, P, P, P], I),
         "kvq_step_io_bytes": ([CP], Sz),
+        "kvq_append_decode": ([CP, KP, P, P, P, P, P, Sz, IP, P], I),
         "kvq_decode_step_host": ([CP, KP, P, P, P, P, P, Sz, P, Sz, IP, IP, P], I),
         "kvq_paged_bytes": ([CP, I64, I], Sz),
         "kvq_paged_init": ([CP, PP, P], I),
@@ -218,10 +220,24 @@ class KVQCache:
                                    self._stream()), "kvq_decode_attn")
         return out
 
+    def append_decode(self, q, k_new, v_new, out=None) -> Tuple[object, bool]:
+        """Insert the token and attend (kvq_append_decode); returns (out, fused), fused
+        telling whether one launch did both."""
+        torch = self.torch
+        shp, shk = (self.cfg.B, self.cfg.H_q, self.cfg.D), (self.cfg.B, self.cfg.H_kv, self.cfg.D)
+        if out is None:
+            out = torch.empty(shp, dtype=torch.float16, device=self.device)
+        fused = ctypes.c_int(0)
+        _check(lib.kvq_append_decode(ctypes.byref(self.cfg), ctypes.byref(self.c),
+                                     self._ptr(k_new, shk, "k_new"), self._ptr(v_new, shk, "v_new"),
+                                     self._ptr(q, shp, "q"), self._ptr(out, shp, "out"),
+                                     ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+                                     ctypes.byref(fused), self._stream()), "kvq_append_decode")
+        return out, bool(fused.value)
+
     def step(self, q, k_new, v_new, out=None):
         """One decode step in the Kitty pipeline order: insert, attend, flush."""
-        self.append_token(k_new, v_new)
-        out = self.decode_attn(q, out)
+        out, _ = self.append_decode(q, k_new, v_new, out)
         self.flush_group()
         return out
 

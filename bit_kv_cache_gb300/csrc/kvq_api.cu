@@ -404,8 +404,47 @@ int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream) {
     return status_of(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
 }
 
+// Decode attention over cache k.  kn / vn (may be null): append them in the same launch
+// (k already holds the lengths after the append); returns kDeclined, with nothing
+// enqueued, if the packed-tile path does not serve this call.
+static constexpr int kDeclined = 1;
+static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
+                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn);
+
 int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
                     size_t ws_bytes, void *stream) {
+    return decode_impl(c, k, q, out, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, const uint16_t *vn,
+                      const uint16_t *q, uint16_t *out, void *ws, size_t ws_bytes, int *fused, void *stream) {
+    if (fused) *fused = 0;
+    int e = kvq_config_check(c);
+    if (e) return e;
+    if ((e = check_cache_ptrs(c, k))) return e;
+    if (!kn || !vn || !aligned16(kn) || !aligned16(vn)) return KVQ_ERR_INVALID_ARG;
+    // one launch: the token goes to both residuals of a KIVI cache, and the tile path
+    // serves the attention over the lengths after the append
+    if (!kitty(c) && k->n_sink >= c->S && k->n_kres < cap_k(c) && k->n_vres < cap_v(c) &&
+        k->n_sink + k->T_k + k->n_kres == k->n_sink + k->T_v + k->n_vres + k->n_local) {
+        kvq_cache nk = *k;
+        nk.n_kres++;
+        nk.n_vres++;
+        e = decode_impl(c, &nk, q, out, ws, ws_bytes, stream, kn, vn);
+        if (e != kDeclined) {
+            if (e == KVQ_OK) {
+                *k = nk;
+                if (fused) *fused = 1;
+            }
+            return e;
+        }
+    }
+    if ((e = kvq_append_token(c, k, kn, vn, stream))) return e;
+    return kvq_decode_attn(c, k, q, out, ws, ws_bytes, stream);
+}
+
+static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
+                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn) {
     int e = kvq_config_check(c);
     if (e) return e;
     if ((e = check_cache_ptrs(c, k))) return e;
@@ -422,6 +461,7 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     // token, packed values never ahead of packed keys, mixed key blocks only at 2 bits.
     bool fast = fast_supported(c) && k->T_v <= k->T_k && k->T_v % tok == 0 &&
                 (k->T_k == k->T_v || (kitty(c) && (k->T_k - k->T_v) % 16 == 0));
+    if (kn && !fast) return kDeclined;
     const int wpc = decode_warps_per_cta(c->bits, vbits_of(c), kitty(c), kitty(c) ? c->n_boost : 0, fast);
 
     DecodeParams p;
@@ -575,6 +615,8 @@ int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, 
     p.v_local = k->v_local;
     p.q = q;
     p.out = out;
+    p.k_new = kn;
+    p.v_new = vn;
     char *w = static_cast<char *>(ws);
     p.status = reinterpret_cast<int32_t *>(w + wl.status);
     p.slot_ctr = reinterpret_cast<int32_t *>(w + wl.slot_ctr);
@@ -628,8 +670,7 @@ int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, c
         cudaMemcpyAsync(dv, v_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
         cudaMemcpyAsync(dq, q, nq, cudaMemcpyDefault, st) != cudaSuccess)
         return KVQ_ERR_CUDA;
-    if ((e = kvq_append_token(c, k, dk, dv, stream))) return e;
-    if ((e = kvq_decode_attn(c, k, dq, dout, ws, ws_bytes, stream))) return e;
+    if ((e = kvq_append_decode(c, k, dk, dv, dq, dout, ws, ws_bytes, nullptr, stream))) return e;
     if ((e = kvq_flush_group(c, k, flushed_k, flushed_v, stream))) return e;
     if (cudaMemcpyAsync(out, dout, nq, cudaMemcpyDefault, st) != cudaSuccess) return KVQ_ERR_CUDA;
     return KVQ_OK;

@@ -123,6 +123,10 @@ struct DecodeParams {
     const uint16_t *k_sink, *v_sink, *k_res, *v_res, *v_local;
     const uint16_t *q;
     uint16_t *out;
+    // appended in the same launch (dense KIVI caches, mini tiles): the new token's key
+    // and value rows [U][D]; it is the last logical token, and the warp whose mini
+    // tile holds it stores it into k_res / v_res.  Null: no append.
+    const uint16_t *k_new, *v_new;
     float *partials;       // [U][max_slots][g][D + 4]
     int32_t *slot_ctr;     // [U] slots taken (zero between calls)
     unsigned long long *item_ctr;  // [U] items merged << 32 | CTAs arrived (zero between calls)

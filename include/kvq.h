@@ -222,7 +222,7 @@ size_t kvq_step_io_bytes(const kvq_config *cfg);
  * order (Kitty Sec. 4.3), with the copies in and out.
  *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) are copied
  *      into the device staging buffer io, one cudaMemcpyAsync each;
- *   2. kvq_append_token, kvq_decode_attn (output into io), kvq_flush_group;
+ *   2. kvq_append_decode (output into io), then kvq_flush_group;
  *   3. the attention output is copied into out (host fp16 [B][H_q][D]).
  * Everything is enqueued on `stream` and nothing is synchronized: out holds the result
  * once the stream has passed this point (cudaStreamSynchronize or an event), and the
@@ -238,6 +238,18 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
                          const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, void *io,
                          size_t io_bytes, void *ws, size_t ws_bytes, int *flushed_k,
                          int *flushed_v, void *stream);
+
+/* Stages (1) and (2) together: kvq_append_token(k_new, v_new), then kvq_decode_attn(q,
+ * out), with the same arguments, layouts, results and errors.  Where the token goes to
+ * the key and value residuals of a KIVI cache (sink full) and the packed-tile path
+ * serves the attention, both run in one launch: the 16-token tile holding the new
+ * token reads its key and value rows straight from k_new and v_new, and the warp that
+ * owns that tile also stores them into the residuals.  Otherwise the two calls run one
+ * after the other (then, if the attention stage fails, the append has taken effect).
+ * *fused (may be NULL) receives 1 if one launch did both, else 0. */
+int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k_new,
+                      const uint16_t *v_new, const uint16_t *q, uint16_t *out, void *ws,
+                      size_t ws_bytes, int *fused, void *stream);
 
 /* Size of the library's own decode scratch region (16 MiB per device). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
