@@ -133,16 +133,20 @@ def assert_close(out, ref, what="attention"):
     return float(err[mask].max()) if mask.any() else 0.0
 
 
-def run_steps(gpu, ora, wl, n_steps, device, check_every=1, units=None):
-    """n decode steps (append, attend, flush) on both sides; compares outputs."""
+def run_steps(gpu, ora, wl, n_steps, device, check_every=1, units=None, fused=False):
+    """n decode steps (append, attend, flush) on both sides; compares outputs.  fused:
+    the GPU side inserts and attends with one kvq_append_decode call per step."""
     kn, vn = kvq_synth.decode_tokens(wl, n_steps)
     qs = kvq_synth.queries(wl, n_steps)
     worst = 0.0
     for i in range(n_steps):
-        gpu.append_token(to_dev(kn[i], device), to_dev(vn[i], device))
+        if fused:
+            out_t, _ = gpu.append_decode(to_dev(qs[i], device), to_dev(kn[i], device), to_dev(vn[i], device))
+        else:
+            gpu.append_token(to_dev(kn[i], device), to_dev(vn[i], device))
         ora.append(kn[i], vn[i])
         if i % check_every == 0 or i == n_steps - 1:
-            out = _np(gpu.decode_attn(to_dev(qs[i], device)).float())
+            out = _np((out_t if fused else gpu.decode_attn(to_dev(qs[i], device))).float())
             ref = ora.attend(qs[i], units=units)
             worst = max(worst, assert_close(out, ref, what="step %d" % i))
         fk, fv = gpu.flush_group()

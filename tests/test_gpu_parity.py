@@ -208,6 +208,7 @@ def test_full_size_sampled(name):
     units = [U[i] for i in sorted(rng.choice(len(U), size=min(4, len(U)), replace=False))]
     assert_state_equal(gpu, ora)          # every code, scale, min: bit-exact
     run_steps(gpu, ora, wl, 2, DEV, units=units)
+    run_steps(gpu, ora, wl, 2, DEV, units=units, fused=True)   # insert and attend in one call
     assert gpu.read_status() == 0
 
 
@@ -226,6 +227,7 @@ def test_full_size_pre_rope_sampled(wl):
     U = [(b, h) for b in range(wl.B) for h in range(wl.H_kv)]
     units = [U[i] for i in sorted(rng.choice(len(U), size=min(3, len(U)), replace=False))]
     run_steps(gpu, ora, wl, 2, DEV, units=units)
+    run_steps(gpu, ora, wl, 2, DEV, units=units, fused=True)   # insert and attend in one call
     assert gpu.read_status() == 0
 
 
@@ -240,4 +242,5 @@ def test_full_size_nvfp4_sampled():
     del K, V
     assert_state_equal(gpu, ora)
     run_steps(gpu, ora, wl, 2, DEV, units=[(0, 1), (3, 6)])
+    run_steps(gpu, ora, wl, 2, DEV, units=[(0, 1), (3, 6)], fused=True)   # insert and attend in one call
     assert gpu.read_status() == 0
