@@ -26,6 +26,21 @@ Oracle functions and their pins (``tests/test_oracle.py``):
                                inputs, one-token cache, uniform logits, permutation
                                invariance, long-double cross-check
   bytes accounting          -- the KV-cache size formula and the pages' tables
+  rope (``tests/test_oracle_rope.py``)
+                            -- D = 2 is the textbook rotation, the complex form with
+                               the KVQuant page's theta_i, scores depend only on the
+                               relative position, norms, pairs and the group law,
+                               attention against numpy over complex-rotated keys
+  e2m1 / e4m3, nvfp4_page, nvfp4_dequant (``tests/test_oracle_nvfp4.py``)
+                            -- brute force over every representable value (nearest,
+                               ties to even, saturation), page scales and codes
+                               recomputed in numpy float32, the error bound, attention
+                               over an NVFP4 cache against the textbook formula
+
+Parity unpinned: the codes that running the KIVI page's fp16 quantization snippet
+literally would give in near-tie cases.  The oracle follows the fp32 definition
+(scale rounded once to fp16, then fp32 IEEE division) instead, and the pins above
+tie that definition down.
 """
 from __future__ import annotations
 
