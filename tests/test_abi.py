@@ -155,3 +155,24 @@ def test_step_io_bytes_and_refusals_before_any_copy(kvq):
     assert call(io_=P(0x10010)) == -1               # staging not 256-byte aligned
     assert call(io_bytes=need - 1) == -4            # staging too small
     assert call(cfg=_cfg(kvq, H_q=7)) == -1         # invalid configuration
+
+
+def test_append_decode_refusals_before_any_launch(kvq):
+    c = _cfg(kvq)
+    P = ctypes.c_void_p
+    f = kvq.lib.kvq_append_decode
+    fused = ctypes.c_int(7)
+
+    def call(cache, kn=P(0x1000), vn=P(0x2000), cfg=c):
+        return f(ctypes.byref(cfg), ctypes.byref(cache), kn, vn, P(0x3000), P(0x4000), P(0x5000), 1 << 20,
+                 ctypes.byref(fused), None)
+    empty = kvq.Cache()                              # no buffers: refused by the pointer check
+    assert call(empty) == -1 and fused.value == 0    # *fused is cleared first
+    full = kvq.Cache()
+    for name in ("k_codes", "k_meta", "v_codes", "v_meta", "k_res", "v_res"):
+        setattr(full, name, 0x10000)                 # never dereferenced
+    assert call(full, kn=P(0)) == -1                 # a missing new token
+    assert call(full, vn=P(0x2008)) == -1            # misaligned value row
+    assert call(full, cfg=_cfg(kvq, H_q=7)) == -1    # invalid configuration
+    assert f(ctypes.byref(c), None, P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 1 << 20,
+             None, None) == -1                       # no cache; fused may be NULL
