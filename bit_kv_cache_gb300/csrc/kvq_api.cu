@@ -7,6 +7,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
+#include <unordered_map>
 
 #include "kvq.h"
 #include "kvq_host.h"
@@ -25,22 +27,49 @@ int64_t slot_bound(const kvq_config *c) { return cdiv(4 * (int64_t)num_sms(), un
 // range within two sequences (about U / warps-per-CTA).
 int64_t max_pool_ctas(const kvq_config *c) { return std::max<int64_t>(num_sms(), cdiv(units(c), 6)); }
 
-// Workspace: [status word][slot counters U x 4 B][item counters U x 8 B][partials].  The
-// counters are zero between calls (the combining CTA resets them).
+// Workspace: [status word][item counters U x 8 B][partials].  The counters are zero
+// between calls (the combining CTA resets them); the partials need no initial value.
 struct WsLayout {
-    size_t status, slot_ctr, item_ctr, partials, total;
+    size_t status, item_ctr, partials, total;
 };
 
 WsLayout ws_layout(const kvq_config *c) {
     WsLayout w;
     const int64_t U = units(c), g = c->H_q / c->H_kv;
-    const size_t ctr = (size_t)cdiv(U * 4, 256) * 256;
     w.status = 0;
-    w.slot_ctr = 256;
-    w.item_ctr = w.slot_ctr + ctr;                       // 8 bytes per sequence
-    w.partials = w.item_ctr + 2 * ctr;
+    w.item_ctr = 256;
+    w.partials = w.item_ctr + (size_t)cdiv(U * 8, 256) * 256;
     w.total = w.partials + (size_t)U * slot_bound(c) * g * (c->D + 4) * 4;
     return w;
+}
+
+// Packed pages a prefill or flush has written since the cache's last decode, per cache
+// (keyed by its key-code buffer): the first such key and value token.  Decode launches
+// may start before the preceding kernel in the stream has completed, and copy the
+// packed pages below these tokens early; the others only after that kernel is done.
+constexpr int64_t kNoFresh = INT64_MAX;
+struct Fresh {
+    int64_t k = kNoFresh, v = kNoFresh;
+};
+std::mutex g_fresh_mu;
+std::unordered_map<const void *, Fresh> g_fresh;
+
+void mark_fresh(const kvq_cache *k, int64_t k_tok, int64_t v_tok) {
+    std::lock_guard<std::mutex> lock(g_fresh_mu);
+    Fresh &f = g_fresh[k->k_codes];
+    f.k = std::min(f.k, k_tok);
+    f.v = std::min(f.v, v_tok);
+}
+
+// The first fresh token of the cache (keys or values), which is then forgotten: a
+// later decode is preceded by this one, which writes no packed page.
+int64_t take_fresh(const kvq_cache *k) {
+    std::lock_guard<std::mutex> lock(g_fresh_mu);
+    auto it = g_fresh.find(k->k_codes);
+    if (it == g_fresh.end()) return kNoFresh;
+    const int64_t r = std::min(it->second.k, it->second.v);
+    g_fresh.erase(it);
+    return r;
 }
 
 // CTAs of a pool (C CTAs, wpc warps each, N items, n per sequence) holding items of u.
@@ -155,6 +184,7 @@ cudaError_t copy_rows(const kvq_config *c, const uint16_t *src, int64_t src_rows
 
 }  // namespace
 
+
 extern "C" {
 
 const char *kvq_status_str(int s) {
@@ -258,6 +288,7 @@ int kvq_quant_pack_k(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
     }
     if (ce == cudaSuccess && kres > 0) ce = copy_rows(c, src, L0, ns + tk, k->k_res, cap_k(c), 0, kres, st);
     if (ce != cudaSuccess) return KVQ_ERR_CUDA;
+    if (tk > 0) mark_fresh(k, 0, kNoFresh);
     k->n_sink = ns;
     k->T_k = tk;
     k->n_kres = kres;
@@ -296,6 +327,7 @@ int kvq_quant_pack_v(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
     if (ce == cudaSuccess && vres > 0) ce = copy_rows(c, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres, st);
     if (ce == cudaSuccess && nl > 0) ce = copy_rows(c, src, L0, ns + older, k->v_local, c->R, 0, nl, st);
     if (ce != cudaSuccess) return KVQ_ERR_CUDA;
+    if (tv > 0) mark_fresh(k, kNoFresh, 0);
     k->n_sink = ns;
     k->T_v = tv;
     k->n_vres = vres;
@@ -375,6 +407,7 @@ int kvq_flush_group(const kvq_config *c, kvq_cache *k, int *flushed_k, int *flus
         p.n_pages = cap_k(c) / c->G;
         p.pg0 = k->T_k / c->G;
         if (launch_keys(c, k, p, st) != cudaSuccess) return KVQ_ERR_CUDA;
+        mark_fresh(k, k->T_k, kNoFresh);
         k->T_k += cap_k(c);
         k->n_kres = 0;
     }
@@ -386,6 +419,7 @@ int kvq_flush_group(const kvq_config *c, kvq_cache *k, int *flushed_k, int *flus
         p.n_tok = cap_v(c);
         p.tok0 = k->T_v;
         if (launch_values(c, k, p, st) != cudaSuccess) return KVQ_ERR_CUDA;
+        mark_fresh(k, kNoFresh, k->T_v);
         k->T_v += cap_v(c);
         k->n_vres = 0;
     }
@@ -409,7 +443,8 @@ int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream) {
 // enqueued, if the packed-tile path does not serve this call.
 static constexpr int kDeclined = 1;
 static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
-                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn);
+                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn,
+                       int32_t *status_word = nullptr);
 
 int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
                     size_t ws_bytes, void *stream) {
@@ -444,14 +479,11 @@ int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, con
 }
 
 static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
-                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn) {
-    int e = kvq_config_check(c);
+                       size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn,
+                       int32_t *status_word) {
+    int e = kvq::host::decode_check_args(c, k, q, out);
     if (e) return e;
-    if ((e = check_cache_ptrs(c, k))) return e;
-    if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
     const int64_t L = k->n_sink + k->T_k + k->n_kres;
-    const int64_t Lv = k->n_sink + k->T_v + k->n_vres + k->n_local;
-    if (L < 1 || L != Lv) return KVQ_ERR_INVALID_ARG;
     const WsLayout wl = ws_layout(c);
     if (!ws || !aligned16(ws) || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE;
 
@@ -618,8 +650,12 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
     p.k_new = kn;
     p.v_new = vn;
     char *w = static_cast<char *>(ws);
-    p.status = reinterpret_cast<int32_t *>(w + wl.status);
-    p.slot_ctr = reinterpret_cast<int32_t *>(w + wl.slot_ctr);
+    p.status = status_word ? status_word : reinterpret_cast<int32_t *>(w + wl.status);
+    p.slot_ctr = nullptr;  // dense caches: a CTA's slot follows from the schedule
+    {
+        const int64_t fresh = take_fresh(k);
+        p.early_tiles = fast ? (int)std::min<int64_t>(p.n_fast, fresh / tok) : 0;
+    }
     p.item_ctr = reinterpret_cast<unsigned long long *>(w + wl.item_ctr);
     p.partials = reinterpret_cast<float *>(w + wl.partials);
     return status_of(launch_decode(p, fast, (cudaStream_t)stream));
@@ -677,3 +713,27 @@ int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, c
 }
 
 }  // extern "C"
+
+namespace kvq {
+namespace host {
+
+int decode_check_args(const kvq_config *c, const kvq_cache *k, const uint16_t *q, const uint16_t *out) {
+    int e = kvq_config_check(c);
+    if (e) return e;
+    if ((e = check_cache_ptrs(c, k))) return e;
+    if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+    const int64_t L = k->n_sink + k->T_k + k->n_kres;
+    const int64_t Lv = k->n_sink + k->T_v + k->n_vres + k->n_local;
+    if (L < 1 || L != Lv) return KVQ_ERR_INVALID_ARG;
+    return KVQ_OK;
+}
+
+size_t decode_ws_counter_end(const kvq_config *c) { return ws_layout(c).partials; }
+
+int decode_attn_status(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
+                       size_t ws_bytes, void *stream, int32_t *status_word) {
+    return decode_impl(c, k, q, out, ws, ws_bytes, stream, nullptr, nullptr, status_word);
+}
+
+}  // namespace host
+}  // namespace kvq

@@ -301,6 +301,30 @@ __device__ __forceinline__ void load_q_gen(const DecodeParams &p, int u, uint16_
     __syncwarp();
 }
 
+// CTA (within its pool of W warps, wpc per CTA, N items) of the warp that owns item x:
+// the largest k with floor(k N / W) <= x.
+__device__ __forceinline__ long long cta_of_item(long long W, long long N, long long x, int wpc) {
+    const long long k = ((x + 1) * W - 1) / N;
+    return (k < W - 1 ? k : W - 1) / wpc;
+}
+
+// Slot of this CTA's partial of sequence u (dense caches): its rank among the CTAs that
+// hold items of u, fast pool first.  Every CTA between a sequence's first and last one
+// in a pool holds some of its items (the host schedule), so the slots of u are 0 .. its
+// CTA count - 1, and the combine adds them in a fixed order: the result does not depend
+// on the order in which CTAs finish.
+__device__ __forceinline__ int dense_slot(const DecodeParams &p, int u, bool tile_kernel) {
+    const long long c = blockIdx.x;
+    if (!tile_kernel) return (int)(c - ((long long)u * p.n_gc) / p.wpc);
+    long long flo = 0, nf = 0;
+    if (p.n_fast > 0) {
+        flo = cta_of_item(p.W_f, p.N_f, (long long)u * p.n_fast, p.wpc);
+        nf = cta_of_item(p.W_f, p.N_f, (long long)(u + 1) * p.n_fast - 1, p.wpc) - flo + 1;
+    }
+    if (c >= p.C_m) return (int)((c - p.C_m) - flo);
+    return (int)(nf + c - cta_of_item(p.W_m, p.N_m, (long long)u * p.n_mini, p.wpc));
+}
+
 __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long *ptr, unsigned long long v) {
     unsigned long long old;
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
@@ -308,17 +332,18 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long
 }
 
 // ---------------------------------------------------------------------------------
-// The kernel.  FAST: CTAs [0, C_f) fast warps, [C_f, C_f + C_m) mini warps.
+// The kernel.  FAST: CTAs [0, C_m) mini warps, [C_m, C_m + C_f) fast warps.
 // Otherwise: generic warps only, one chunk each.
 //
 // Epilogue, per sequence u that a CTA holds items of:
 //   1. merge: the CTA's warp partials of u (shared memory) -> one partial, written to
-//      slot s of u in global memory, s taken from a per-sequence slot counter;
+//      slot s of u in global memory: the CTA's rank among the CTAs holding items of u
+//      (dense caches), or a slot id of the CTA listed under u (paged caches);
 //   2. publish: one acquire-release atomic adds the CTA's item count of u to a
 //      per-sequence item counter; the CTA that completes the count of all items
 //      combines (no CTA ever waits for another);
-//   3. combine: log-sum-exp of the slots [0, slot counter) -> fp16 out; the combining
-//      CTA resets both counters to zero for the next call.
+//   3. combine: log-sum-exp of the slots in slot order -> fp16 out; the combining CTA
+//      resets the counters to zero for the next call.
 // ---------------------------------------------------------------------------------
 // theta_j (hi, lo), passed by value to the pre-RoPE kernels (the first kRopeArgFloats
 // of their shared-memory tables); the other kernels take an empty argument.
@@ -465,6 +490,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     __shared__ int s_fl[2 * NU];   // paged: first and last sequence of each unit range
     __shared__ int s_ml[2 * NU];   // paged: the CTA's merged sequences, ascending
     __shared__ int s_nl, s_nm;
+    // The next decode launch in the stream may start as this kernel's CTAs leave.
+    griddep_launch_dependents();
+    // The paged cache's prologue reads device lengths that preceding work writes.
+    if (FAST && PG) griddep_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = PAIR ? warp >> 1 : warp, role = PAIR ? warp & 1 : 0;
     const int D = p.D, g = p.g;
@@ -539,11 +568,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
 
     // The CTA's sequences ulo .. ulo + nu - 1 follow from its item range.  Their slots
     // are taken now (lanes of warp 0); the atomics' latency hides behind the tiles.
-    const bool fastpool = FAST && (int)blockIdx.x < p.C_f;
+    // The grid holds the mini pool's CTAs first: their work is short, and under a
+    // programmatic dependent launch the first CTAs are the first to get SMs.
+    const bool fastpool = FAST && (int)blockIdx.x >= p.C_m;
     const Pool32 P = fastpool ? Pool32{(int)p.n_fast, p.qN_f, p.rN_f, p.W_f}
                               : Pool32{(int)p.n_mini, p.qN_m, p.rN_m, p.W_m};
     const int *pfx = fastpool ? s_pf : s_pm;
-    const int kc = ((int)blockIdx.x - (fastpool ? 0 : p.C_f)) * p.wpc;
+    const int kc = ((int)blockIdx.x - (fastpool ? p.C_m : 0)) * p.wpc;
     int ulo, nu;
     if (RG) {
         // merged sequences: first and last of each unit range, ascending and distinct
@@ -596,13 +627,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         return (s_pf[b + 1] - s_pf[b]) + (s_pm[b + 1] - s_pm[b]);
     };
     // The slots are taken by lanes 16.. of the last warp, which issue no copies and no
-    // release fences, so nothing waits for these atomics before the epilogue.
+    // release fences, so nothing waits for the paged cache's atomics before the epilogue.
     const int slot_lane = tid - (NW * 32 - 16);
     int my_slot = 0;
     auto take_slot = [&]() {
         const int u = seq_at(slot_lane);
+        if (!RG) return dense_slot(p, u, FAST);
         const int k = atomicAdd(&p.slot_ctr[u], 1);
-        if (!RG) return k;
         const int id = (int)blockIdx.x * (2 * NU) + slot_lane;  // the CTA's own pool slots
         if (k < p.smax) p.seq_slots[(size_t)u * p.smax + k] = id;
         else report(p.status, KVQ_DEV_BAD_STATE_BIT);
@@ -627,6 +658,19 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         if (role == 0) pw.init_bars();  // all of the unit's mbarriers (mini units use four)
         if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // the pair's partner
         if (slot_lane >= 0 && slot_lane < nu) my_slot = take_slot();
+        // Before the wait for the preceding kernel in the stream: the first copies of a
+        // packed-tile warp's first segment, when those tiles lie in pages that no
+        // library call has written since this cache's previous decode (p.early_tiles).
+        bool pre = false;
+        if (!PAIR && !F4 && !RG && fastpool && x < x1) {
+            const Seg sg = seg_of<RG>(p, P, pfx, x);
+            const int a = x - sg.s0, b = min(x1, sg.s0 + sg.n) - sg.s0;
+            if (a + min(b - a, 2) <= p.early_tiles) {
+                pw.start(sg.u, a, b);
+                pre = true;
+            }
+        }
+        if (!RG) griddep_wait();
         // mini units: the first warp of a pair runs the 16-token tiles alone
         const bool active = fastpool || role == 0;
         const int writer = (PAIR && fastpool) ? 1 : 0;  // the warp that writes the partial
@@ -641,7 +685,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
             if (F4 && fastpool) {
                 fw.run(u, x - sg.s0, end - sg.s0, dst);
             } else if (fastpool) {
-                if (!PAIR) pw.run(u, x - sg.s0, end - sg.s0, dst);
+                if (!PAIR) pw.run(u, x - sg.s0, end - sg.s0, dst, pre && e == 0);
                 else if (role == 0) pw.run_q(u, x - sg.s0, end - sg.s0);
                 else pw.run_p(u, x - sg.s0, end - sg.s0, dst);
             } else if (active) {
@@ -660,6 +704,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         }
     } else {
         // ---- generic warp: one chunk of one sequence ----
+        griddep_wait();
         if (slot_lane >= 0 && slot_lane < nu) my_slot = take_slot();
         const int64_t j = (int64_t)blockIdx.x * p.wpc + warp;
         GenState<DPL> st;
@@ -765,7 +810,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
     }
     __syncthreads();
     if (tid < nl) {
-        p.slot_ctr[s_lu[tid]] = 0;
+        if (RG) p.slot_ctr[s_lu[tid]] = 0;
         p.item_ctr[s_lu[tid]] = 0;
     }
 }
@@ -824,8 +869,21 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidValue;
     RopeArg<RP> ra;
     if constexpr (RP) ra.t = rope_tables(p.D, p.rope_base);
-    k<<<(unsigned)(p.C_f + p.C_m + p.C_g), NW * 32, smem, st>>>(p, ra);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the kernel's CTAs may start while the preceding
+    // kernel in the stream finishes; every read of data that kernel may write waits
+    // for it (griddep_wait in the kernel).
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)(p.C_f + p.C_m + p.C_g));
+    lc.blockDim = dim3(NW * 32);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, k, p, ra);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // KIVI tiles of key width KB and value width VB; p.wpc == tile_units(KB, VB).

@@ -199,7 +199,8 @@ __device__ __forceinline__ ColConst col_const(bool lo_col) { return ColConst{lo_
 // B operands of one 16-channel slab from the page's (scale, min) words kmA..kmD of
 // channels chan_of(sl, t, 0..3): the folded query (hi or lo part by column) and
 // q * 2^-4 for the min mma (zero in lo columns); A operand of the min mma.
-//   hi column: t = fl16(q s);  lo column: fl16(q s - t), exact (fused)
+//   hi column: t = fl16(q s);  lo column: fl16(t - q s), exact (fused) -- the residual
+//   with its sign flipped, so a head's logit is (hi column) - (lo column).
 struct SlabB {
     uint32_t b0, b1, c0, c1, am0, am1;
 };
@@ -209,8 +210,8 @@ __device__ __forceinline__ SlabB slab_b(uint2 qp, uint32_t kmA, uint32_t kmB, ui
     const uint32_t s01 = prmt(kmA, kmB, 0x5410), s23 = prmt(kmC, kmD, 0x5410);
     const uint32_t t01 = hmul2(qp.x, s01), t23 = hmul2(qp.y, s23);
     if (cc.lo) {
-        r.b0 = hfma2(qp.x, s01, t01 ^ 0x80008000u);
-        r.b1 = hfma2(qp.y, s23, t23 ^ 0x80008000u);
+        r.b0 = hfma2(qp.x ^ 0x80008000u, s01, t01);
+        r.b1 = hfma2(qp.y ^ 0x80008000u, s23, t23);
         r.c0 = r.c1 = 0u;
     } else {
         r.b0 = t01;
@@ -220,6 +221,36 @@ __device__ __forceinline__ SlabB slab_b(uint2 qp, uint32_t kmA, uint32_t kmB, ui
     }
     r.am0 = prmt(kmA, kmB, 0x7632);  // (min A, min B)
     r.am1 = prmt(kmC, kmD, 0x7632);  // (min C, min D)
+    return r;
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; -inf gives 0).
+// The softmax weights feed fp16 operands, so this is far below their rounding.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The lane's share of a 16-channel slab's B operands, prepared once per tile by
+// prep_slabs(): lane (sl, t) turns the (scale, min) words of its channels chan_of(sl,
+// t, 0..3) into {scales of channels 0, 1 | 2, 3; mins of 0, 1 | 2, 3} (half2 each), in
+// place over the tile's (scale, min) row (32 lanes x 16 bytes = the row's 512 bytes).
+template <int PS>
+__device__ __forceinline__ void prep_slabs(unsigned char *km_row) {
+    const int lane = threadIdx.x & 31, sl = lane >> 2, t = lane & 3;
+    uint32_t *km = reinterpret_cast<uint32_t *>(km_row);
+    const uint32_t a = km[chan_of<PS>(sl, t, 0)], b = km[chan_of<PS>(sl, t, 1)];
+    const uint32_t c = km[chan_of<PS>(sl, t, 2)], d = km[chan_of<PS>(sl, t, 3)];
+    __syncwarp();
+    reinterpret_cast<uint4 *>(km_row)[lane] =
+        make_uint4(prmt(a, b, 0x5410), prmt(c, d, 0x5410), prmt(a, b, 0x7632), prmt(c, d, 0x7632));
+    __syncwarp();
+}
+
+__device__ __forceinline__ uint32_t lop_xor_and(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(r) : "r"(a), "r"(b), "r"(c));  // (a ^ b) & c
     return r;
 }
 
@@ -499,20 +530,46 @@ struct FastWarp {
 
     // One 16-channel slab of S = Kcodes . q' (+ the min mma) for the key half in st;
     // slab 0 starts the accumulators from zero.
+    // KIVI tiles (not Kitty, keys as stored) prepare their slabs' scales and mins once
+    // per tile (prep_slabs); Kitty's boost pass and the pre-RoPE path read the row as it
+    // was copied.
+    static constexpr bool kPrep = !KITTY && !RP;
+
     __device__ __forceinline__ void qk_slab(int sl, const unsigned char *st, float (&acc)[CK::NJ][4],
                                             float (&cm)[4]) const {
         const int gq = lane >> 2, t = lane & 3;
-        const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
         const uint2 qp = reinterpret_cast<const uint2 *>(wbase + L.qpair)[((gq >> 1) * 8 + sl) * 4 + t];
-        const SlabB b = slab_b(qp, km[chan_of<T::P>(sl, t, 0)], km[chan_of<T::P>(sl, t, 1)],
-                               km[chan_of<T::P>(sl, t, 2)], km[chan_of<T::P>(sl, t, 3)], col_const((gq & 1) != 0));
-        if (sl == 0) mma_16816_z(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
-        else mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
+        uint32_t b0, b1, am0, am1, c0, c1;
+        if constexpr (kPrep) {
+            // hi column (even gq): fl16(q s); lo column: fl16(q s) - q s, the sign-flipped
+            // exact residual, formed as fma(q * m, s, fl16(q s)) with m = 0 or -1 by column
+            const uint4 sm = reinterpret_cast<const uint4 *>(st + T::OFF_KM)[sl * 4 + t];
+            const uint32_t m = (gq & 1) ? 0xBC00BC00u : 0u;  // half2(-1, -1) or 0
+            b0 = hfma2(hmul2(qp.x, m), sm.x, hmul2(qp.x, sm.x));
+            b1 = hfma2(hmul2(qp.y, m), sm.y, hmul2(qp.y, sm.y));
+            am0 = sm.z;
+            am1 = sm.w;
+            c0 = qp.x;  // the min mma: q in both columns of a head (only the hi one is read)
+            c1 = qp.y;
+        } else {
+            const uint32_t *km = reinterpret_cast<const uint32_t *>(st + T::OFF_KM);
+            const SlabB b = slab_b(qp, km[chan_of<T::P>(sl, t, 0)], km[chan_of<T::P>(sl, t, 1)],
+                                   km[chan_of<T::P>(sl, t, 2)], km[chan_of<T::P>(sl, t, 3)],
+                                   col_const((gq & 1) != 0));
+            b0 = b.b0;
+            b1 = b.b1;
+            am0 = b.am0;
+            am1 = b.am1;
+            c0 = b.c0;
+            c1 = b.c1;
+        }
+        if (sl == 0) mma_16816_z(cm, am0, am0, am1, am1, c0, c1);
+        else mma_16816(cm, am0, am0, am1, am1, c0, c1);
         uint32_t w[4], x[4], xs[4];
         ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3) + 64 * sl);
         split<CK>(w, x, xs);
-        if (sl == 0) mma_sets<true>(acc, x, xs, b.b0, b.b1);
-        else mma_sets<false>(acc, x, xs, b.b0, b.b1);
+        if (sl == 0) mma_sets<true>(acc, x, xs, b0, b1);
+        else mma_sets<false>(acc, x, xs, b0, b1);
     }
 
     // Kitty: S += hi-plane codes . (4 q') over the boosted slots.
@@ -591,8 +648,8 @@ struct FastWarp {
 #define KVQ_Z(J)                                                                        \
     if (J < CK::NJ) {                                                                   \
         const float f = unscale<CK, J>() * C;                                           \
-        z[J % CK::NJ][0] = fmaf(acc[J % CK::NJ][0] + acc[J % CK::NJ][1], f, cst);       \
-        z[J % CK::NJ][1] = fmaf(acc[J % CK::NJ][2] + acc[J % CK::NJ][3], f, cst);       \
+        z[J % CK::NJ][0] = fmaf(acc[J % CK::NJ][0] - acc[J % CK::NJ][1], f, cst);       \
+        z[J % CK::NJ][1] = fmaf(acc[J % CK::NJ][2] - acc[J % CK::NJ][3], f, cst);       \
         tm = fmaxf(tm, fmaxf(z[J % CK::NJ][0], z[J % CK::NJ][1]));                      \
     }
         KVQ_Z(0) KVQ_Z(1) KVQ_Z(2) KVQ_Z(3) KVQ_Z(4) KVQ_Z(5) KVQ_Z(6) KVQ_Z(7)
@@ -605,7 +662,7 @@ struct FastWarp {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
         const float nm = fmaxf(m, tm);
-        a = exp2f(m - nm);  // 0 while m is -inf
+        a = ex2(m - nm);  // 0 while m is -inf
         grow = __any_sync(0xffffffffu, nm > m);
         m = nm;
         l *= a;
@@ -741,13 +798,25 @@ struct FastWarp {
     // Softmax of a tile, row set j: p = exp2(z - m) of the lane's two tokens (rows g
     // and g+8: tokens KFPI g + j and KFPI g + KFPI/2 + j), their sums, and p' = p *
     // scale_v into the tile's p' buffer.
-    __device__ __forceinline__ void softmax_chunk(int j, const float (&z)[CK::NJ][2], const unsigned char *vms,
+    // The value (scale, min) words of the lane's tokens KFPI g .. KFPI g + KFPI - 1,
+    // 16 bytes at a time.
+    __device__ __forceinline__ void load_vm(const unsigned char *vms, uint32_t (&vm)[CK::FPI]) const {
+        const uint4 *src = reinterpret_cast<const uint4 *>(vms) + (CK::FPI / 4) * (lane >> 2);
+#pragma unroll
+        for (int i = 0; i < CK::FPI / 4; i++) {
+            const uint4 w = src[i];
+            vm[4 * i] = w.x;
+            vm[4 * i + 1] = w.y;
+            vm[4 * i + 2] = w.z;
+            vm[4 * i + 3] = w.w;
+        }
+    }
+    __device__ __forceinline__ void softmax_chunk(int j, const float (&z)[CK::NJ][2], const uint32_t (&vm)[CK::FPI],
                                                   uint16_t *pb, float m, float &l, float &mn) const {
         const int gq = lane >> 2, t = lane & 3;
         const int tk0 = CK::FPI * gq + j, tk1 = tk0 + CK::FPI / 2;
-        const uint32_t *vm = reinterpret_cast<const uint32_t *>(vms);
-        const float2 sm0 = unpack_half2(vm[tk0]), sm1 = unpack_half2(vm[tk1]);
-        const float p0 = exp2f(z[j][0] - m), p1 = exp2f(z[j][1] - m);
+        const float2 sm0 = unpack_half2(vm[j]), sm1 = unpack_half2(vm[j + CK::FPI / 2]);
+        const float p0 = ex2(z[j][0] - m), p1 = ex2(z[j][1] - m);
         l += p0 + p1;
         mn = fmaf(p0, sm0.y, fmaf(p1, sm1.y, mn));
         uint16_t *row = pb + t * T::PROW;
@@ -776,14 +845,23 @@ struct FastWarp {
     // j&1); batch V(j) = value codes of j + value (scale, min) of j+1 -> value half
     // j&1, meta row (j+1)&1 (barrier 2 + j&1).  Both are issued two tiles ahead, each
     // into a buffer whose previous contents the warp has just finished reading.
-    __device__ void run(int uu, int64_t t0, int64_t t1, float *part) {
+    // The first copies of tiles [t0, t1) of sequence uu: batches K(0), V(0), K(1).
+    __device__ void start(int uu, int64_t t0, int64_t t1) {
+        u = uu;
+        pid.set(p, uu);
+        issue_kb(t0, 0);
+        issue_vb(t0, 0, t1 - t0);
+        if (t1 - t0 > 1) issue_kb(t0, 1);
+    }
+
+    // started: start(uu, t0, t1) has issued the first copies already (before the
+    // kernel's wait for the preceding kernel in the stream).
+    __device__ void run(int uu, int64_t t0, int64_t t1, float *part, bool started = false) {
         u = uu;
         pid.set(p, uu);
         const int64_t n = t1 - t0;
         const QRegs qr = load_q_regs(p, u);  // its loads go out before the first copies
-        issue_kb(t0, 0);
-        issue_vb(t0, 0, n);
-        if (n > 1) issue_kb(t0, 1);
+        if (!started) start(uu, t0, t1);
         store_q_warp<T::P>(qr, reinterpret_cast<uint16_t *>(wbase + L.qraw),
                             reinterpret_cast<uint2 *>(wbase + L.qpair));
         uint16_t *pb0 = reinterpret_cast<uint16_t *>(wbase + L.pbuf);
@@ -805,6 +883,7 @@ struct FastWarp {
 
         // prologue: QK(0), softmax(0) (the value (scale, min) of tile 0 came with K(0))
         ok &= wait_slot(0);
+        if (kPrep) prep_slabs<T::P>(kslot(0) + T::OFF_KM);
         if (RP) {
             qk_rope(kslot(0), rpos(0), reinterpret_cast<float (&)[CK::FPI][4]>(accr), z);
         } else {
@@ -817,8 +896,10 @@ struct FastWarp {
             bool grow;
             if (RP) softmax_begin_z(z, m, l, mn, a0, a1, grow);
             else softmax_begin(acc, cm, z, m, l, mn, a0, a1, grow);
+            uint32_t vm[CK::FPI];
+            load_vm(vmslot(0), vm);
 #pragma unroll
-            for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vmslot(0), pb0, m, l, mn);
+            for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vm, pb0, m, l, mn);
         }
         __syncwarp();
         fence_proxy_async();
@@ -831,6 +912,7 @@ struct FastWarp {
             if (more) ok &= wait_slot(nxt);  // K(i+1)
             ok &= wait_slot(2 + cur);        // V(i): codes of i, (scale, min) of i+1
             if (!ok) break;
+            if (kPrep && more) prep_slabs<T::P>(kslot(nxt) + T::OFF_KM);
             const uint16_t *pb = pb0 + cur * 4 * T::PROW;
             if (RP && more) {  // PV of tile i, then the CUDA-core QK of tile i+1 (a rolled loop)
 #pragma unroll
@@ -867,8 +949,10 @@ struct FastWarp {
                     }
                 }
                 uint16_t *pbn = pb0 + nxt * 4 * T::PROW;
+                uint32_t vm[CK::FPI];
+                load_vm(vmslot(nxt), vm);
 #pragma unroll
-                for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vmslot(nxt), pbn, m, l, mn);
+                for (int j = 0; j < CK::NJ; j++) softmax_chunk(j, z, vm, pbn, m, l, mn);
             }
             __syncwarp();
             fence_proxy_async();
@@ -1014,6 +1098,7 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
             const int s = (int)(j & 1);
             ok &= this->wait_slot(s);  // K(j)
             if (!ok) break;
+            if (Base::kPrep) prep_slabs<T::P>(this->kslot(s) + T::OFF_KM);
 #pragma unroll
             for (int sl = 0; sl < 8; sl++) this->qk_slab(sl, this->kslot(s), acc, cm);
             if (KITTY && this->p.n_boost > 0) this->qk_boost(this->kslot(s), acc);
@@ -1023,8 +1108,10 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
             if (j >= 2) ok &= this->wait_slot(B_EMPTY + s);  // PV(j-2) is done with buffer s
             if (!ok) break;
             uint16_t *pb = pbuf(s);
+            uint32_t vm[CK::FPI];
+            this->load_vm(this->vmslot(s), vm);
 #pragma unroll
-            for (int jj = 0; jj < CK::NJ; jj++) this->softmax_chunk(jj, z, this->vmslot(s), pb, m, l, mn);
+            for (int jj = 0; jj < CK::NJ; jj++) this->softmax_chunk(jj, z, vm, pb, m, l, mn);
             if (lane < 4) alpha()[8 * s + lane] = a;
             arrive(B_FULL + s);
             fence_proxy_async();
@@ -1302,7 +1389,7 @@ struct F4Warp {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
         const float nm = fmaxf(m, tm);
-        const float a = exp2f(m - nm);
+        const float a = ex2(m - nm);
         grow = __any_sync(0xffffffffu, nm > m);
         m = nm;
         l *= a;
@@ -1311,7 +1398,7 @@ struct F4Warp {
         uint16_t *row = pb + t * PROW;
 #pragma unroll
         for (int rs = 0; rs < 4; rs++) {
-            const float p0 = exp2f(z[rs][0] - m), p1 = exp2f(z[rs][1] - m);
+            const float p0 = ex2(z[rs][0] - m), p1 = ex2(z[rs][1] - m);
             l += p0 + p1;
             row[16 * rs + gq] = __half_as_ushort(__float2half_rn(p0 * SV));
             row[16 * rs + 8 + gq] = __half_as_ushort(__float2half_rn(p1 * SV));
@@ -1660,14 +1747,14 @@ struct MiniWarp {
             }
             // softmax over the 16 tokens (lane: head t, tokens gq and gq+8)
             const float cst = cm[0] * C;
-            float z0 = fmaf(s[0] + s[1], unsc * C, cst), z1 = fmaf(s[2] + s[3], unsc * C, cst);
+            float z0 = fmaf(s[0] - s[1], unsc * C, cst), z1 = fmaf(s[2] - s[3], unsc * C, cst);
             if (gq >= mt.n) z0 = -INFINITY;
             if (gq + 8 >= mt.n) z1 = -INFINITY;
             float tm = fmaxf(z0, z1);
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
             const float nm = fmaxf(m, tm);
-            const float a = exp2f(m - nm);
+            const float a = ex2(m - nm);
             m = nm;
             l *= a;
             const float a0 = __shfl_sync(0xffffffffu, a, (lane & ~3) | ((2 * t) & 3));
@@ -1679,7 +1766,7 @@ struct MiniWarp {
                 O[o][1] *= a1;
                 O[o][3] *= a1;
             }
-            const float p0 = exp2f(z0 - m), p1 = exp2f(z1 - m);
+            const float p0 = ex2(z0 - m), p1 = ex2(z1 - m);
             l += p0 + p1;
             pb[t * 16 + gq] = __half_as_ushort(__float2half_rn(p0));
             pb[t * 16 + gq + 8] = __half_as_ushort(__float2half_rn(p1));

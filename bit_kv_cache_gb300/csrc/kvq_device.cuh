@@ -20,6 +20,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while the
+// preceding kernel in the stream is still running.  griddep_wait() returns once that
+// kernel has completed and its memory operations are visible; launch_dependents()
+// lets the next such kernel in the stream start (its CTAs take SMs as this kernel's
+// CTAs leave).  Both are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

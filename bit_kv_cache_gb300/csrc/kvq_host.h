@@ -53,6 +53,17 @@ inline int num_sms() {
     return n;
 }
 
+// Decode attention pieces shared by the C ABI translation units (kvq_api.cu):
+//   decode_check_args: the argument checks of kvq_decode_attn other than the workspace;
+//   decode_ws_counter_end: bytes [0, n) of a workspace that must be zero when a call
+//     starts (status word and per-sequence counters; the partials after them need not);
+//   decode_attn_status: kvq_decode_attn with the kernels' device error bits sent to
+//     status_word instead of the workspace's own status word.
+int decode_check_args(const kvq_config *c, const kvq_cache *k, const uint16_t *q, const uint16_t *out);
+size_t decode_ws_counter_end(const kvq_config *c);
+int decode_attn_status(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
+                       size_t ws_bytes, void *stream, int32_t *status_word);
+
 inline bool fast_supported(const kvq_config *c) {
     const int tok = 256 / c->bits;  // a tile holds 8 key word rows
     if (nvfp4(c) && (c->rope || c->D != 128 || c->H_q / c->H_kv > 4 || c->G % 64 || (c->G & (c->G - 1))))

@@ -128,12 +128,12 @@ struct DecodeParams {
     // tile holds it stores it into k_res / v_res.  Null: no append.
     const uint16_t *k_new, *v_new;
     float *partials;       // [U][max_slots][g][D + 4]
-    int32_t *slot_ctr;     // [U] slots taken (zero between calls)
+    int32_t *slot_ctr;     // [U] slots taken (paged caches; zero between calls)
     unsigned long long *item_ctr;  // [U] items merged << 32 | CTAs arrived (zero between calls)
     int32_t *status;       // workspace status word
     // schedule
     int U, wpc;            // sequences, warps per CTA
-    int C_f, C_m, C_g;     // CTAs of the fast, mini and generic pools (grid order)
+    int C_f, C_m, C_g;     // CTAs of the fast, mini and generic pools (grid: mini, fast; or generic)
     int n_gc, max_slots;
     int n_items;           // items per sequence over all pools
     int W_f, qN_f, rN_f;   // fast pool: warps, N_f / W_f, N_f % W_f
@@ -155,6 +155,10 @@ struct DecodeParams {
     int32_t *seq_slots;    // [U][smax] partial slot ids of each sequence (paged)
     int smax;              // slot ids per sequence
     int mid_base;          // first slot id of the middle segments: pool * U + u above it
+    // Packed tiles [0, early_tiles) of every sequence lie in pages that no prefill or
+    // flush has written since the cache's previous decode: their copies may start
+    // before the preceding kernel in the stream has completed (dense caches).
+    int early_tiles;
 };
 
 constexpr int kMaxWarps = 8;

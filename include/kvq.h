@@ -31,6 +31,17 @@
  *     modified.  KVQ_ERR_CUDA means a launch failed (cudaGetLastError).
  *   - Every sequence (b, h_kv) of a kvq_cache has the same length.  The paged
  *     cache (kvq_paged, below) holds sequences of different lengths.
+ *   - Decode attention kernels (kvq_decode_attn, kvq_append_decode,
+ *     kvq_decode_step_host, kvq_decode_attn_noalloc, kvq_paged_decode_attn) are
+ *     launched as programmatic dependent launches: a kernel may start while the
+ *     preceding kernel in the stream is still running, and reads nothing that kernel
+ *     may write (q, new tokens, residuals, lengths, workspace) before that kernel has
+ *     completed.  The one exception is the packed pages of a dense cache: the first
+ *     copies of pages that no kvq_quant_pack_k / _v or kvq_flush_group call has
+ *     written since the cache's previous decode attention may start early.  The
+ *     library tracks those calls per cache (by its k_codes pointer), so a cache's
+ *     packed buffers (k_codes, k_hi, k_bidx, k_meta, v_codes, v_meta) must be written
+ *     only through the library's calls.
  */
 #ifndef KVQ_H_
 #define KVQ_H_
@@ -128,7 +139,10 @@ typedef struct {
  *                                            key scales [G][D/16] (16 channels of a token)
  *   v_meta  bytes [U][max_T/G][16 + G*D/16]  the same with value scales [G/16][D]
  *                                            (16 tokens of a channel)
- *   k_hi, k_bidx, v_local unused.  Decode attention runs on the CUDA-core path.
+ *   k_hi, k_bidx, v_local unused.  Decode attention runs on tensor-core tiles of 64
+ *   tokens (each code byte converted to an exact f16x2 operand, fp32 accumulation) when
+ *   D = 128, H_q/H_kv <= 4, rope = 0 and G is a power-of-two multiple of 64; other
+ *   shapes run on the CUDA-core path.
  * Lengths: n_sink sink tokens, T_k / T_v packed key / value tokens, n_kres keys in
  * k_res, n_vres values in v_res, n_local values in v_local.  A fresh cache has all
  * lengths 0.  Logical token order: keys [sink | packed | k_res], values
@@ -261,18 +275,23 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
  * for example an inference engine whose memory pool is already fully reserved for
  * weights and KV pages, or a plugin called from a host runtime that forbids
  * allocations inside its step callback.  Nothing here allocates.
- *   - The first call on a device (with that device current) looks the region up
- *     and enqueues a zero fill of it on `stream`; the status word and the
- *     split-T counters must start at zero, and every call leaves the counters at
- *     zero again.  Make that first call before any stream capture.
+ *   - The first call on a device (with that device current) looks the region up;
+ *     that may load the library's module onto the device, so the first call is
+ *     refused with KVQ_ERR_INVALID_ARG while `stream` is capturing.  Make it before
+ *     any stream capture.
+ *   - Every call enqueues on `stream` a zero fill of the region's first bytes (its
+ *     per-sequence counters, whose extent depends on cfg), then the decode kernel.
+ *     Calls with different configurations may therefore follow one another.
  *   - Configurations whose workspace (kvq_decode_attn_workspace_bytes) exceeds the
- *     region are refused with KVQ_ERR_WORKSPACE; nothing is enqueued.
+ *     region are refused with KVQ_ERR_WORKSPACE; nothing is enqueued.  Argument errors
+ *     enqueue nothing; a later refusal (KVQ_ERR_UNSUPPORTED from the scheduler) may
+ *     leave the zero fill enqueued, which touches only the library's own region.
  *   - The region is shared by all calls on a device: two calls whose kernels may
  *     overlap (different streams, or different host threads without ordering)
  *     race on it and give wrong results.  Serialize them, e.g. on one stream.
- *   - Device-side error bits of these calls are kept in the region's own status
- *     word and are not returned by kvq_read_status.
- * Other arguments, layouts and errors as for kvq_decode_attn. */
+ *   - cache->status must be set (else KVQ_ERR_INVALID_ARG): the kernels' device error
+ *     bits go there, and kvq_read_status(cache, NULL, ...) returns and clears them.
+ * Other arguments, layouts, results and errors as for kvq_decode_attn. */
 int kvq_decode_attn_noalloc(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
                             uint16_t *out, void *stream);
 

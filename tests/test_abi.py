@@ -176,3 +176,23 @@ def test_append_decode_refusals_before_any_launch(kvq):
     assert call(full, cfg=_cfg(kvq, H_q=7)) == -1    # invalid configuration
     assert f(ctypes.byref(c), None, P(0x1000), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 1 << 20,
              None, None) == -1                       # no cache; fused may be NULL
+
+
+def test_noalloc_refusals_before_any_launch(kvq):
+    """The no-allocation decode entry point checks everything before it looks up its
+    region or enqueues anything (fake pointers, never dereferenced)."""
+    P = ctypes.c_void_p
+    f = kvq.lib.kvq_decode_attn_noalloc
+    c = _cfg(kvq)
+    assert f(ctypes.byref(c), ctypes.byref(kvq.Cache()), P(0x3000), P(0x4000), None) == -1
+    full = kvq.Cache()
+    for name in ("k_codes", "k_meta", "v_codes", "v_meta", "k_res", "v_res"):
+        setattr(full, name, 0x10000)
+    full.T_k = full.T_v = 128
+    full.n_kres = full.n_vres = 5
+    assert f(ctypes.byref(c), ctypes.byref(full), P(0x3008), P(0x4000), None) == -1   # misaligned q
+    assert f(ctypes.byref(c), ctypes.byref(full), P(0x3000), P(0x4000), None) == -1   # no status word
+    full.status = 0x20000
+    big = _cfg(kvq, B=512, H_q=32, H_kv=32, max_T=1024)
+    assert kvq.lib.kvq_decode_attn_workspace_bytes(ctypes.byref(big)) > 16 * 1024 * 1024
+    assert f(ctypes.byref(big), ctypes.byref(full), P(0x3000), P(0x4000), None) == -4
