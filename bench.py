@@ -100,11 +100,15 @@ def decode_bytes_struct(wl, st) -> int:
                              "n_vres": st.n_vres, "n_local": st.n_local})
 
 
-def kernel_hash() -> str:
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode.cuh", "kvq_decode_fast.cuh", "kvq_device.cuh", "kvq_internal.h",
+                  "kvq_api.cu", "kvq_host.h", "kvq_paged.cu", "kvq_decode_paged.cu", "kvq_decode_rope.cu",
+                  "kvq_decode_nvfp4.cu")
+QUANT_SOURCES = ("kvq_quant.cu", "kvq_device.cuh", "kvq_internal.h", "kvq_api.cu", "kvq_host.h")
+
+
+def kernel_hash(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_decode.cuh", "kvq_decode_fast.cuh", "kvq_device.cuh", "kvq_internal.h",
-              "kvq_api.cu", "kvq_host.h", "kvq_paged.cu", "kvq_decode_paged.cu", "kvq_decode_rope.cu",
-              "kvq_decode_nvfp4.cu"):
+    for f in sources:
         with open(os.path.join(ROOT, "bit_kv_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -119,7 +123,8 @@ def profiled_traffic(workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    src = QUANT_SOURCES if workload.startswith("quant_") else DECODE_SOURCES
+    if not e or e.get("kernel_hash") != kernel_hash(src):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -196,18 +201,40 @@ def reduce_over_ranks(ms: float, nbytes: float, world: int, device=None):
     return float(mx[0]), float(sm[0])
 
 
-def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
-    """The oracle (single thread, fp64) on a bounded sample: decode attention over
-    n_units (b, h_kv) sequences of the workload.  Returns (GB/s in the benchmark's
-    byte accounting, seconds, steps, sample description)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_oracle_rate(wl, max_seconds: float, threads: int = 1):
+    """The oracle (fp64 attention) on a bounded sample of the workload: decode attention
+    over `threads` independent (b, h_kv) sequences of the workload's length, one per
+    thread, repeated for about max_seconds.  Returns (GB/s in the benchmark's byte
+    accounting, seconds, repetitions, sample description)."""
     import oracle
     L0 = wl.T + 64
-    rng = np.random.default_rng(1)
+    n_units = max(1, threads)
     sub = wl.replace(B=1, H_kv=n_units, H_q=n_units * wl.g)
-    K, V = kvq_synth.prefill_kv(wl.replace(B=1, H_kv=min(wl.H_kv, n_units)), L0)
+    K, V = kvq_synth.prefill_kv(sub, L0)
     ora = oracle.OracleCache(sub.B, sub.H_q, sub.H_kv, sub.D, sub.G, sub.bits, S=sub.S, R=sub.R,
                              n_boost=sub.n_boost, mode=sub.mode, v_bits=sub.v_bits, rope_base=sub.rope_base)
     ora.prefill(K, V)
+    del K, V
     q = kvq_synth.queries(sub, 1)[0]
     lengths = dict(n_sink=ora.n_sink, T_k=ora.T_k, n_kres=ora.n_kres, T_v=ora.T_v,
                    n_vres=ora.n_vres, n_local=ora.n_local)
@@ -215,15 +242,65 @@ def cpu_oracle_rate(wl, max_seconds: float, n_units: int = 1):
     t0 = time.perf_counter()
     steps = 0
     while True:
-        ora.attend(q)
+        ora.attend(q, threads=threads)
         steps += 1
         if time.perf_counter() - t0 >= max_seconds:
             break
     dt = time.perf_counter() - t0
-    desc = ("oracle decode attention (fp64, 1 thread) over %d of %d (b,h_kv) sequences, "
-            "%d tokens each, %d repetitions" % (n_units, wl.B * wl.H_kv, L0, steps))
-    del rng
+    desc = ("oracle decode attention (fp64, %d thread%s, one (b,h_kv) sequence each) over %d sequences "
+            "of %d tokens, %d repetitions" % (threads, "s" if threads > 1 else "", n_units, L0, steps))
     return per * steps / dt / 1e9, dt, steps, desc
+
+
+def cpu_quant_rate(wl, max_seconds: float, threads: int = 1):
+    """The oracle's prefill quantizer (keys per channel, values per token, packing) over
+    `threads` independent sequences of n tokens each, n sized for about max_seconds."""
+    import oracle
+    probe_n = 4 * wl.G
+    sub = wl.replace(B=1, H_kv=1, H_q=wl.g)
+    K, V = kvq_synth.prefill_kv(sub, probe_n)
+    o = oracle.OracleCache(1, wl.g, 1, wl.D, wl.G, wl.bits, R=wl.R, v_bits=wl.v_bits)
+    t0 = time.perf_counter()
+    o.prefill(K, V)
+    per_tok = (time.perf_counter() - t0) / probe_n
+    n = max(wl.G, int(max_seconds / max(per_tok, 1e-9)) // wl.G * wl.G)
+    n = min(n, wl.T)
+    n_units = max(1, threads)
+    sub = wl.replace(B=1, H_kv=n_units, H_q=n_units * wl.g)
+    K, V = kvq_synth.prefill_kv(sub, n)
+
+    def one(h):
+        oc = oracle.OracleCache(1, wl.g, 1, wl.D, wl.G, wl.bits, R=wl.R, v_bits=wl.v_bits)
+        oc.prefill(np.ascontiguousarray(K[:, h:h + 1]), np.ascontiguousarray(V[:, h:h + 1]))
+    t0 = time.perf_counter()
+    if threads > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(n_units)))
+    else:
+        one(0)
+    dt = time.perf_counter() - t0
+    b = quant_pack_bytes(sub, n)
+    return (b["k"] + b["v"]) / dt / 1e9, dt, ("oracle kvq_quant_pack_k + _v (fp32 quantizer, %d thread%s) "
+                                              "over %d sequence%s of %d tokens" % (
+                                                  threads, "s" if threads > 1 else "", n_units,
+                                                  "s" if n_units > 1 else "", n))
+
+
+def cpu_baseline(wl, seconds: float) -> dict:
+    """The oracle timed on this host: single-threaded, and on all cores over independent
+    (b, h_kv) sequences (results identical: the same code per sequence)."""
+    nproc = os.cpu_count() or 1
+    v1, dt1, n1, d1 = cpu_oracle_rate(wl, seconds * 0.4, 1)
+    va, dta, na, da = cpu_oracle_rate(wl, seconds * 0.3, nproc)
+    q1, qdt1, qd1 = cpu_quant_rate(wl, seconds * 0.15, 1)
+    qa, qdta, qda = cpu_quant_rate(wl, seconds * 0.15, nproc)
+    return {"value": v1, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": d1, "seconds": dt1,
+            "cpu_model": cpu_model(), "nproc": nproc,
+            "all_cores": {"value": va, "unit": "GB/s", "cores": nproc, "sample": da, "seconds": dta},
+            "quant_pack": {"value": q1, "unit": "GB/s", "cores": 1, "sample": qd1, "seconds": qdt1,
+                           "all_cores": {"value": qa, "unit": "GB/s", "cores": nproc, "sample": qda,
+                                         "seconds": qdta}}}
 
 
 def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
@@ -278,6 +355,57 @@ def reference_arm(args, wl, baseline, rank, world, budget_s: float = 150.0):
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def quant_pack_bytes(wl, L0) -> dict:
+    """Algorithmic bytes of the prefill calls over L0 tokens (no sink): the fp16 input read
+    once; packed codes, per-group (scale, min) and the fp16 residual rows written."""
+    U, D, G = wl.B * wl.H_kv, wl.D, wl.G
+    T = L0 // G * G
+    res = L0 - T
+    k = U * L0 * D * 2 + U * T * D * wl.bits // 8 + U * (T // G) * D * 4 + U * res * D * 2
+    v = U * L0 * D * 2 + U * T * D * wl.vbits // 8 + U * T * (D // min(G, D)) * 4 + U * res * D * 2
+    return {"k": k, "v": v}
+
+
+def quant_pack_measure(kvq, dev, peak, reps: int = 5) -> dict:
+    """kvq_quant_pack_k and kvq_quant_pack_v over the long-context prefill (B=1, H_kv=8,
+    131072 + 64 tokens, 2-bit): CUDA events around each call, a 512 MB write between calls
+    so that the input is not in L2; the median of `reps` calls."""
+    import torch
+    wl = kvq_synth.WORKLOADS["long_128k"]
+    L0 = wl.T + 64
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    del K, V
+    c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, R=wl.R, max_T=wl.T + wl.G, device=dev)
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ts = {"k": [], "v": []}
+    for r in range(reps + 1):
+        for name in ("n_sink", "T_k", "n_kres", "T_v", "n_vres", "n_local", "local_head"):
+            setattr(c.c, name, 0)       # an empty cache again (host-side lengths)
+        for side, fn, x in (("k", c.quant_pack_k, Kd), ("v", c.quant_pack_v, Vd)):
+            scrub.fill_(r & 255)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(x)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if r > 0:                   # the first call warms up
+                ts[side].append(a.elapsed_time(b))
+    assert c.read_status() == 0
+    nb = quant_pack_bytes(wl, L0)
+    outp = {"workload": "long_128k prefill: B=1, H_kv=8, D=128, %d tokens, 2-bit, G=128 (%d MB fp16 per side)" % (
+        L0, nb["k"] // 2**20 // 1), "timing": "median of %d calls, CUDA events, L2 scrubbed before each" % reps}
+    for side in ("k", "v"):
+        ms = statistics.median(ts[side])
+        gbs = nb[side] / (ms * 1e-3) / 1e9
+        outp["kvq_quant_pack_" + side] = {"us": ms * 1e3, "algorithmic_bytes": nb[side], "achieved": gbs,
+                                          "frac": gbs / peak, "traffic": profiled_traffic("quant_" + side)}
+    del Kd, Vd, c, scrub
+    torch.cuda.empty_cache()
+    return outp
 
 
 def paged_bytes(wl, lens_host) -> int:
@@ -456,9 +584,7 @@ def paged_main(args, wl, baseline, rank, world, dev):
                 "d2h_bytes_per_step": d2h, "us_per_step": e_dt / Ke * 1e6},
     }
     if not args.no_cpu_baseline and world == 1:
-        v, dt, n, desc = cpu_oracle_rate(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -472,9 +598,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="llama3_8b_gqa_b2", choices=sorted(kvq_synth.WORKLOADS))
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=24.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quant-pack", action="store_true", help="skip the prefill quant/pack measurement")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="repeat the K-step timed region until this much device time")
+    ap.add_argument("--max-timed-steps", type=int, default=24000,
+                    help="cap on the steps of all timed regions (sets the caches' capacity)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     baseline = load_baseline()
@@ -501,7 +632,8 @@ def main():
 
     # ---- N_LAYERS layer caches: one seeded draw, rolled per layer; staggered fills ----
     extra = (wl.S + wl.R) if wl.mode == "kitty" else 0
-    grow = -(-(args.steps + args.warmup + 256) // N_LAYERS)          # appends per layer
+    max_timed_steps = max(args.steps, args.max_timed_steps)
+    grow = -(-(max_timed_steps + args.steps + args.warmup + args.e2e_steps + 256) // N_LAYERS)  # appends per layer
     max_T = wl.T + wl.G * (grow // wl.G + 3)
     L0 = wl.T + extra + wl.G - 1
     K0, V0 = kvq_synth.prefill_kv(wl, L0, replica=rank)
@@ -529,8 +661,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     # The timed steps call the C ABI directly with prepared arguments, so that the
-    # host enqueues ahead of the GPU and the per-launch events time the kernels, not
-    # the argument marshalling of the Python binding.
+    # host enqueues ahead of the GPU and the device time is the kernels' own.
     import ctypes
     lib = kvq.lib
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -544,34 +675,43 @@ def main():
     fkr, fvr = ctypes.byref(fk), ctypes.byref(fv)
 
     # KIVI caches on the packed-tile path insert and attend in one launch
-    # (kvq_append_decode); the others append, then attend, so that the events around
-    # the attention time the decode kernel alone
+    # (kvq_append_decode); the others append, then attend.
     tok = 256 // wl.bits
     one_launch = wl.mode != "kitty" and wl.D == 128 and wl.H_q // wl.H_kv <= 4 and wl.G % tok == 0
     fused = ctypes.c_int(0)
     fusedr = ctypes.byref(fused)
+    cap = wl.G if wl.mode == "kitty" else wl.R
 
-    def step(i, ev=None):
+    def step(i, fl_ev=None, dec_ev=None):
+        """One step; fl_ev / dec_ev (lists) receive event pairs around a flush launch and
+        around the attention launch (dec_ev only where the step has separate launches)."""
         cfg, cc, ws, wsb, st = layer_args[i % N_LAYERS]
         j = i % 64
         if one_launch:
             b = decode_bytes(wl, after_append(wl, caches[i % N_LAYERS].lengths))
-            if ev is not None:
-                ev[0].record(stream)
             rc = lib.kvq_append_decode(cfg, cc, knp[j], vnp[j], qp[j], outp, ws, wsb, fusedr, sp)
-            if ev is not None:
-                ev[1].record(stream)
             if not fused.value:
                 raise RuntimeError("step %d was not one launch" % i)
         else:
             rc = lib.kvq_append_token(cfg, cc, knp[j], vnp[j], sp)
             b = decode_bytes_struct(wl, st)
-            if ev is not None:
+            ev = None
+            if dec_ev is not None:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 ev[0].record(stream)
             rc |= lib.kvq_decode_attn(cfg, cc, qp[j], outp, ws, wsb, sp)
             if ev is not None:
                 ev[1].record(stream)
+                dec_ev.append(ev)
+        full = st.n_kres == cap or st.n_vres == cap     # the flush below launches
+        ev = None
+        if full and fl_ev is not None:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(stream)
         rc |= lib.kvq_flush_group(cfg, cc, fkr, fvr, sp)
+        if ev is not None:
+            ev[1].record(stream)
+            fl_ev.append(ev)
         if rc:
             raise RuntimeError("libkvq call failed in step %d" % i)
         return b, fk.value + fv.value
@@ -581,54 +721,91 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # Timed regions of K steps, repeated until about min_seconds of device time (at least
+    # one region).  Only flush launches (rare) and, where a step has separate append and
+    # attention launches, the attention launch carry events inside a region: events between
+    # kernels would stop one decode launch from starting as the previous one drains.
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    total_bytes = 0
+    region_ms, region_bytes = [], []
+    flush_ms, dec_ms = [], []
     flushes = 0
+    done = 0
     clk = Clocks(local)
     clk.start()
     torch.cuda.synchronize()
     w0 = time.time()
-    t_start.record(stream)
-    for i in range(K):
-        b, f = step(args.warmup + i, evs[i])
-        total_bytes += b
-        flushes += f
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    reps = None
+    while True:
+        fl_ev, dec_ev = [], ([] if not one_launch else None)
+        nbytes = 0
+        t_start.record(stream)
+        for s in range(K):
+            b, f = step(args.warmup + done + s, fl_ev, dec_ev)
+            nbytes += b
+            flushes += f
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        done += K
+        region_ms.append(t_start.elapsed_time(t_end))
+        region_bytes.append(nbytes)
+        flush_ms.append(sum(a.elapsed_time(bb) for a, bb in fl_ev))
+        if dec_ev is not None:
+            dec_ms.extend(a.elapsed_time(bb) for a, bb in dec_ev)
+        del fl_ev, dec_ev
+        if reps is None:      # regions to run: enough for min_seconds, within the cache capacity
+            want = int(np.ceil(args.min_seconds * 1e3 / max(region_ms[0], 1e-3)))
+            reps = max(1, min(want, max_timed_steps // K))
+            if world > 1:
+                r = torch.tensor([reps], dtype=torch.int64, device=dev)
+                dist.all_reduce(r, op=dist.ReduceOp.MAX)
+                reps = int(r[0])
+        if len(region_ms) >= reps:
+            break
     w1 = time.time()
     clk.stop()
-    ms = t_start.elapsed_time(t_end)
-    dec_ms = [a.elapsed_time(bb) for a, bb in evs]
-    # tens of thousands of live events slow down later runtime calls on the host
-    # (one host-buffer step went from about 42 to 226 us of host time): free them
-    # before the end-to-end leg
-    del evs
+    ms = sum(region_ms)
+    total_bytes = sum(region_bytes)
+    steps_timed = K * len(region_ms)
     st = sum(c.read_status() for c in caches)
     if st != 0:
         print("device status %d" % st, file=sys.stderr)
-    launches = (1 if one_launch else 2) * K + flushes
+    launches = (1 if one_launch else 2) * steps_timed + flushes
     ms_max, bytes_all = reduce_over_ranks(ms, float(total_bytes), world, dev)
+    per_step = sorted(r / K for r in region_ms)
 
     # ---- end to end through host buffers: one kvq_decode_step_host call per step
-    # (copies in, append, attend, flush, copy out; pinned memory), then a stream sync ----
+    # (copies in, append, attend, flush, copy out; pinned memory), then a stream
+    # synchronize, through the C ABI with prepared arguments ----
     kn_h = torch.from_numpy(kn).pin_memory()
     vn_h = torch.from_numpy(vn).pin_memory()
     q_h = torch.from_numpy(qs).pin_memory()
     out_h = torch.empty((wl.B, wl.H_q, wl.D), dtype=torch.float16).pin_memory()
-    Ke = max(1, min(K, args.e2e_steps))
-    e_bytes = 0
+    hk = [ctypes.c_void_p(kn_h[j].data_ptr()) for j in range(64)]
+    hv = [ctypes.c_void_p(vn_h[j].data_ptr()) for j in range(64)]
+    hq = [ctypes.c_void_p(q_h[j].data_ptr()) for j in range(64)]
+    ho = ctypes.c_void_p(out_h.data_ptr())
+    io_args = [(ctypes.c_void_p(c.io.data_ptr()), c.io.numel()) for c in caches]
+    Ke = max(1, min(steps_timed, args.e2e_steps))
+    e_bytes, t_call, t_sync = 0, 0.0, 0.0
     for i in range(Ke + 3):
         if i == 3:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            e_bytes = 0
-        c = caches[i % N_LAYERS]
+            e_bytes, t_call, t_sync = 0, 0.0, 0.0
+        li = (args.warmup + done + i) % N_LAYERS
+        cfg, cc, ws, wsb, _ = layer_args[li]
+        io, iob = io_args[li]
         j = i % 64
-        e_bytes += decode_bytes(wl, after_append(wl, c.lengths))
-        c.step_host(q_h[j], kn_h[j], vn_h[j], out_h)
+        e_bytes += decode_bytes(wl, after_append(wl, caches[li].lengths))
+        a = time.perf_counter()
+        rc = lib.kvq_decode_step_host(cfg, cc, hq[j], hk[j], hv[j], ho, io, iob, ws, wsb, fkr, fvr, sp)
+        b = time.perf_counter()
         stream.synchronize()
+        t_call += b - a
+        t_sync += time.perf_counter() - b
+        if rc:
+            raise RuntimeError("kvq_decode_step_host failed: %d" % rc)
     e_dt = time.perf_counter() - t0
     h2d = (kn_h[0].numel() + vn_h[0].numel() + q_h[0].numel()) * 2
     d2h = out_h.numel() * 2
@@ -638,16 +815,19 @@ def main():
             dist.destroy_process_group()
         return 0
     peak, peak_kind = measured_peaks()
-    us_step = ms_max * 1e3 / K
     value = bytes_all / (ms_max * 1e-3) / 1e9
-    dec_avg_ms = statistics.mean(dec_ms)
-    dec_bytes = total_bytes / K
+    dec_bytes = total_bytes / steps_timed
+    if one_launch:      # the step's own launch, without the flushes
+        dec_avg_ms = (ms - sum(flush_ms)) / steps_timed
+    else:
+        dec_avg_ms = statistics.mean(dec_ms)
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = profiled_traffic(wl.name)
     line = {
         "metric": baseline["metric"], "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K,
-        "us_per_step": us_step, "hbm_frac_step": value / world / peak,
+        "steps": K, "warmup": args.warmup, "ms_per_step": statistics.median(per_step),
+        "ms_per_step_min": per_step[0], "ms_per_step_max": per_step[-1],
+        "us_per_step": statistics.median(per_step) * 1e3, "hbm_frac_step": value / world / peak,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded; shapes and outlier structure of the workload)",
         "config": {"workload": wl.name, "B": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv, "D": wl.D,
@@ -658,19 +838,24 @@ def main():
                    "l2": "%d layer caches rotated (%.0f MB each, %.2f GB > 2 x L2)" % (
                        N_LAYERS, dec_bytes / 1e6, N_LAYERS * dec_bytes / 1e9),
                    "parallelism": "independent replicas per GPU" if world > 1 else "single GPU"},
+        "timing": {"regions": len(region_ms), "steps_timed": steps_timed, "device_s": ms * 1e-3,
+                   "per_region": "K steps between two events; median / min / max of region time / K"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel", "us_per_launch": dec_avg_ms * 1e3,
-                     "algorithmic_bytes_per_launch": dec_bytes, "traffic": traffic},
+                     "algorithmic_bytes_per_launch": dec_bytes, "traffic": traffic,
+                     "launch_time": ("(timed regions - flush launches) / steps" if one_launch
+                                     else "mean of events around each attention launch")},
         "gpu_launches": launches,
         "clocks": clk.summary(w0, w1),
         "e2e": {"value": e_bytes / e_dt / 1e9 * world, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": e_dt / Ke * 1e6},
+                "d2h_bytes_per_step": d2h, "us_per_step": e_dt / Ke * 1e6,
+                "host_call_us": t_call / Ke * 1e6, "sync_wait_us": t_sync / Ke * 1e6},
     }
+    if not args.no_quant_pack and world == 1:
+        line["quant_pack"] = quant_pack_measure(kvq, dev, peak)
     if not args.no_cpu_baseline and world == 1:
-        v, dt, n, desc = cpu_oracle_rate(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

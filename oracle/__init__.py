@@ -496,12 +496,20 @@ class OracleCache:
         lib().kvq_or_seq_rows(ctypes.byref(s), _p(Kh), _p(Vh))
         return Kh, Vh
 
-    def attend(self, q: np.ndarray, units: Optional[Sequence] = None) -> np.ndarray:
-        """q fp16 [B,H_q,D] -> fp64 [B,H_q,D] (NaN for units not requested)."""
+    def attend(self, q: np.ndarray, units: Optional[Sequence] = None, threads: int = 1) -> np.ndarray:
+        """q fp16 [B,H_q,D] -> fp64 [B,H_q,D] (NaN for units not requested).  threads > 1
+        runs the (b, h_kv) units on a thread pool (each unit's arithmetic unchanged)."""
         g = self.H_q // self.H_kv
         out = np.full((self.B, self.H_q, self.D), np.nan)
         if units is None:
             units = [(b, h) for b in range(self.B) for h in range(self.H_kv)]
+        if threads > 1 and len(units) > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            with ThreadPoolExecutor(min(threads, len(units))) as ex:
+                parts = list(ex.map(lambda u: self.attend(q, [u]), units))
+            for (b, h), o in zip(units, parts):
+                out[b, h * g:(h + 1) * g] = o[b, h * g:(h + 1) * g]
+            return out
         for b, h in units:
             if self.nvfp4:
                 Kh, Vh = self._nvfp4_rows(b, h)

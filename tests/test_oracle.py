@@ -55,19 +55,33 @@ def test_f2h_matches_numpy_rne():
 # The quantizer of one group                                                   #
 # --------------------------------------------------------------------------- #
 
+def _slack(bits):
+    """Relative slack on half a step.  The code is rint(v) with v = fl32(fl32(x - mn) / s):
+    two fp32 roundings of a quotient below max_int (1 + 2^-11) (s is the fp16 rounding of
+    (mx - mn) / max_int, at most 2^-11 below it), so v is within max_int (1 + 2^-10) 2^-23
+    of the exact quotient, and x - (code s + mn) within s/2 (1 + max_int (1 + 2^-10) 2^-22)."""
+    return ((1 << bits) - 1) * (1 + 2.0 ** -10) * 2.0 ** -22
+
+
 def _err_bound_ok(x16, bits):
     s, mn, c = oracle.quant_group(x16, bits)
     xh = oracle.dequant(c, s, mn)
     x = x16.astype(np.float64)
     sf = float(s)
-    assert c.max(initial=0) <= (1 << bits) - 1
+    mi = (1 << bits) - 1
+    assert c.max(initial=0) <= mi
     if sf == 0.0:
         # zero scale: every code is 0, the error is at most the group's range
         assert not c.any()
         assert np.all(np.abs(x - xh) <= x.max() - x.min())
         return
-    if abs(sf) >= 2.0 ** -14:  # normal fp16 scale: half a step (+ fp32 rounding slack)
-        assert np.all(np.abs(x - xh) <= sf / 2 * (1 + 2.0 ** -16)), (x16, s, mn, c)
+    bound = sf / 2 * (1 + _slack(bits))
+    if abs(sf) < 2.0 ** -14:
+        # A subnormal scale is (mx - mn) / max_int rounded to a multiple of 2^-24: up to
+        # 2^-25 off, an unbounded fraction of the scale.  Values that clamp to the top code
+        # then sit up to max_int (2^-25 + 2^-24 s) above it; interior codes keep the bound.
+        bound += mi * (2.0 ** -25 + 2.0 ** -24 * sf)
+    assert np.all(np.abs(x - xh) <= bound), (x16, s, mn, c)
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
@@ -515,3 +529,31 @@ def test_mixed_widths_codes_and_attention(kb, vb, S):
         p = np.exp(z - z.max())
         ref = (p / p.sum()) @ Vf[0, hq // g]
         assert np.allclose(out[0, hq], ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_quant_error_bound_subnormal_scales(bits):
+    """Groups whose scale is an fp16 subnormal (ranges below max_int 2^-14): the interior
+    bound plus the clamp term of the rounded scale; the case is hit, not skipped."""
+    rng = np.random.default_rng(40 + bits)
+    hit = 0
+    for _ in range(2000):
+        n = int(rng.integers(2, 64))
+        span = 2.0 ** rng.uniform(-24, -14) * ((1 << bits) - 1)
+        base = float(rng.choice([0.0, 1.0, -3.5e-3, 2.0 ** -10]))
+        x = (base + rng.uniform(0, span, n)).astype(np.float16)
+        s, _, _ = oracle.quant_group(x, bits)
+        hit += 0.0 < float(s) < 2.0 ** -14
+        _err_bound_ok(x, bits)
+    assert hit > 100
+
+
+def test_oracle_attend_threads_equal_single_thread():
+    """The all-cores form of the oracle (units on a thread pool) gives the same numbers."""
+    import kvq_synth
+    wl = kvq_synth.WORKLOADS["llama3_8b_gqa_b2"].replace(B=2, H_q=8, H_kv=4, T=512)
+    K, V = kvq_synth.prefill_kv(wl, 512 + 70)
+    o = OracleCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, R=wl.R)
+    o.prefill(K, V)
+    q = kvq_synth.queries(wl, 1)[0]
+    assert np.array_equal(o.attend(q), o.attend(q, threads=4))
