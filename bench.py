@@ -408,6 +408,72 @@ def quant_pack_measure(kvq, dev, peak, reps: int = 5) -> dict:
     return outp
 
 
+def long_sequence_measure(kvq, dev, peak, reps: int = 3) -> dict:
+    """The long-context workload as a whole: kvq_quant_pack_k + _v over the 131072 + 64
+    token prefill, then 64 decode steps (kvq_append_decode + kvq_flush_group; the flush
+    fires on step 64).  CUDA events around the prefill and around the 64 steps; L2
+    scrubbed before each repetition; the median of `reps`."""
+    import ctypes
+    import torch
+    wl = kvq_synth.WORKLOADS["long_128k"]
+    L0 = wl.T + 64
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    del K, V
+    kn, vn = kvq_synth.decode_tokens(wl, 64)
+    qs = kvq_synth.queries(wl, 64)
+    kn_d, vn_d, q_d = (torch.from_numpy(a).to(dev) for a in (kn, vn, qs))
+    out = torch.empty((wl.B, wl.H_q, wl.D), dtype=torch.float16, device=dev)
+    c = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, R=wl.R, max_T=wl.T + 2 * wl.G, device=dev)
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    lib = kvq.lib
+    args = (ctypes.byref(c.cfg), ctypes.byref(c.c))
+    ws, wsb = ctypes.c_void_p(c.ws.data_ptr()), c.ws.numel()
+    fk, fv, fu = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    pre, seq, flush_at, step_bytes = [], [], [], 0
+    for r in range(reps + 1):
+        for name in ("n_sink", "T_k", "n_kres", "T_v", "n_vres", "n_local", "local_head"):
+            setattr(c.c, name, 0)
+        scrub.fill_(r & 255)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        c.prefill(Kd, Vd)
+        e[1].record(stream)
+        nbytes, fl = 0, []
+        for j in range(64):
+            nbytes += decode_bytes(wl, after_append(wl, c.lengths))
+            rc = lib.kvq_append_decode(*args, ctypes.c_void_p(kn_d[j].data_ptr()), ctypes.c_void_p(vn_d[j].data_ptr()),
+                                       ctypes.c_void_p(q_d[j].data_ptr()), ctypes.c_void_p(out.data_ptr()), ws, wsb,
+                                       ctypes.byref(fu), sp)
+            rc |= lib.kvq_flush_group(*args, ctypes.byref(fk), ctypes.byref(fv), sp)
+            if rc:
+                raise RuntimeError("long-context step %d failed: %d" % (j, rc))
+            if fk.value:
+                fl.append(j + 1)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        if r > 0:
+            pre.append(e[0].elapsed_time(e[1]))
+            seq.append(e[1].elapsed_time(e[2]))
+            flush_at, step_bytes = fl, nbytes
+    assert c.read_status() == 0
+    nb = quant_pack_bytes(wl, L0)
+    p_ms, s_ms = statistics.median(pre), statistics.median(seq)
+    res = {"workload": "long_128k: B=1, H_q=32, H_kv=8, D=128, prefill 131072 + 64 tokens, then 64 decode steps",
+           "timing": "median of %d sequences, CUDA events, L2 scrubbed before each" % reps,
+           "prefill_us": p_ms * 1e3, "prefill_bytes": nb["k"] + nb["v"],
+           "prefill_GBps": (nb["k"] + nb["v"]) / (p_ms * 1e-3) / 1e9,
+           "prefill_frac": (nb["k"] + nb["v"]) / (p_ms * 1e-3) / 1e9 / peak,
+           "steps_us": s_ms * 1e3, "us_per_step": s_ms * 1e3 / 64, "steps_bytes": step_bytes,
+           "steps_GBps": step_bytes / (s_ms * 1e-3) / 1e9, "flush_on_steps": flush_at,
+           "total_us": (p_ms + s_ms) * 1e3}
+    del Kd, Vd, c, scrub
+    torch.cuda.empty_cache()
+    return res
+
+
 def paged_bytes(wl, lens_host) -> int:
     """decode_bytes of a paged cache: the sum over active slots of each slot's bytes."""
     H, D, G = wl.H_kv, wl.D, wl.G
@@ -854,6 +920,8 @@ def main():
     }
     if not args.no_quant_pack and world == 1:
         line["quant_pack"] = quant_pack_measure(kvq, dev, peak)
+    if wl.name == "long_128k" and world == 1:
+        line["sequence"] = long_sequence_measure(kvq, dev, peak)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)

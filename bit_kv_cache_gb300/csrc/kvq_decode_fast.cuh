@@ -392,6 +392,17 @@ struct FastWarp {
     uint32_t pending = 0;  // bit s: slot s has copies in flight
     PageIds<PG> pid;       // page index of a logical page of sequence u
     const float *rt = nullptr;  // RP: the RoPE tables
+    // Dense caches: this lane's copy of a key batch and of a value batch (codes rows,
+    // the key (scale, min) row, Kitty planes) is at  base + (tile >> tpp_shift) * pstride
+    // + (tile & tiles-per-page - 1) * tstride  (bytes), set per sequence by set_copies();
+    // bytes == 0: no copy.  vm_base: the value (scale, min) rows of the sequence.
+    struct CopyLane {
+        const unsigned char *base;
+        uint32_t pstride, tstride, dst, bytes;
+    };
+    CopyLane ck{}, cv{};
+    const unsigned char *vm_base = nullptr;
+    uint32_t k_total = 0;  // bytes of a key batch (without the first batch's value meta)
 
     __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
         : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
@@ -416,9 +427,57 @@ struct FastWarp {
         return ok;
     }
 
+    // Per-lane copies of sequence u (dense caches).  Key batch: lanes 0..7 the code rows
+    // of the tile, lane 8 the page's (scale, min) row, Kitty lanes 10..17 the high-plane
+    // rows and lane 18 the boost index.  Value batch: lanes 0..V_ROWS-1 the code rows.
+    __device__ void set_copies() {
+        const int64_t pages = p.max_T / p.G, pg0 = (int64_t)u * pages;
+        const int tpp = 1 << p.tpp_shift;
+        const int nb = KITTY ? p.n_boost : 0;
+        const unsigned char *kc = reinterpret_cast<const unsigned char *>(p.k_codes);
+        ck = CopyLane{kc, 0, 0, 0, 0};
+        if (lane < 8) {
+            const uint32_t row = T::D * 4, page = (uint32_t)(p.G / CK::FPI) * row;
+            ck = CopyLane{kc + (size_t)pg0 * page + lane * row, page, 8 * row, (uint32_t)(T::OFF_K + lane * T::K_STRIDE),
+                          row};
+        } else if (lane == 8) {
+            ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_meta) + (size_t)pg0 * T::D * 4, T::D * 4, 0,
+                          (uint32_t)T::OFF_KM, T::D * 4};
+        } else if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
+            const uint32_t row = nb * 4, page = (uint32_t)(p.G / 16) * row;
+            ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_hi) + (size_t)pg0 * page + (lane - 10) * row,
+                          page, 8 * row, (uint32_t)(T::OFF_HI + (lane - 10) * hi_stride(nb)), row};
+        } else if (KITTY && lane == 18) {
+            ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_bidx) + (size_t)pg0 * T::D, T::D, 0,
+                          (uint32_t)(T::OFF_HI + 8 * hi_stride(nb)), T::D};
+        }
+        k_total = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0);
+        cv = CopyLane{nullptr, 0, 0, 0, 0};
+        if (lane < T::V_ROWS) {
+            const uint32_t row = (uint32_t)p.G * 4;
+            cv = CopyLane{reinterpret_cast<const unsigned char *>(p.v_codes) + ((size_t)pg0 * T::V_ROWS + lane) * row,
+                          T::V_ROWS * row, T::TOK * 4, (uint32_t)(lane * T::V_STRIDE), T::TOK * 4};
+        }
+        vm_base = reinterpret_cast<const unsigned char *>(p.v_meta) + (size_t)pg0 * p.G * 4;
+        (void)tpp;
+    }
+    __device__ __forceinline__ const unsigned char *copy_src(const CopyLane &c, int64_t ti) const {
+        return c.base + (size_t)(ti >> p.tpp_shift) * c.pstride + (size_t)(ti & ((1 << p.tpp_shift) - 1)) * c.tstride;
+    }
+
     // Batch K(j): key codes and (scale, min) of tile t0 + j -> key half j & 1, barrier
     // j & 1; the first batch also brings the value (scale, min) of tile t0.
     __device__ void issue_kb(int64_t t0, int j) {
+        if constexpr (!PG) {
+            const int s = j & 1;
+            const int64_t ti = t0 + j;
+            pending |= 1u << s;
+            if (lane == 0) mbar_arrive_expect_tx(&bars[s], k_total + (j == 0 ? T::TOK * 4 : 0));
+            __syncwarp();
+            if (ck.bytes) issue_copy(kslot(s) + ck.dst, copy_src(ck, ti), ck.bytes, &bars[s]);
+            if (j == 0 && lane == 9) issue_copy(vmslot(0), vm_base + (size_t)ti * T::TOK * 4, T::TOK * 4, &bars[s]);
+            return;
+        }
         const int s = j & 1;
         const int64_t ti = t0 + j;
         pending |= 1u << s;
@@ -450,6 +509,18 @@ struct FastWarp {
     // Batch V(j): value codes of tile t0 + j -> value half j & 1 and, if tile j + 1
     // exists, its value (scale, min) -> value-meta row (j + 1) & 1; barrier 2 + (j & 1).
     __device__ void issue_vb(int64_t t0, int j, int64_t n) {
+        if constexpr (!PG) {
+            const int s = 2 + (j & 1);
+            const int64_t ti = t0 + j;
+            const bool meta = j + 1 < n;
+            pending |= 1u << s;
+            if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
+            __syncwarp();
+            if (cv.bytes) issue_copy(vslot(j & 1) + cv.dst, copy_src(cv, ti), cv.bytes, &bars[s]);
+            if (meta && lane == T::V_ROWS % 32)
+                issue_copy(vmslot((j + 1) & 1), vm_base + (size_t)(ti + 1) * T::TOK * 4, T::TOK * 4, &bars[s]);
+            return;
+        }
         const int s = 2 + (j & 1);
         const int64_t ti = t0 + j;
         const bool meta = j + 1 < n;
@@ -849,6 +920,7 @@ struct FastWarp {
     __device__ void start(int uu, int64_t t0, int64_t t1) {
         u = uu;
         pid.set(p, uu);
+        if (!PG) set_copies();
         issue_kb(t0, 0);
         issue_vb(t0, 0, t1 - t0);
         if (t1 - t0 > 1) issue_kb(t0, 1);

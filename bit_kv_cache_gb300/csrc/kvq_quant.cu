@@ -79,12 +79,50 @@ __device__ __forceinline__ unsigned long long abs_units(uint32_t h) {
 constexpr uint32_t kMagicBits = 0x4B400000u;  // 1.5 * 2^23
 constexpr float kTieMargin = 0.5f - 0x1p-14f;
 
-__device__ __forceinline__ uint32_t qbits(float x, float mn, float inv, uint32_t lim, float &emax) {
-    const float r = __fmul_rn(__fsub_rn(x, mn), inv);
-    const float t = __fadd_rn(r, 12582912.0f);
-    emax = fmaxf(emax, fabsf(__fsub_rn(r, __fsub_rn(t, 12582912.0f))));
-    return min(__float_as_uint(t), lim);
+// fp32 pairs (Blackwell's f32x2 arithmetic): each lane of the pair rounds exactly as
+// the scalar operation, so the pair forms give the same bits, in half the instructions.
+__device__ __forceinline__ uint64_t pk2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
 }
+__device__ __forceinline__ float2 up2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// qbits for two elements at once: h is a half2 of two fp16 values whose groups have
+// (min, rcp(scale)) = mn2, inv2.  Returns the two clamped magic-biased codes; em
+// tracks the largest distance to a rounding tie.
+__device__ __forceinline__ void qbits2(uint32_t h, uint64_t mn2, uint64_t inv2, uint32_t lim, uint32_t &c0,
+                                       uint32_t &c1, float &em) {
+    const uint64_t mg2 = 0x4B4000004B400000ull;  // (1.5 * 2^23, 1.5 * 2^23)
+    const float2 f = unpack_half2(h);
+    const uint64_t r = mul_x2(sub_x2(pk2(f.x, f.y), mn2), inv2);
+    const uint64_t t = add_x2(r, mg2);
+    const float2 e = up2(sub_x2(r, sub_x2(t, mg2)));
+    em = fmaxf(em, fmaxf(fabsf(e.x), fabsf(e.y)));
+    const float2 tf = up2(t);
+    c0 = min(__float_as_uint(tf.x), lim);
+    c1 = min(__float_as_uint(tf.y), lim);
+}
+
 // 0x4B400000 * sum_{j < n} 2^(b j)  (mod 2^32): the offset a word of n codes picks up.
 __host__ __device__ constexpr uint32_t magic_sum(int b, int n) {
     uint32_t s = 0;
@@ -365,11 +403,13 @@ __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int6
         g.zero = g.s == 0.0f;
         uint32_t a = 0;
         float emax = 0.f;
+        const uint64_t mn2 = pk2(g.mn, g.mn), inv2 = pk2(g.inv, g.inv);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            const float2 f = unpack_half2((&x[i].x)[k]);
-            a += qbits(f.x, g.mn, g.inv, lim, emax) * (1u << (BITS * (2 * k)));
-            a += qbits(f.y, g.mn, g.inv, lim, emax) * (1u << (BITS * (2 * k + 1)));
+            uint32_t c0, c1;
+            qbits2((&x[i].x)[k], mn2, inv2, lim, c0, c1, emax);
+            a += c0 * (1u << (BITS * (2 * k)));
+            a += c1 * (1u << (BITS * (2 * k + 1)));
         }
         a -= magic_sum(BITS, 8);
         if (emax > kTieMargin) {  // near a half-integer in this piece: the exact path

@@ -192,7 +192,7 @@ def _full_state(name):
     if wl.mode == "kitty":
         L0 = wl.S + wl.T + wl.R + 127   # K Q-buffer 127 after prefill; one append fills it
     else:
-        L0 = wl.T + 64
+        L0 = wl.T + wl.R - 2            # the residual fills on the second step: one flush
     return wl, L0
 
 
@@ -243,4 +243,22 @@ def test_full_size_nvfp4_sampled():
     assert_state_equal(gpu, ora)
     run_steps(gpu, ora, wl, 2, DEV, units=[(0, 1), (3, 6)])
     run_steps(gpu, ora, wl, 2, DEV, units=[(0, 1), (3, 6)], fused=True)   # insert and attend in one call
+    assert gpu.read_status() == 0
+
+
+def test_long_context_sequence_full_size():
+    """The long-context workload as specified: kvq_quant_pack_k / _v over a 131072 + 64
+    token prefill (B=1, H_kv=8), then 64 steps of insert-and-attend and flush, the flush
+    firing on step 64.  Attention of two sampled sequences at steps 1, 32, 63 and 64;
+    every code, scale and min bit-exact after the flush."""
+    wl = WORKLOADS["long_128k"]
+    L0 = wl.T + 64
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    gpu, ora = make_pair(wl, max_T=wl.T + 2 * wl.G, device=DEV)
+    prefill_both(gpu, ora, K, V, DEV)
+    del K, V
+    assert gpu.lengths["n_kres"] == 64
+    run_steps(gpu, ora, wl, 64, DEV, check_every=31, units=[(0, 2), (0, 7)], fused=True)
+    assert gpu.lengths["T_k"] == wl.T + wl.G and gpu.lengths["n_kres"] == 0
+    assert_state_equal(gpu, ora)
     assert gpu.read_status() == 0
