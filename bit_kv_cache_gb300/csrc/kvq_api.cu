@@ -679,6 +679,18 @@ int kvq_read_status(const kvq_cache *k, void *ws, int32_t *dev_status, void *str
     return acc ? KVQ_ERR_DEVICE : KVQ_OK;
 }
 
+// The device address of page-locked host memory mapped into the current device's
+// address space, or null (pageable memory, device memory, or no such mapping).
+static const void *mapped_host(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+    return a.devicePointer;
+}
+
 // Staging layout of kvq_decode_step_host: q, k_new, v_new, out, each 256-byte aligned.
 static size_t step_io_part(size_t n) { return (n + 255) & ~(size_t)255; }
 
@@ -702,13 +714,32 @@ int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, c
     uint16_t *dv = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + step_io_part(nk));
     uint16_t *dout = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + 2 * step_io_part(nk));
     cudaStream_t st = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(dk, k_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
-        cudaMemcpyAsync(dv, v_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
-        cudaMemcpyAsync(dq, q, nq, cudaMemcpyDefault, st) != cudaSuccess)
+    // Page-locked host buffers mapped into the device's address space are read by one
+    // stage-in kernel and the attention output is written straight into `out`; other
+    // host memory goes through one cudaMemcpyAsync per buffer.
+    const void *mq = mapped_host(q), *mk = mapped_host(k_new), *mv = mapped_host(v_new);
+    void *mo = const_cast<void *>(mapped_host(out));
+    const bool direct = mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo);
+    if (direct) {
+        StageParams sp;
+        sp.src[0] = mq;
+        sp.src[1] = mk;
+        sp.src[2] = mv;
+        sp.dst[0] = dq;
+        sp.dst[1] = dk;
+        sp.dst[2] = dv;
+        sp.n[0] = (int64_t)nq;
+        sp.n[1] = sp.n[2] = (int64_t)nk;
+        if (launch_stage_in(sp, st) != cudaSuccess) return KVQ_ERR_CUDA;
+        dout = static_cast<uint16_t *>(mo);
+    } else if (cudaMemcpyAsync(dk, k_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
+               cudaMemcpyAsync(dv, v_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
+               cudaMemcpyAsync(dq, q, nq, cudaMemcpyDefault, st) != cudaSuccess) {
         return KVQ_ERR_CUDA;
+    }
     if ((e = kvq_append_decode(c, k, dk, dv, dq, dout, ws, ws_bytes, nullptr, stream))) return e;
     if ((e = kvq_flush_group(c, k, flushed_k, flushed_v, stream))) return e;
-    if (cudaMemcpyAsync(out, dout, nq, cudaMemcpyDefault, st) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (!direct && cudaMemcpyAsync(out, dout, nq, cudaMemcpyDefault, st) != cudaSuccess) return KVQ_ERR_CUDA;
     return KVQ_OK;
 }
 

@@ -352,85 +352,77 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
 }
 
 // ------------------------------------------------------------------------------
-// Values, D = Gv = 128: one CTA per 128 tokens.  Lane (c8, hb) of warp w loads
-// channels 8 c8 .. + 7 of tokens 16 w + 2 i + hb (i = 0..7): each load of a warp is
-// two contiguous rows.  A token's min / max reduces over its 16 lanes by shuffles;
-// lane i computes the group of the half-warp's token i and shares it; codes pack
-// along channels and are staged in shared memory so that each word row of the page
+// Values, D = Gv = 128: one CTA per 128 tokens, 16 tokens per warp.  Lane (tq, c) of
+// warp w holds tokens 16 w + 8 g + tq (g = 0, 1) and of each the 8-channel chunks
+// c, c + 4, c + 8, c + 12 (a warp load reads 64 contiguous bytes of 8 rows).  A
+// token's min / max reduces over its 4 lanes by two shuffles, and each of them forms
+// the token's group itself.  Codes pack along channels (2-bit words pair the chunks of
+// lanes c and c ^ 1) and are staged in shared memory, so that each word row of the page
 // leaves as contiguous 512-byte stores.
 // ------------------------------------------------------------------------------
 template <int BITS>
 __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int64_t tl0, const uint16_t *src) {
+    static_assert(BITS == 2 || BITS == 4, "2- or 4-bit values");
     constexpr int D = 128, FPI = 32 / BITS, NWORD = D / FPI;
     __shared__ __align__(16) uint32_t s_codes[NWORD][128];
     __shared__ __align__(16) uint32_t s_meta[128];
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, c8 = lane & 15, hb = lane >> 4;
-    uint4 x[8];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, tq = lane >> 2, c = lane & 3;
+    uint4 x[2][4];
 #pragma unroll
-    for (int i = 0; i < 8; i++) x[i] = reinterpret_cast<const uint4 *>(src + (size_t)(16 * w + 2 * i + hb) * D)[c8];
-    float smn = 0.f, smx = 0.f;  // min / max of the half-warp's token c8 & 7
+    for (int g = 0; g < 2; g++)
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        __half2 lo = *reinterpret_cast<const __half2 *>(&x[i].x), hi = lo;
+        for (int i = 0; i < 4; i++)
+            x[g][i] = reinterpret_cast<const uint4 *>(src + (size_t)(16 * w + 8 * g + tq) * D)[c + 4 * i];
+    constexpr uint32_t lim = kMagicBits + (1u << BITS) - 1;
 #pragma unroll
-        for (int k = 1; k < 4; k++) {
-            const uint32_t wk = (&x[i].x)[k];
-            const __half2 v = *reinterpret_cast<const __half2 *>(&wk);
-            lo = __hmin2(lo, v);
-            hi = __hmax2(hi, v);
-        }
+    for (int g = 0; g < 2; g++) {
+        const int tt = 16 * w + 8 * g + tq;
+        __half2 lo = *reinterpret_cast<const __half2 *>(&x[g][0].x), hi = lo;
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int k = (i == 0 ? 1 : 0); k < 4; k++) {
+                const uint32_t wk = (&x[g][i].x)[k];
+                const __half2 v = *reinterpret_cast<const __half2 *>(&wk);
+                lo = __hmin2(lo, v);
+                hi = __hmax2(hi, v);
+            }
         float a = fminf(__low2float(lo), __high2float(lo)), b = fmaxf(__low2float(hi), __high2float(hi));
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
+        for (int o = 1; o < 4; o <<= 1) {
             a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
             b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
         }
-        if ((c8 & 7) == i) smn = a, smx = b;
-    }
-    // lane c8 = i (< 8) of each half-warp forms the group of its token i
-    GroupQ mine = make_group(smn, smx, (1 << BITS) - 1);
-    if (c8 < 8) s_meta[16 * w + 2 * c8 + hb] = (uint32_t)mine.s16 | ((uint32_t)mine.mn16 << 16);
-    constexpr uint32_t lim = kMagicBits + (1u << BITS) - 1;
-    uint32_t part[8];
+        const GroupQ gr = make_group(a, b, (1 << BITS) - 1);
+        if (c == 0) s_meta[tt] = (uint32_t)gr.s16 | ((uint32_t)gr.mn16 << 16);
+        const uint64_t mn2 = pk2(gr.mn, gr.mn), inv2 = pk2(gr.inv, gr.inv);
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const int srcl = (lane & 16) | i;
-        GroupQ g;
-        g.mn = __shfl_sync(0xffffffffu, mine.mn, srcl);
-        g.inv = __shfl_sync(0xffffffffu, mine.inv, srcl);
-        g.s = __shfl_sync(0xffffffffu, mine.s, srcl);
-        g.maxf = (float)((1 << BITS) - 1);
-        g.zero = g.s == 0.0f;
-        uint32_t a = 0;
-        float emax = 0.f;
-        const uint64_t mn2 = pk2(g.mn, g.mn), inv2 = pk2(g.inv, g.inv);
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            uint32_t c0, c1;
-            qbits2((&x[i].x)[k], mn2, inv2, lim, c0, c1, emax);
-            a += c0 * (1u << (BITS * (2 * k)));
-            a += c1 * (1u << (BITS * (2 * k + 1)));
-        }
-        a -= magic_sum(BITS, 8);
-        if (emax > kTieMargin) {  // near a half-integer in this piece: the exact path
-            a = 0;
+        for (int i = 0; i < 4; i++) {  // chunk c + 4 i: channels 8 (c + 4 i) .. + 7
+            uint32_t part = 0;
+            float emax = 0.f;
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                const float2 f = unpack_half2((&x[i].x)[k]);
-                a |= quant_code(f.x, g) << (BITS * (2 * k));
-                a |= quant_code(f.y, g) << (BITS * (2 * k + 1));
+                uint32_t c0, c1;
+                qbits2((&x[g][i].x)[k], mn2, inv2, lim, c0, c1, emax);
+                part += c0 * (1u << (BITS * (2 * k)));
+                part += c1 * (1u << (BITS * (2 * k + 1)));
             }
-        }
-        part[i] = a;
-    }
+            part -= magic_sum(BITS, 8);
+            if (emax > kTieMargin) {  // near a half-integer in this chunk: the exact path
+                part = 0;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const int tt = 16 * w + 2 * i + hb;
-        if (BITS == 2) {  // 16 channels per word: lanes c8 and c8 ^ 1
-            const uint32_t nb = __shfl_xor_sync(0xffffffffu, part[i], 1);
-            if ((c8 & 1) == 0) s_codes[c8 >> 1][tt] = part[i] | (nb << 16);
-        } else {
-            s_codes[c8][tt] = part[i];
+                for (int k = 0; k < 4; k++) {
+                    const float2 f = unpack_half2((&x[g][i].x)[k]);
+                    part |= quant_code(f.x, gr) << (BITS * (2 * k));
+                    part |= quant_code(f.y, gr) << (BITS * (2 * k + 1));
+                }
+            }
+            if (BITS == 2) {  // 16 channels per word: chunks 2m (lane c even) and 2m + 1
+                const uint32_t nb = __shfl_xor_sync(0xffffffffu, part, 1);
+                if ((c & 1) == 0) s_codes[(c + 4 * i) >> 1][tt] = part | (nb << 16);
+            } else {
+                s_codes[c + 4 * i][tt] = part;
+            }
         }
     }
     __syncthreads();
@@ -757,6 +749,30 @@ cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st) {
 
 cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st) {
     set_lens_kernel<<<1, 1, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// Copies up to three 16-byte-aligned arrays (n[i] bytes, multiples of 16) from src[i]
+// to dst[i]; the sources may be page-locked host memory mapped into the device's
+// address space (kvq_decode_step_host), read over the host link.
+__global__ void stage_in_kernel(StageParams p) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t off = i;
+#pragma unroll
+    for (int a = 0; a < 3; a++) {
+        const int64_t n16 = p.n[a] / 16;
+        if (off < n16) {
+            reinterpret_cast<uint4 *>(p.dst[a])[off] = __ldcs(reinterpret_cast<const uint4 *>(p.src[a]) + off);
+            return;
+        }
+        off -= n16;
+    }
+}
+
+cudaError_t launch_stage_in(const StageParams &p, cudaStream_t st) {
+    const int64_t total = (p.n[0] + p.n[1] + p.n[2]) / 16;
+    if (total == 0) return cudaSuccess;
+    stage_in_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -233,21 +233,25 @@ int kvq_decode_attn(const kvq_config *cfg, const kvq_cache *cache, const uint16_
 size_t kvq_step_io_bytes(const kvq_config *cfg);
 
 /* One whole decode step from host memory: the three stages of the decode pipeline in
- * order (Kitty Sec. 4.3), with the copies in and out.
- *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) are copied
- *      into the device staging buffer io, one cudaMemcpyAsync each;
- *   2. kvq_append_decode (output into io), then kvq_flush_group;
- *   3. the attention output is copied into out (host fp16 [B][H_q][D]).
+ * order (Kitty Sec. 4.3), with the transfers in and out.
+ *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) are brought
+ *      into the device staging buffer io;
+ *   2. kvq_append_decode, then kvq_flush_group;
+ *   3. the attention output reaches out (host fp16 [B][H_q][D]).
+ * When all four host buffers are page-locked memory mapped into the device's address
+ * space (cudaHostAlloc / cudaHostRegister; with unified addressing every page-locked
+ * allocation is), one kernel reads the inputs over the host link into io and the
+ * attention kernel writes its output straight into out.  Otherwise there is one
+ * cudaMemcpyAsync per buffer in and out (asynchronous only for page-locked memory).
  * Everything is enqueued on `stream` and nothing is synchronized: out holds the result
  * once the stream has passed this point (cudaStreamSynchronize or an event), and the
- * host inputs must stay unchanged until then.  The copies are asynchronous only from
- * and to page-locked host memory.
+ * host inputs must stay unchanged until then.
  * io: device buffer of io_bytes >= kvq_step_io_bytes(cfg), 256-byte aligned, owned by
  * the caller (KVQ_ERR_WORKSPACE if too small); ws, ws_bytes as for kvq_decode_attn;
  * flushed_k, flushed_v as for kvq_flush_group.
  * Returns KVQ_OK or the status of the first stage that fails; the stages before it
  * have taken effect, as if called one by one (a refused append leaves the cache as it
- * was; only the copies into io were enqueued). */
+ * was; only the transfers into io were enqueued). */
 int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *q,
                          const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, void *io,
                          size_t io_bytes, void *ws, size_t ws_bytes, int *flushed_k,

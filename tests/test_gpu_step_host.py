@@ -1,12 +1,14 @@
 """kvq_decode_step_host (one decode step from host buffers: copies in, append,
-attend, flush, copy out) against the same steps through the device-buffer calls,
-over steps that cross a flush of the residual."""
+attend, flush, copy out) against the same steps through the device-buffer calls (bit
+for bit: decode is deterministic) and against the CPU oracle, over steps that cross a
+flush of the residual."""
 import numpy as np
 import pytest
 
 import kvq_synth
 from kvq_synth import WORKLOADS
-from parity_util import TOL_ABS, TOL_REL, to_dev
+import oracle
+from parity_util import assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +46,9 @@ def test_host_step_matches_device_steps(kvq, name):
     kn, vn = kvq_synth.decode_tokens(wl, STEPS)
     qs = kvq_synth.queries(wl, STEPS, replica=3)
     dev, host = _cache(kvq, wl, K, V), _cache(kvq, wl, K, V)
+    ora = oracle.OracleCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
+                             n_boost=wl.n_boost, mode=wl.mode)
+    ora.prefill(K, V)
     flushes = 0
     for i in range(STEPS):
         dev.append_token(to_dev(kn[i], DEV), to_dev(vn[i], DEV))
@@ -55,10 +60,11 @@ def test_host_step_matches_device_steps(kvq, name):
         torch.cuda.synchronize()
         assert fh == fd
         flushes += fd[0] or fd[1]
-        a = out.numpy().astype(np.float64)
-        r = ref.cpu().numpy().astype(np.float64)
-        err = np.abs(a - r)
-        assert np.isfinite(a).all() and (err <= TOL_ABS + TOL_REL * np.abs(r)).all(), float(err.max())
+        a = out.numpy()
+        assert np.array_equal(a.view(np.uint16), ref.cpu().numpy().view(np.uint16))
+        ora.append(kn[i], vn[i])
+        assert_close(a, ora.attend(qs[i]), what="host step %d" % i)
+        assert ora.flush() == fh
         assert host.lengths == dev.lengths
     assert flushes >= 1
     for name_ in host.buf:                                # packed state and buffers: bit-exact
