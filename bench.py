@@ -94,6 +94,24 @@ def after_append(wl, lengths) -> dict:
     return n
 
 
+def replay_steps(wl, states, first, K, cap) -> int:
+    """Algorithmic bytes of steps first .. first + K - 1 of the one-launch loop (step s
+    appends to and attends over layer s % N_LAYERS, then flushes a full residual),
+    replayed on host copies of the lengths; `states` (one dict per layer) advances.
+    KIVI caches only: a flush packs the cap residual tokens of keys and values."""
+    total = 0
+    for s in range(first, first + K):
+        li = s % N_LAYERS
+        st = after_append(wl, states[li])
+        total += decode_bytes(wl, st)
+        if st["n_kres"] == cap or st["n_vres"] == cap:
+            st["T_k"] += st["n_kres"]
+            st["T_v"] += st["n_vres"]
+            st["n_kres"] = st["n_vres"] = 0
+        states[li] = st
+    return total
+
+
 def decode_bytes_struct(wl, st) -> int:
     """decode_bytes for the lengths held in a kvq_cache struct."""
     return decode_bytes(wl, {"T_k": st.T_k, "T_v": st.T_v, "n_sink": st.n_sink, "n_kres": st.n_kres,
@@ -748,6 +766,28 @@ def main():
     fusedr = ctypes.byref(fused)
     cap = wl.G if wl.mode == "kitty" else wl.R
 
+    f_ad, f_fl = lib.kvq_append_decode, lib.kvq_flush_group
+
+    def step_one(i, fl_ev):
+        """One-launch step with nothing but the two C-ABI calls (and events around a
+        flush launch): the host stays ahead of the device.  Bytes: replay_steps."""
+        cfg, cc, ws, wsb, st = layer_args[i % N_LAYERS]
+        j = i & 63
+        rc = f_ad(cfg, cc, knp[j], vnp[j], qp[j], outp, ws, wsb, fusedr, sp)
+        if not fused.value:
+            raise RuntimeError("step %d was not one launch" % i)
+        if st.n_kres == cap:    # the flush below launches
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(stream)
+            rc |= f_fl(cfg, cc, fkr, fvr, sp)
+            ev[1].record(stream)
+            fl_ev.append(ev)
+        else:
+            rc |= f_fl(cfg, cc, fkr, fvr, sp)
+        if rc:
+            raise RuntimeError("libkvq call failed in step %d" % i)
+        return fk.value + fv.value
+
     def step(i, fl_ev=None, dec_ev=None):
         """One step; fl_ev / dec_ev (lists) receive event pairs around a flush launch and
         around the attention launch (dec_ev only where the step has separate launches)."""
@@ -802,15 +842,24 @@ def main():
     torch.cuda.synchronize()
     w0 = time.time()
     reps = None
+    states = [dict(c.lengths) for c in caches] if one_launch else None
     while True:
         fl_ev, dec_ev = [], ([] if not one_launch else None)
         nbytes = 0
-        t_start.record(stream)
-        for s in range(K):
-            b, f = step(args.warmup + done + s, fl_ev, dec_ev)
-            nbytes += b
-            flushes += f
-        t_end.record(stream)
+        s0 = args.warmup + done
+        if one_launch:
+            t_start.record(stream)
+            for s in range(s0, s0 + K):
+                flushes += step_one(s, fl_ev)
+            t_end.record(stream)
+            nbytes = replay_steps(wl, states, s0, K, cap)
+        else:
+            t_start.record(stream)
+            for s in range(K):
+                b, f = step(s0 + s, fl_ev, dec_ev)
+                nbytes += b
+                flushes += f
+            t_end.record(stream)
         torch.cuda.synchronize()
         done += K
         region_ms.append(t_start.elapsed_time(t_end))
@@ -830,6 +879,10 @@ def main():
             break
     w1 = time.time()
     clk.stop()
+    if one_launch:      # the replayed lengths are the caches' own
+        for c, st in zip(caches, states):
+            if dict(c.lengths) != st:
+                raise RuntimeError("replayed lengths %s differ from the cache's %s" % (st, c.lengths))
     ms = sum(region_ms)
     total_bytes = sum(region_bytes)
     steps_timed = K * len(region_ms)

@@ -112,6 +112,13 @@ def _check(code: int, what: str):
         raise KvqError(code, what)
 
 
+def v_tile_tokens(cfg) -> int:
+    """Tokens per value tile of a page (the library's value pages are tile-major): 256 /
+    key bits when that divides G, else G."""
+    t = 256 // (2 if cfg.mode == KVQ_MODE_KITTY else cfg.bits)
+    return t if cfg.G % t == 0 else cfg.G
+
+
 def make_config(B, H_q, H_kv, D, G, bits, S=0, R=None, n_boost=0, mode="kivi", max_T=0,
                 v_bits=0, rope_base=0.0) -> Config:
     """rope_base > 0: keys are stored before RoPE and rotated in decode attention."""
@@ -295,8 +302,9 @@ class KVQCache:
             return b[: U * (T // G) * D].view(cfg.B, cfg.H_kv, T // G, D)
         if name == "k_meta":
             return b.view(torch.float16).view(cfg.B, cfg.H_kv, T // G, D, 2)
-        if name == "v_codes":
-            return b.view(torch.int32).view(cfg.B, cfg.H_kv, T // G, D // vfpi, G)
+        if name == "v_codes":  # tile-major pages: [G / TV][D / fpi rows][TV words]
+            TV = v_tile_tokens(cfg)
+            return b.view(torch.int32).view(cfg.B, cfg.H_kv, T // G, G // TV, D // vfpi, TV)
         if name == "v_meta":
             return b.view(torch.float16).view(cfg.B, cfg.H_kv, T, D // Gv, 2)
         rows = {"k_sink": cfg.S, "v_sink": cfg.S, "k_res": G if kitty else cfg.R,
@@ -430,8 +438,9 @@ class KVQPagedCache:
             return b.view(torch.int32).view(P, H, G // kfpi, D)
         if name == "k_meta":
             return b.view(torch.float16).view(P, H, D, 2)
-        if name == "v_codes":
-            return b.view(torch.int32).view(P, H, D // vfpi, G)
+        if name == "v_codes":  # tile-major pages: [G / TV][D / fpi rows][TV words]
+            TV = v_tile_tokens(cfg)
+            return b.view(torch.int32).view(P, H, G // TV, D // vfpi, TV)
         if name == "v_meta":
             return b.view(torch.float16).view(P, H, G, D // Gv, 2)
         rows = {"k_sink": cfg.S, "v_sink": cfg.S, "k_res": cfg.R, "v_res": cfg.R}[name]

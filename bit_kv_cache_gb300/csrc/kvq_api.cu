@@ -124,6 +124,7 @@ QuantVParams qv_params(const kvq_config *c, kvq_cache *k) {
     p.D = c->D;
     p.G = c->G;
     p.Gv = gv_of(c);
+    p.TV = vtile_of(c);
     p.v_codes = k->v_codes;
     p.v_meta = k->v_meta;
     p.status = k->status;
@@ -615,6 +616,7 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
     p.bits = c->bits;
     p.vbits = vbits_of(c);
     p.Gv = gv_of(c);
+    p.v_tile = vtile_of(c);
     p.n_boost = kitty(c) ? c->n_boost : 0;
     p.kitty = kitty(c) ? 1 : 0;
     p.S_cap = c->S;

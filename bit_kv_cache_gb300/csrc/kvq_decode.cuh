@@ -102,13 +102,15 @@ __device__ __forceinline__ void load_k8(const DecodeParams &p, int u, int64_t tl
     if (tk < p.T_k) {
         const int kb = p.kitty ? 2 : p.bits, fpi = 32 / kb;
         const int64_t page = tk / p.G;
-        const int32_t *wp = p.k_codes + ((size_t)u * (p.max_T / fpi) + tk / fpi) * D + d;
+        // word row tk / fpi, row (tk % G) / fpi of its page: channel c at kword_pos(c, row)
+        const int32_t *wp = p.k_codes + ((size_t)u * (p.max_T / fpi) + tk / fpi) * D;
+        const int kr = (int)((tk % p.G) / fpi);
         const uint32_t *mp = reinterpret_cast<const uint32_t *>(p.k_meta) +
                              ((size_t)u * (p.max_T / p.G) + page) * D + d;
         const int sh = kb * (int)(tk % fpi);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            uint32_t code = ((uint32_t)wp[i] >> sh) & ((1u << kb) - 1);
+            uint32_t code = ((uint32_t)wp[kword_pos(d + i, kr)] >> sh) & ((1u << kb) - 1);
             if (p.kitty && p.n_boost) {
                 int slot = p.k_bidx[((size_t)u * (p.max_T / p.G) + page) * D + d + i];
                 if (slot < p.n_boost) {
@@ -158,12 +160,16 @@ __device__ __forceinline__ void load_v(const DecodeParams &p, int u, int64_t tl,
             return;
         }
         if (tv < p.T_v) {
-            const int fpi = 32 / p.vbits;
+            const int fpi = 32 / p.vbits, TV = p.v_tile;
             const int64_t page = tv / p.G, tin = tv % p.G;
+            // the value tile of token tin within the page, position vword_pos there
+            const int32_t *vt = p.v_codes + ((size_t)u * (p.max_T / p.G) + page) * (size_t)(D / fpi) * p.G +
+                                (size_t)(tin / TV) * (D / fpi) * TV;
+            const int j = (int)(tin % TV);
 #pragma unroll
             for (int i = 0; i < DPL; i++) {
                 const int dd = d + i;
-                uint32_t w = (uint32_t)p.v_codes[(((size_t)u * (p.max_T / p.G) + page) * (D / fpi) + dd / fpi) * p.G + tin];
+                uint32_t w = (uint32_t)vt[(dd / fpi) * TV + vword_pos(j, dd / fpi, TV)];
                 uint32_t code = (w >> (p.vbits * (dd % fpi))) & ((1u << p.vbits) - 1);
                 float2 sm = unpack_half2(reinterpret_cast<const uint32_t *>(p.v_meta)[((size_t)u * p.max_T + tv) * (D / p.Gv) + dd / p.Gv]);
                 vv[i] = (float)code * sm.x + sm.y;

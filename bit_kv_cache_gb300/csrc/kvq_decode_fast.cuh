@@ -66,9 +66,9 @@ struct Tile {
     static constexpr int TOK = 8 * K::FPI;                  // 128, 64 or 32 tokens
     static constexpr int P = KB == 2 ? 8 : 4;
     static constexpr bool P_ADJ = K::FPI / 2 == P;          // a lane's two p' values are adjacent
-    static constexpr int K_STRIDE = D * 4 + 16;             // padded key row: conflict-free ldmatrix
+    static constexpr int K_STRIDE = D * 4;                  // key word row (chunks in kword_pos order)
     static constexpr int V_ROWS = D / V::FPI;               // value channel blocks: 8, 16 or 32
-    static constexpr int V_STRIDE = TOK * 4 + 16;
+    static constexpr int V_STRIDE = TOK * 4;                // value word row (chunks in vword_pos order)
     static constexpr int NSET = V_ROWS / 8;                 // 1, 2 or 4 sets of 8 word rows
     static constexpr int TSLABS = TOK / 16;                 // 16-token slabs for PV
     static constexpr int PV_STEPS = TSLABS * NSET;          // one ldmatrix + split each
@@ -88,6 +88,8 @@ constexpr int kMiniRow = 128 * 2 + 16;                 // padded fp16 row of the
 constexpr int kMiniHalf = 16 * kMiniRow;               // 16 fp16 rows
 
 __host__ __device__ constexpr int round128(int x) { return (x + 127) & ~127; }
+// The NVFP4 tiles' four stages (F4Warp) live in the 4-bit tile region.
+constexpr int kF4Region = 2 * 4736 + 2 * 4608;
 
 // Per-warp shared memory (fast and mini warps share one layout):
 //   [tile region][p' buffer x2][q fp16 [4][128]][q' pairs [4 heads][8 slabs][4 lanes] x 8 B]
@@ -102,9 +104,9 @@ struct WarpSmem {
     // kb, vb: key and value code widths of the tile (2, 4 or 8)
     __host__ __device__ constexpr WarpSmem(int kb, int vb, bool kitty, int nb) {
         const int D = 128, tok = 256 / kb, v_rows = D * vb / 32;
-        const int off_hi = 8 * (D * 4 + 16) + D * 4, pbuf1 = 4 * (tok + 8) * 2;
+        const int off_hi = 8 * D * 4 + D * 4, pbuf1 = 4 * (tok + 8) * 2;
         ksz = round128(off_hi + (kitty ? 8 * hi_stride(nb) + D : 0));
-        vsz = round128(v_rows * (tok * 4 + 16));
+        vsz = round128(v_rows * tok * 4);
         vmsz = round128(tok * 4);
         const int mk = 1024 + ((4 * nb + 15) & ~15) + 128;  // mini packed-key block
         mslot = round128(kMiniHalf > mk ? kMiniHalf : mk);
@@ -113,6 +115,7 @@ struct WarpSmem {
         vm0 = v0 + 2 * vsz;
         region = vm0 + 2 * vmsz;
         if (region < kSlots * mslot) region = kSlots * mslot;
+        if (kb == 4 && vb == 4 && !kitty && region < kF4Region) region = kF4Region;
         pbuf = region;
         qraw = pbuf + 2 * pbuf1;
         qpair = qraw + 4 * 128 * 2;
@@ -403,11 +406,18 @@ struct FastWarp {
     CopyLane ck{}, cv{};
     const unsigned char *vm_base = nullptr;
     uint32_t k_total = 0;  // bytes of a key batch (without the first batch's value meta)
+    // ldmatrix: the lane addresses row r = lane & 7 of a row set at logical 16-byte chunk
+    // 4 sl + lane / 8 of slab sl, stored at chunk (4 sl + lane / 8) ^ r (kword_pos /
+    // vword_pos): 128 (sl / 2) bytes + cx[sl & 1].
+    uint32_t cx[2];
 
     __device__ FastWarp(const DecodeParams &pp, unsigned char *wb)
         : p(pp), wbase(wb), L(KB, VB, KITTY, pp.n_boost), u(0), lane(threadIdx.x & 31) {
         bars = reinterpret_cast<uint64_t *>(wbase + L.bars);
+        cx[0] = 16u * (uint32_t)((lane >> 3) ^ (lane & 7));
+        cx[1] = 16u * (uint32_t)((4 + (lane >> 3)) ^ (lane & 7));
     }
+    __device__ __forceinline__ uint32_t chunk(int sl) const { return 128u * (uint32_t)(sl >> 1) + cx[sl & 1]; }
     __device__ unsigned char *kslot(int s) const { return wbase + L.k0 + s * L.ksz; }
     __device__ unsigned char *vslot(int s) const { return wbase + L.v0 + s * L.vsz; }
     __device__ unsigned char *vmslot(int s) const { return wbase + L.vm0 + s * L.vmsz; }
@@ -427,19 +437,19 @@ struct FastWarp {
         return ok;
     }
 
-    // Per-lane copies of sequence u (dense caches).  Key batch: lanes 0..7 the code rows
-    // of the tile, lane 8 the page's (scale, min) row, Kitty lanes 10..17 the high-plane
-    // rows and lane 18 the boost index.  Value batch: lanes 0..V_ROWS-1 the code rows.
+    // Per-lane copies of sequence u (dense caches).  Key batch: lane 0 the tile's eight
+    // code rows (one contiguous block of the page), lane 8 the page's (scale, min) row,
+    // Kitty lanes 10..17 the high-plane rows and lane 18 the boost index.  Value batch:
+    // lane 0 the tile's code rows (one contiguous block of the tile-major page).
     __device__ void set_copies() {
         const int64_t pages = p.max_T / p.G, pg0 = (int64_t)u * pages;
         const int tpp = 1 << p.tpp_shift;
         const int nb = KITTY ? p.n_boost : 0;
         const unsigned char *kc = reinterpret_cast<const unsigned char *>(p.k_codes);
         ck = CopyLane{kc, 0, 0, 0, 0};
-        if (lane < 8) {
+        if (lane == 0) {
             const uint32_t row = T::D * 4, page = (uint32_t)(p.G / CK::FPI) * row;
-            ck = CopyLane{kc + (size_t)pg0 * page + lane * row, page, 8 * row, (uint32_t)(T::OFF_K + lane * T::K_STRIDE),
-                          row};
+            ck = CopyLane{kc + (size_t)pg0 * page, page, 8 * row, (uint32_t)T::OFF_K, 8 * row};
         } else if (lane == 8) {
             ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_meta) + (size_t)pg0 * T::D * 4, T::D * 4, 0,
                           (uint32_t)T::OFF_KM, T::D * 4};
@@ -453,10 +463,9 @@ struct FastWarp {
         }
         k_total = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0);
         cv = CopyLane{nullptr, 0, 0, 0, 0};
-        if (lane < T::V_ROWS) {
-            const uint32_t row = (uint32_t)p.G * 4;
-            cv = CopyLane{reinterpret_cast<const unsigned char *>(p.v_codes) + ((size_t)pg0 * T::V_ROWS + lane) * row,
-                          T::V_ROWS * row, T::TOK * 4, (uint32_t)(lane * T::V_STRIDE), T::TOK * 4};
+        if (lane == 0) {
+            const uint32_t page = (uint32_t)T::V_ROWS * p.G * 4, tile = T::V_ROWS * T::TOK * 4;
+            cv = CopyLane{reinterpret_cast<const unsigned char *>(p.v_codes) + (size_t)pg0 * page, page, tile, 0u, tile};
         }
         vm_base = reinterpret_cast<const unsigned char *>(p.v_meta) + (size_t)pg0 * p.G * 4;
         (void)tpp;
@@ -489,9 +498,9 @@ struct FastWarp {
         // tiles per page: a power of two; pg: page index, tin: tile within the page
         const int64_t pg = pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
         const int i = lane;
-        if (i < 8) {
-            issue_copy(st + T::OFF_K + i * T::K_STRIDE,
-                       p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8 + i) * T::D, T::D * 4, &bars[s]);
+        if (i == 0) {
+            issue_copy(st + T::OFF_K, p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8) * T::D, 8 * T::D * 4,
+                       &bars[s]);
         } else if (i == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &bars[s]);
         } else if (i == 9) {
@@ -517,7 +526,7 @@ struct FastWarp {
             if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
             __syncwarp();
             if (cv.bytes) issue_copy(vslot(j & 1) + cv.dst, copy_src(cv, ti), cv.bytes, &bars[s]);
-            if (meta && lane == T::V_ROWS % 32)
+            if (meta && lane == 1)
                 issue_copy(vmslot((j + 1) & 1), vm_base + (size_t)(ti + 1) * T::TOK * 4, T::TOK * 4, &bars[s]);
             return;
         }
@@ -529,14 +538,14 @@ struct FastWarp {
         if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
         __syncwarp();
         const int tmask = (1 << p.tpp_shift) - 1;
-        const int64_t pg = pid(p, ti >> p.tpp_shift), off = (ti & tmask) * T::TOK;
+        const int64_t pg = pid(p, ti >> p.tpp_shift), tin = ti & tmask;
         const int64_t pg1 = meta ? pid(p, (ti + 1) >> p.tpp_shift) : 0, off1 = ((ti + 1) & tmask) * T::TOK;
         const int i = lane;
-        if (i < T::V_ROWS) {
-            issue_copy(st + i * T::V_STRIDE, p.v_codes + ((size_t)pg * T::V_ROWS + i) * p.G + off, T::TOK * 4,
+        if (i == 0) {  // the tile's value rows: one block of the tile-major page
+            issue_copy(st, p.v_codes + ((size_t)pg * p.G + tin * T::TOK) * T::V_ROWS, T::V_ROWS * T::TOK * 4,
                        &bars[s]);
         }
-        if (i == T::V_ROWS % 32 && meta) {  // 8-bit values: every lane has a row, lane 0 also the meta
+        if (i == 1 && meta) {
             issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)pg1 * p.G + off1) * 2, T::TOK * 4, &bars[s]);
         }
     }
@@ -637,7 +646,7 @@ struct FastWarp {
         if (sl == 0) mma_16816_z(cm, am0, am0, am1, am1, c0, c1);
         else mma_16816(cm, am0, am0, am1, am1, c0, c1);
         uint32_t w[4], x[4], xs[4];
-        ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + 16 * (lane >> 3) + 64 * sl);
+        ldmatrix_x4(w, smem_u32(st + T::OFF_K) + (lane & 7) * T::K_STRIDE + chunk(sl));
         split<CK>(w, x, xs);
         if (sl == 0) mma_sets<true>(acc, x, xs, b0, b1);
         else mma_sets<false>(acc, x, xs, b0, b1);
@@ -691,7 +700,7 @@ struct FastWarp {
         uint2 bp = make_uint2(0u, 0u);
         if (gq < 4) bp = *reinterpret_cast<const uint2 *>(pb + gq * T::PROW + 16 * sl + 4 * t);
         uint32_t w[4], x[4], xs[4];
-        ldmatrix_x4(w, smem_u32(st) + (set * 8 + (lane & 7)) * T::V_STRIDE + 16 * (lane >> 3) + 64 * sl);
+        ldmatrix_x4(w, smem_u32(st) + (set * 8 + (lane & 7)) * T::V_STRIDE + chunk(sl));
         split<CV>(w, x, xs);
         mma_sets_o(O, set, x, xs, bp.x, bp.y);
     }
@@ -777,7 +786,9 @@ struct FastWarp {
         for (int ii = 0; ii < 2; ii++) {
             if (ii >= n) break;
             const int pr = t + 4 * (i0 + ii);
-            const uint2 w = *reinterpret_cast<const uint2 *>(st + T::OFF_K + gq * T::K_STRIDE + 8 * pr);
+            // words 2 pr, 2 pr + 1 of row gq: chunk pr / 2, stored at chunk (pr / 2) ^ gq
+            const uint2 w = *reinterpret_cast<const uint2 *>(st + T::OFF_K + gq * T::K_STRIDE +
+                                                             16 * ((pr >> 1) ^ gq) + 8 * (pr & 1));
             const uint2 km = *reinterpret_cast<const uint2 *>(st + T::OFF_KM + 8 * pr);
             const float2 sa = unpack_half2(km.x), sb = unpack_half2(km.y);  // (scale, min)
             const uint64_t SA = f2(sa.x, sa.x), MA = f2(sa.y, sa.y), SB = f2(sb.x, sb.x), MB = f2(sb.y, sb.y);
@@ -1114,9 +1125,8 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
         if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], bytes);
         __syncwarp();
         const int64_t pg = this->pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
-        if (lane < 8) {
-            issue_copy(st + T::OFF_K + lane * T::K_STRIDE,
-                       p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8 + lane) * T::D, T::D * 4,
+        if (lane == 0) {
+            issue_copy(st + T::OFF_K, p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8) * T::D, 8 * T::D * 4,
                        &this->bars[s]);
         } else if (lane == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &this->bars[s]);
@@ -1141,10 +1151,10 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
         unsigned char *st = this->vslot(j & 1);
         if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], T::V_ROWS * T::TOK * 4);
         __syncwarp();
-        const int64_t pg = this->pid(p, ti >> p.tpp_shift), off = (ti & ((1 << p.tpp_shift) - 1)) * T::TOK;
-        if (lane < T::V_ROWS)
-            issue_copy(st + lane * T::V_STRIDE, p.v_codes + ((size_t)pg * T::V_ROWS + lane) * p.G + off,
-                       T::TOK * 4, &this->bars[s]);
+        const int64_t pg = this->pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
+        if (lane == 0)  // the tile's value rows: one block of the tile-major page
+            issue_copy(st, p.v_codes + ((size_t)pg * p.G + tin * T::TOK) * T::V_ROWS, T::V_ROWS * T::TOK * 4,
+                       &this->bars[s]);
     }
 
     __device__ void drain(uint32_t mask) {  // copies still in flight land before smem reuse
@@ -1293,9 +1303,10 @@ struct F4Warp {
     static constexpr int K_CODES = 0, K_SCALES = 4096, K_HDR = 4608, V_HDR = 4624, K_STAGE = 4736;
     static constexpr int V_CODES = 0, V_SCALES = 4096, V_STAGE = 4608;
     static constexpr int PROW = TOK + 8;  // p' row (halves), padded
+    static_assert(2 * K_STAGE + 2 * V_STAGE <= kF4Region, "the stages fit the 4-bit tile region");
     const DecodeParams &p;
     unsigned char *wbase;
-    WarpSmem L;  // the 4-bit tile layout: the stages below fit its tile region exactly
+    WarpSmem L;  // the 4-bit tile layout: its tile region holds the stages below (kF4Region)
     int u, lane;
     uint64_t *bars;
     uint32_t phase = 0, pending = 0;
@@ -1762,6 +1773,9 @@ struct MiniWarp {
                 // Kitty mixed block: 16 tokens of packed keys, rows g / g+8 <-> tokens g / g+8
                 const uint32_t *w = reinterpret_cast<const uint32_t *>(sK + MB_W);
                 const uint32_t *km = reinterpret_cast<const uint32_t *>(sK + MB_M);
+                // the block is word row (tok0 - n_sink) / 16 of the cache, row rb of its
+                // 8-row group: logical chunk c of the row is stored at chunk c ^ rb
+                const int rb = (int)(((mt.tok0 - sq.n_sink) >> 4) & 7);
                 const uint2 *qpair = reinterpret_cast<const uint2 *>(wbase + L.qpair);
 #pragma unroll
                 for (int sl = 0; sl < 8; sl++) {
@@ -1771,7 +1785,7 @@ struct MiniWarp {
                     mma_16816(cm, b.am0, b.am0, b.am1, b.am1, b.c0, b.c1);
                     uint32_t wv[4], x[4], xs[4];
 #pragma unroll
-                    for (int kk = 0; kk < 4; kk++) wv[kk] = w[16 * sl + 4 * kk + t];
+                    for (int kk = 0; kk < 4; kk++) wv[kk] = w[4 * ((4 * sl + kk) ^ rb) + t];
                     FastWarp<2, 2, KITTY, false, false>::template split<Codes<2>>(wv, x, xs);
                     uint32_t a[4];
 #pragma unroll

@@ -8,6 +8,7 @@
 #include <algorithm>
 
 #include "kvq.h"
+#include "kvq_internal.h"
 
 namespace kvq {
 namespace host {
@@ -20,6 +21,8 @@ inline int vbits_of(const kvq_config *c) { return c->v_bits ? c->v_bits : c->bit
 inline int kfpi(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY ? 16 : 32 / c->bits; }
 inline int vfpi(const kvq_config *c) { return 32 / vbits_of(c); }
 inline int gv_of(const kvq_config *c) { return std::min(c->G, c->D); }
+// tokens per value tile of a page (the in-page value arrangement, kvq_internal.h)
+inline int vtile_of(const kvq_config *c) { return v_tile_tokens(c->mode == KVQ_MODE_KITTY ? 2 : c->bits, c->G); }
 inline bool kitty(const kvq_config *c) { return c->mode == KVQ_MODE_KITTY; }
 inline bool nvfp4(const kvq_config *c) { return c->mode == KVQ_MODE_NVFP4; }
 inline int64_t nvfp4_page_bytes(const kvq_config *c) { return 16 + (int64_t)c->G * c->D / 16; }

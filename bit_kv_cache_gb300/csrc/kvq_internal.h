@@ -7,6 +7,25 @@
 
 namespace kvq {
 
+// In-page arrangement of the packed words (KIVI codes and Kitty's low plane; NVFP4
+// pages have their own layout).  The words themselves are pack_tensor's; only their
+// order inside a page is chosen so that a decode tile arrives with one contiguous bulk
+// copy and its ldmatrix reads are free of shared-memory bank conflicts:
+//   keys:   a page is G/fpi word rows of D words; the word of channel d in row r
+//           (0-based within the page) sits at kword_pos(d, r) -- the 16-byte chunks of
+//           each row are permuted by XOR with r mod 8.
+//   values: a page is G/TV tiles of TV tokens, each [D/fpi rows][TV words]; the word of
+//           token j in row b sits at vword_pos(j, b, TV).  TV is the token count of a
+//           decode tile, 256 / key bits (eight key word rows), when it divides G, else G.
+__host__ __device__ __forceinline__ int kword_pos(int d, int r) { return d ^ ((r & 7) << 2); }
+__host__ __device__ __forceinline__ int vword_pos(int j, int b, int TV) {
+    return (TV & 31) ? j : j ^ ((b & 7) << 2);
+}
+__host__ __device__ __forceinline__ int v_tile_tokens(int kbits, int G) {
+    const int t = 256 / kbits;
+    return G % t == 0 ? t : G;
+}
+
 // Destination of the quant kernels' pages.  Dense (ptab null): grid unit u writes
 // page u * max_T/G + pg0 + j.  Paged: grid unit i is head h = i % H_kv of listed
 // sequence b = seq[i / H_kv]; its page j goes to physical page
@@ -46,6 +65,7 @@ struct QuantVParams {
     int64_t tok0;          // destination packed-token index of the first one (multiple of G)
     int64_t max_T;
     int U, D, G, Gv;
+    int TV;                // tokens per value tile of a page (v_tile_tokens)
     int32_t *v_codes;
     uint16_t *v_meta;
     int32_t *status;       // device status word (may be null)
@@ -114,6 +134,7 @@ struct SetLensParams {
 struct DecodeParams {
     // shape
     int B, H_kv, g, D, G, bits, vbits, Gv, n_boost, kitty;  // bits: keys, vbits: values
+    int v_tile;            // tokens per value tile of a page (v_tile_tokens)
     int S_cap, cap_k, cap_v, R_local;
     int64_t max_T;
     int rope;              // keys stored before RoPE: rotate key t by t * theta_j

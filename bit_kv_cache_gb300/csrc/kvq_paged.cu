@@ -110,6 +110,7 @@ QuantVParams qv_paged(const kvq_config *c, const kvq_paged *pc) {
     p.D = c->D;
     p.G = c->G;
     p.Gv = gv_of(c);
+    p.TV = vtile_of(c);
     p.v_codes = pc->v_codes;
     p.v_meta = pc->v_meta;
     p.status = pc->status;
@@ -412,6 +413,7 @@ int kvq_paged_decode_attn(const kvq_config *c, const kvq_paged *pc, const uint16
     p.bits = c->bits;
     p.vbits = vbits_of(c);
     p.Gv = gv_of(c);
+    p.v_tile = vtile_of(c);
     p.S_cap = c->S;
     p.cap_k = c->R;
     p.cap_v = c->R;

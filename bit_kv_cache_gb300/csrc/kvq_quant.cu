@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
 
     const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.pg0, u, pg);  // page index
     const int64_t wrow0 = page * (p.G / FPI) + sl * NW;  // first word row of this thread
-    uint2 *dst = reinterpret_cast<uint2 *>(p.k_codes) + pr;
+    uint2 *dst = reinterpret_cast<uint2 *>(p.k_codes);   // channel pairs; in-page order kword_pos
 #pragma unroll
     for (int wi = 0; wi < NW; wi++) {
         uint32_t w0 = 0, w1 = 0, h0 = 0, h1 = 0;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
                 h1 |= (c1 >> 2) << (2 * j);
             }
         }
-        dst[(size_t)(wrow0 + wi) * pairs] = make_uint2(w0, w1);
+        dst[(size_t)(wrow0 + wi) * pairs + (kword_pos(d0, sl * NW + wi) >> 1)] = make_uint2(w0, w1);
         if (KITTY) {
             int32_t *hp = p.k_hi + (size_t)(wrow0 + wi) * p.n_boost;
             if (slot[0] < p.n_boost) hp[slot[0]] = (int32_t)h0;
@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
     }
     // tok0 is a multiple of G: page tl / G of the call, token tl % G within it
     const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.tok0 / p.G, u, tl / p.G), tin = tl % p.G;
-    int32_t *vc = p.v_codes + ((size_t)page * NWORD) * p.G + tin;
+    // value tile of token tin and its position j there (in-page order vword_pos)
+    const int TV = p.TV, j = (int)(tin % TV);
+    int32_t *vc = p.v_codes + ((size_t)page * NWORD) * p.G + (size_t)(tin / TV) * NWORD * TV;
     uint32_t *vm = reinterpret_cast<uint32_t *>(p.v_meta) + ((size_t)page * p.G + tin) * (D / GV);
 #pragma unroll
     for (int g0 = 0; g0 < D; g0 += GV) {
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
                 w |= quant_code(f.x, g) << (BITS * j);
                 w |= quant_code(f.y, g) << (BITS * (j + 1));
             }
-            vc[(size_t)wi * p.G] = (int32_t)w;
+            vc[(size_t)wi * TV + vword_pos(j, wi, TV)] = (int32_t)w;
         }
     }
 }
@@ -357,8 +359,8 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
 // c, c + 4, c + 8, c + 12 (a warp load reads 64 contiguous bytes of 8 rows).  A
 // token's min / max reduces over its 4 lanes by two shuffles, and each of them forms
 // the token's group itself.  Codes pack along channels (2-bit words pair the chunks of
-// lanes c and c ^ 1) and are staged in shared memory, so that each word row of the page
-// leaves as contiguous 512-byte stores.
+// lanes c and c ^ 1) and are staged in shared memory, so that each word row of a value
+// tile leaves as contiguous stores (16-byte chunks in the tile's in-page order).
 // ------------------------------------------------------------------------------
 template <int BITS>
 __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int64_t tl0, const uint16_t *src) {
@@ -431,7 +433,10 @@ __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int6
     for (int i = tid; i < NWORD * 32; i += 256) {
         const int m = i >> 5, q4 = i & 31;
         const uint4 v = *reinterpret_cast<const uint4 *>(&s_codes[m][4 * q4]);
-        *reinterpret_cast<uint4 *>(p.v_codes + ((size_t)page * NWORD + m) * p.G + tin0 + 4 * q4) = v;
+        // tokens tt .. tt + 3 of the page: value tile tt / TV, position vword_pos there
+        const int TV = p.TV, tt = (int)tin0 + 4 * q4, tile = tt / TV, j = tt - tile * TV;
+        *reinterpret_cast<uint4 *>(p.v_codes + (size_t)page * NWORD * p.G + ((size_t)tile * NWORD + m) * TV +
+                                   vword_pos(j, m, TV)) = v;
     }
     if (tid < 32)
         reinterpret_cast<uint4 *>(reinterpret_cast<uint32_t *>(p.v_meta) + (size_t)page * p.G + tin0)[tid] =

@@ -8,6 +8,31 @@ TOL_ABS = 2e-3
 TOL_REL = 2e-3
 
 
+# The library keeps pack_tensor's words but orders them within a page for its decode
+# tiles: the 16-byte chunks of key word row r (0-based in its page) are permuted by XOR
+# with r mod 8, and value pages are tile-major ([G/TV][D/fpi rows][TV words]) with the
+# chunks of row b permuted by XOR with b mod 8 when TV is a multiple of 32.  These undo
+# that, giving the oracle's (the pages') layouts.
+def keys_logical(kc, G, kfpi):
+    """[..., T/fpi, D] words as stored -> pack_tensor's [..., T/fpi, D]."""
+    rows, D = kc.shape[-2:]
+    r = (np.arange(rows) % (G // kfpi)) & 7
+    pos = np.arange(D)[None, :] ^ (r[:, None] << 2)
+    return np.take_along_axis(kc, np.broadcast_to(pos, kc.shape), axis=-1)
+
+
+def values_logical(vc):
+    """[..., P, G/TV, D/fpi, TV] words as stored -> [..., P * G, D/fpi] (token-major)."""
+    rows, TV = vc.shape[-2:]
+    if TV % 32 == 0:
+        b = np.arange(rows) & 7
+        pos = np.arange(TV)[None, :] ^ (b[:, None] << 2)
+        vc = np.take_along_axis(vc, np.broadcast_to(pos, vc.shape), axis=-1)
+    vc = np.swapaxes(vc, -1, -2)
+    sh = vc.shape
+    return vc.reshape(sh[:-4] + (sh[-4] * sh[-3] * sh[-2], sh[-1]))
+
+
 def make_pair(wl, max_T, device):
     import bit_kv_cache_gb300 as kvq
     gpu = kvq.KVQCache(wl.B, wl.H_q, wl.H_kv, wl.D, wl.G, wl.bits, S=wl.S, R=wl.R,
@@ -94,12 +119,11 @@ def assert_state_equal(gpu, ora, units=None):
                 assert np.array_equal(pick(_u16(_np(gpu.view(name)[:, :, :n]))),
                                       pick(_u16(getattr(ora, name)[:, :, :n]))), name + " differs"
         return
-    kc = _np(gpu.view("k_codes")[:, :, : T_k // kfpi])
+    kc = keys_logical(_np(gpu.view("k_codes")[:, :, : T_k // kfpi]), G, kfpi)
     assert np.array_equal(pick(kc), pick(ora.k_codes)), "key codes differ"
     km = _u16(_np(gpu.view("k_meta")[:, :, : T_k // G]))
     assert np.array_equal(pick(km), pick(_u16(ora.k_meta))), "key scale/min differ"
-    vc = _np(gpu.view("v_codes")[:, :, : T_v // G])                 # [B,H,P,D/fpi,G]
-    vc = vc.transpose(0, 1, 2, 4, 3).reshape(cfg.B, cfg.H_kv, T_v, cfg.D // vfpi)
+    vc = values_logical(_np(gpu.view("v_codes")[:, :, : T_v // G]))  # [B,H,T_v,D/fpi]
     assert np.array_equal(pick(vc), pick(ora.v_codes)), "value codes differ"
     vm = _u16(_np(gpu.view("v_meta")[:, :, :T_v]))
     assert np.array_equal(pick(vm), pick(_u16(ora.v_meta))), "value scale/min differ"

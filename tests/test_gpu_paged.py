@@ -14,7 +14,7 @@ import pytest
 import kvq_synth
 import oracle
 from kvq_synth import WORKLOADS
-from parity_util import _np, _u16, assert_close, to_dev
+from parity_util import _np, _u16, assert_close, keys_logical, to_dev, values_logical
 
 pytestmark = pytest.mark.gpu
 
@@ -85,11 +85,11 @@ class Pair:
             assert len(pages) == T // G
             if T:
                 idx = np.asarray(pages)
-                kc = _np(g.view("k_codes"))[idx].transpose(1, 0, 2, 3).reshape(H, T // kfpi, D)
+                kc = keys_logical(_np(g.view("k_codes"))[idx], G, kfpi).transpose(1, 0, 2, 3).reshape(H, T // kfpi, D)
                 assert np.array_equal(kc, o.k_codes[0][:, : T // kfpi]), "slot %d: key codes" % b
                 km = _u16(_np(g.view("k_meta"))[idx].transpose(1, 0, 2, 3))
                 assert np.array_equal(km, _u16(o.k_meta[0][:, : T // G])), "slot %d: key scale/min" % b
-                vc = _np(g.view("v_codes"))[idx].transpose(1, 0, 3, 2).reshape(H, T, D // vfpi)
+                vc = values_logical(_np(g.view("v_codes"))[idx].swapaxes(0, 1))
                 assert np.array_equal(vc, o.v_codes[0][:, :T]), "slot %d: value codes" % b
                 vm = _u16(_np(g.view("v_meta"))[idx].transpose(1, 0, 2, 3, 4).reshape(H, T, D // Gv, 2))
                 assert np.array_equal(vm, _u16(o.v_meta[0][:, :T])), "slot %d: value scale/min" % b
