@@ -501,8 +501,9 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
     memset(&p, 0, sizeof(p));
     p.U = U;
     p.wpc = wpc;
-    // The schedule depends only on these numbers; decode steps repeat them for 16
-    // tokens at a time, so the last one is kept.
+    // The schedule depends only on these numbers.  Decode steps repeat them for 16
+    // tokens at a time, and the layers of a model share them; a small per-thread cache
+    // (direct-mapped on a hash of the numbers) keeps recent ones.
     struct SchedKey {
         int64_t U, wpc, nsm, fast, T_k, T_v, n_sink, n_kres, L, tok;
         bool operator==(const SchedKey &o) const { return memcmp(this, &o, sizeof(*this)) == 0; }
@@ -511,9 +512,12 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
         int C_f, C_m, C_g, n_gc, max_slots;
         int64_t n_fast, n_mini, N_f, N_m, n_gen, gen_chunk;
     };
-    static thread_local SchedKey last_key;
-    static thread_local SchedVal last_val;
-    static thread_local bool have_last = false;
+    struct SchedEntry {
+        SchedKey key;
+        SchedVal val;
+        bool valid;
+    };
+    static thread_local SchedEntry sched_cache[32];
     SchedKey key;
     memset(&key, 0, sizeof(key));
     key.U = U;
@@ -526,8 +530,13 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
     key.n_kres = k->n_kres;
     key.L = L;
     key.tok = tok;
-    if (have_last && key == last_key) {
-        const SchedVal &v = last_val;
+    uint64_t hsh = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(key) / sizeof(int64_t); i++)
+        hsh = (hsh ^ (uint64_t)reinterpret_cast<const int64_t *>(&key)[i]) * 1099511628211ull;
+    SchedEntry &ce = sched_cache[(hsh >> 29) & 31];
+    const bool hit = ce.valid && key == ce.key;
+    if (hit) {
+        const SchedVal &v = ce.val;
         p.C_f = v.C_f;
         p.C_m = v.C_m;
         p.C_g = v.C_g;
@@ -571,7 +580,7 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
             }
         }
     }
-    if (!(have_last && key == last_key)) {
+    if (!hit) {
         // slots per sequence
         int64_t max_slots = 0;
         for (int64_t u = 0; u < U; u++) {
@@ -587,10 +596,10 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
             p.C_g > 4 * (int64_t)max_pool_ctas(c) || !small)
             return KVQ_ERR_UNSUPPORTED;
         p.max_slots = (int)max_slots;
-        last_key = key;
-        last_val = SchedVal{p.C_f, p.C_m, p.C_g, p.n_gc, p.max_slots, p.n_fast,
-                            p.n_mini, p.N_f, p.N_m, p.n_gen, p.gen_chunk};
-        have_last = true;
+        ce.key = key;
+        ce.val = SchedVal{p.C_f, p.C_m, p.C_g, p.n_gc, p.max_slots, p.n_fast,
+                          p.n_mini, p.N_f, p.N_m, p.n_gen, p.gen_chunk};
+        ce.valid = true;
     }
 
     p.n_items = fast ? (int)(p.n_fast + p.n_mini) : p.n_gc;

@@ -822,7 +822,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
 }
 
 // ---------------------------------------------------------------------------------
-constexpr int kSmemMax = 227 * 1024;
+// Dynamic shared memory of a CTA: the 227 KB per block less 4 KB kept for the kernel's
+// static shared memory and the paged / pre-RoPE extras.
+constexpr int kSmemMax = 227 * 1024 - 4096;
 
 // Units (warps, or warp pairs) per CTA of a tile kernel: as many of 8, 6, 4 as fit.
 constexpr int tile_units(int kb, int vb, bool kitty, int n_boost) {
@@ -860,7 +862,8 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
     if (RP) smem += kRopeFloats * 4;        // pre-RoPE: the tables
     auto k = decode_kernel<KB, VB, KITTY, FAST, PAIR, DPL, NW, PG, RP, F4>;
     // The dynamic shared-memory limit is raised once per device to the most any
-    // configuration of this instantiation asks for (the opt-in maximum).
+    // configuration of this instantiation can ask for: the opt-in maximum less the
+    // kernel's static shared memory.
     static int raised[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
@@ -868,7 +871,10 @@ static cudaError_t launch_one(const DecodeParams &p, cudaStream_t st) {
         int optin = 0;
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) raised[dev] = 1;
     }

@@ -403,8 +403,12 @@ struct FastWarp {
         const unsigned char *base;
         uint32_t pstride, tstride, dst, bytes;
     };
-    CopyLane ck{}, cv{};
-    const unsigned char *vm_base = nullptr;
+    CopyLane ck{};         // Kitty: this lane's high-plane row or boost-index copy
+    // Dense caches: tile ti of sequence u (pages contiguous, whole tiles per page) has
+    // its key codes at kc_base + ti * 8 D 4 bytes, its value codes at vc_base + ti *
+    // V_ROWS TOK 4, its page's key (scale, min) row at km_base + (ti >> tpp_shift) * D 4
+    // and its value (scale, min) at vm_base + ti * TOK 4; lane 0 issues those copies.
+    const unsigned char *kc_base = nullptr, *km_base = nullptr, *vc_base = nullptr, *vm_base = nullptr;
     uint32_t k_total = 0;  // bytes of a key batch (without the first batch's value meta)
     // ldmatrix: the lane addresses row r = lane & 7 of a row set at logical 16-byte chunk
     // 4 sl + lane / 8 of slab sl, stored at chunk (4 sl + lane / 8) ^ r (kword_pos /
@@ -437,23 +441,18 @@ struct FastWarp {
         return ok;
     }
 
-    // Per-lane copies of sequence u (dense caches).  Key batch: lane 0 the tile's eight
-    // code rows (one contiguous block of the page), lane 8 the page's (scale, min) row,
-    // Kitty lanes 10..17 the high-plane rows and lane 18 the boost index.  Value batch:
-    // lane 0 the tile's code rows (one contiguous block of the tile-major page).
+    // Copies of sequence u (dense caches): lane 0 the tile's code rows, the page's key
+    // (scale, min) row and the value blocks; Kitty lanes 10..17 the high-plane rows and
+    // lane 18 the boost index.
     __device__ void set_copies() {
-        const int64_t pages = p.max_T / p.G, pg0 = (int64_t)u * pages;
-        const int tpp = 1 << p.tpp_shift;
+        const int64_t pg0 = (int64_t)u * (p.max_T / p.G);
         const int nb = KITTY ? p.n_boost : 0;
-        const unsigned char *kc = reinterpret_cast<const unsigned char *>(p.k_codes);
-        ck = CopyLane{kc, 0, 0, 0, 0};
-        if (lane == 0) {
-            const uint32_t row = T::D * 4, page = (uint32_t)(p.G / CK::FPI) * row;
-            ck = CopyLane{kc + (size_t)pg0 * page, page, 8 * row, (uint32_t)T::OFF_K, 8 * row};
-        } else if (lane == 8) {
-            ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_meta) + (size_t)pg0 * T::D * 4, T::D * 4, 0,
-                          (uint32_t)T::OFF_KM, T::D * 4};
-        } else if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
+        kc_base = reinterpret_cast<const unsigned char *>(p.k_codes) + (size_t)pg0 * (p.G / CK::FPI) * T::D * 4;
+        km_base = reinterpret_cast<const unsigned char *>(p.k_meta) + (size_t)pg0 * T::D * 4;
+        vc_base = reinterpret_cast<const unsigned char *>(p.v_codes) + (size_t)pg0 * T::V_ROWS * p.G * 4;
+        vm_base = reinterpret_cast<const unsigned char *>(p.v_meta) + (size_t)pg0 * p.G * 4;
+        ck = CopyLane{nullptr, 0, 0, 0, 0};
+        if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
             const uint32_t row = nb * 4, page = (uint32_t)(p.G / 16) * row;
             ck = CopyLane{reinterpret_cast<const unsigned char *>(p.k_hi) + (size_t)pg0 * page + (lane - 10) * row,
                           page, 8 * row, (uint32_t)(T::OFF_HI + (lane - 10) * hi_stride(nb)), row};
@@ -462,13 +461,6 @@ struct FastWarp {
                           (uint32_t)(T::OFF_HI + 8 * hi_stride(nb)), T::D};
         }
         k_total = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0);
-        cv = CopyLane{nullptr, 0, 0, 0, 0};
-        if (lane == 0) {
-            const uint32_t page = (uint32_t)T::V_ROWS * p.G * 4, tile = T::V_ROWS * T::TOK * 4;
-            cv = CopyLane{reinterpret_cast<const unsigned char *>(p.v_codes) + (size_t)pg0 * page, page, tile, 0u, tile};
-        }
-        vm_base = reinterpret_cast<const unsigned char *>(p.v_meta) + (size_t)pg0 * p.G * 4;
-        (void)tpp;
     }
     __device__ __forceinline__ const unsigned char *copy_src(const CopyLane &c, int64_t ti) const {
         return c.base + (size_t)(ti >> p.tpp_shift) * c.pstride + (size_t)(ti & ((1 << p.tpp_shift) - 1)) * c.tstride;
@@ -481,10 +473,17 @@ struct FastWarp {
             const int s = j & 1;
             const int64_t ti = t0 + j;
             pending |= 1u << s;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[s], k_total + (j == 0 ? T::TOK * 4 : 0));
-            __syncwarp();
-            if (ck.bytes) issue_copy(kslot(s) + ck.dst, copy_src(ck, ti), ck.bytes, &bars[s]);
-            if (j == 0 && lane == 9) issue_copy(vmslot(0), vm_base + (size_t)ti * T::TOK * 4, T::TOK * 4, &bars[s]);
+            unsigned char *st = kslot(s);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[s], k_total + (j == 0 ? T::TOK * 4 : 0));
+                issue_copy(st + T::OFF_K, kc_base + (size_t)ti * (8 * T::D * 4), 8 * T::D * 4, &bars[s]);
+                issue_copy(st + T::OFF_KM, km_base + (size_t)(ti >> p.tpp_shift) * (T::D * 4), T::D * 4, &bars[s]);
+                if (j == 0) issue_copy(vmslot(0), vm_base + (size_t)ti * (T::TOK * 4), T::TOK * 4, &bars[s]);
+            }
+            if (KITTY) {  // the high-plane rows after lane 0's expect-tx
+                __syncwarp();
+                if (ck.bytes) issue_copy(st + ck.dst, copy_src(ck, ti), ck.bytes, &bars[s]);
+            }
             return;
         }
         const int s = j & 1;
@@ -493,20 +492,19 @@ struct FastWarp {
         unsigned char *st = kslot(s);
         const int nb = KITTY ? p.n_boost : 0;
         const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + (j == 0 ? T::TOK * 4 : 0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], bytes);
-        __syncwarp();
         // tiles per page: a power of two; pg: page index, tin: tile within the page
         const int64_t pg = pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
         const int i = lane;
         if (i == 0) {
+            mbar_arrive_expect_tx(&bars[s], bytes);
             issue_copy(st + T::OFF_K, p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8) * T::D, 8 * T::D * 4,
                        &bars[s]);
-        } else if (i == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &bars[s]);
-        } else if (i == 9) {
             if (j == 0)
                 issue_copy(vmslot(0), p.v_meta + ((size_t)pg * p.G + tin * T::TOK) * 2, T::TOK * 4, &bars[s]);
-        } else if (KITTY && nb > 0 && i >= 10 && i < 18) {
+        }
+        if (KITTY) __syncwarp();  // the high-plane rows after lane 0's expect-tx
+        if (KITTY && nb > 0 && i >= 10 && i < 18) {
             const int r = i - 10;
             issue_copy(st + T::OFF_HI + r * hi_stride(nb), p.k_hi + ((size_t)pg * (p.G / 16) + tin * 8 + r) * nb,
                        nb * 4, &bars[s]);
@@ -523,11 +521,12 @@ struct FastWarp {
             const int64_t ti = t0 + j;
             const bool meta = j + 1 < n;
             pending |= 1u << s;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
-            __syncwarp();
-            if (cv.bytes) issue_copy(vslot(j & 1) + cv.dst, copy_src(cv, ti), cv.bytes, &bars[s]);
-            if (meta && lane == 1)
-                issue_copy(vmslot((j + 1) & 1), vm_base + (size_t)(ti + 1) * T::TOK * 4, T::TOK * 4, &bars[s]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
+                issue_copy(vslot(j & 1), vc_base + (size_t)ti * (T::V_ROWS * T::TOK * 4), T::V_ROWS * T::TOK * 4,
+                           &bars[s]);
+                if (meta) issue_copy(vmslot((j + 1) & 1), vm_base + (size_t)(ti + 1) * (T::TOK * 4), T::TOK * 4, &bars[s]);
+            }
             return;
         }
         const int s = 2 + (j & 1);
@@ -535,18 +534,14 @@ struct FastWarp {
         const bool meta = j + 1 < n;
         pending |= 1u << s;
         unsigned char *st = vslot(j & 1);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
-        __syncwarp();
         const int tmask = (1 << p.tpp_shift) - 1;
         const int64_t pg = pid(p, ti >> p.tpp_shift), tin = ti & tmask;
         const int64_t pg1 = meta ? pid(p, (ti + 1) >> p.tpp_shift) : 0, off1 = ((ti + 1) & tmask) * T::TOK;
-        const int i = lane;
-        if (i == 0) {  // the tile's value rows: one block of the tile-major page
+        if (lane == 0) {  // the tile's value rows: one block of the tile-major page
+            mbar_arrive_expect_tx(&bars[s], T::V_ROWS * T::TOK * 4 + (meta ? T::TOK * 4 : 0));
             issue_copy(st, p.v_codes + ((size_t)pg * p.G + tin * T::TOK) * T::V_ROWS, T::V_ROWS * T::TOK * 4,
                        &bars[s]);
-        }
-        if (i == 1 && meta) {
-            issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)pg1 * p.G + off1) * 2, T::TOK * 4, &bars[s]);
+            if (meta) issue_copy(vmslot((j + 1) & 1), p.v_meta + ((size_t)pg1 * p.G + off1) * 2, T::TOK * 4, &bars[s]);
         }
     }
 
@@ -1122,18 +1117,17 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
         unsigned char *st = this->kslot(s);
         const int nb = KITTY ? p.n_boost : 0;
         const uint32_t bytes = 8 * T::D * 4 + T::D * 4 + (KITTY ? 8 * nb * 4 + T::D : 0) + T::TOK * 4;
-        if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], bytes);
-        __syncwarp();
         const int64_t pg = this->pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
         if (lane == 0) {
+            mbar_arrive_expect_tx(&this->bars[s], bytes);
             issue_copy(st + T::OFF_K, p.k_codes + ((size_t)pg * (p.G / CK::FPI) + tin * 8) * T::D, 8 * T::D * 4,
                        &this->bars[s]);
-        } else if (lane == 8) {
             issue_copy(st + T::OFF_KM, p.k_meta + (size_t)pg * T::D * 2, T::D * 4, &this->bars[s]);
-        } else if (lane == 9) {
             issue_copy(this->vmslot(s), p.v_meta + ((size_t)pg * p.G + tin * T::TOK) * 2, T::TOK * 4,
                        &this->bars[s]);
-        } else if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
+        }
+        if (KITTY) __syncwarp();  // the high-plane rows after lane 0's expect-tx
+        if (KITTY && nb > 0 && lane >= 10 && lane < 18) {
             const int r = lane - 10;
             issue_copy(st + T::OFF_HI + r * hi_stride(nb), p.k_hi + ((size_t)pg * (p.G / 16) + tin * 8 + r) * nb,
                        nb * 4, &this->bars[s]);
@@ -1149,12 +1143,12 @@ struct PairWarp : FastWarp<KB, VB, KITTY, PG, RP> {
         const int64_t ti = t0 + j;
         this->pending |= 1u << s;
         unsigned char *st = this->vslot(j & 1);
-        if (lane == 0) mbar_arrive_expect_tx(&this->bars[s], T::V_ROWS * T::TOK * 4);
-        __syncwarp();
         const int64_t pg = this->pid(p, ti >> p.tpp_shift), tin = ti & ((1 << p.tpp_shift) - 1);
-        if (lane == 0)  // the tile's value rows: one block of the tile-major page
+        if (lane == 0) {  // the tile's value rows: one block of the tile-major page
+            mbar_arrive_expect_tx(&this->bars[s], T::V_ROWS * T::TOK * 4);
             issue_copy(st, p.v_codes + ((size_t)pg * p.G + tin * T::TOK) * T::V_ROWS, T::V_ROWS * T::TOK * 4,
                        &this->bars[s]);
+        }
     }
 
     __device__ void drain(uint32_t mask) {  // copies still in flight land before smem reuse
