@@ -894,8 +894,9 @@ def main():
     per_step = sorted(r / K for r in region_ms)
 
     # ---- end to end through host buffers: one kvq_decode_step_host call per step
-    # (copies in, append, attend, flush, copy out; pinned memory), then a stream
-    # synchronize, through the C ABI with prepared arguments ----
+    # (inputs in, append, attend, flush, output out; pinned memory, which the kernels
+    # read and write in place), then a stream synchronize, through the C ABI with
+    # prepared arguments ----
     kn_h = torch.from_numpy(kn).pin_memory()
     vn_h = torch.from_numpy(vn).pin_memory()
     q_h = torch.from_numpy(qs).pin_memory()

@@ -725,23 +725,16 @@ int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, c
     uint16_t *dv = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + step_io_part(nk));
     uint16_t *dout = reinterpret_cast<uint16_t *>(d + step_io_part(nq) + 2 * step_io_part(nk));
     cudaStream_t st = (cudaStream_t)stream;
-    // Page-locked host buffers mapped into the device's address space are read by one
-    // stage-in kernel and the attention output is written straight into `out`; other
-    // host memory goes through one cudaMemcpyAsync per buffer.
+    // Page-locked host buffers mapped into the device's address space are read and
+    // written by the kernels themselves (plain loads and stores; no bulk copy touches
+    // them); other host memory goes through one cudaMemcpyAsync per buffer.
     const void *mq = mapped_host(q), *mk = mapped_host(k_new), *mv = mapped_host(v_new);
     void *mo = const_cast<void *>(mapped_host(out));
     const bool direct = mq && mk && mv && mo && aligned16(mq) && aligned16(mk) && aligned16(mv) && aligned16(mo);
     if (direct) {
-        StageParams sp;
-        sp.src[0] = mq;
-        sp.src[1] = mk;
-        sp.src[2] = mv;
-        sp.dst[0] = dq;
-        sp.dst[1] = dk;
-        sp.dst[2] = dv;
-        sp.n[0] = (int64_t)nq;
-        sp.n[1] = sp.n[2] = (int64_t)nk;
-        if (launch_stage_in(sp, st) != cudaSuccess) return KVQ_ERR_CUDA;
+        dq = static_cast<uint16_t *>(const_cast<void *>(mq));
+        dk = static_cast<uint16_t *>(const_cast<void *>(mk));
+        dv = static_cast<uint16_t *>(const_cast<void *>(mv));
         dout = static_cast<uint16_t *>(mo);
     } else if (cudaMemcpyAsync(dk, k_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||
                cudaMemcpyAsync(dv, v_new, nk, cudaMemcpyDefault, st) != cudaSuccess ||

@@ -1665,20 +1665,21 @@ struct MiniWarp {
         unsigned char *sK = slot(sk), *sV = slot(sk + 1);
         const int i = lane & 15;
         const int64_t tl = mt.tok0 + (i < mt.n ? i : 0);
-        // appended in this launch: the last token's rows come from k_new / v_new, and this
-        // warp (the only one holding the sequence's last tile) stores them into the
-        // residuals, 16 bytes per lane; no copy of this launch reads those residual rows
-        const bool fresh = p.k_new && tl == sq.L - 1;
+        // appended in this launch: the last token's rows come from k_new / v_new (plain
+        // loads, so they may be host memory the device can map), and this warp -- the
+        // only one holding the sequence's last tile -- stores them into the residuals, 16
+        // bytes per lane; its bulk copies below then read them from there
         if (p.k_new && mt.tok0 + mt.n == sq.L) {
             const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? p.k_new : p.v_new) + (size_t)u * 128);
             uint16_t *dst = lane < 16 ? const_cast<uint16_t *>(krow16(p, sq, u, sq.L - 1))
                                       : const_cast<uint16_t *>(vrow16(p, sq, u, sq.L - 1));
             reinterpret_cast<uint4 *>(dst)[i] = __ldg(src + i);
+            __syncwarp();
+            fence_proxy_async_global();
         }
         if (lane < 16) {
             if (!mt.kpacked) {
-                issue_copy(sK + i * kMiniRow, fresh ? p.k_new + (size_t)u * 128 : krow16(p, sq, u, tl), 256,
-                           &bars[sk]);
+                issue_copy(sK + i * kMiniRow, krow16(p, sq, u, tl), 256, &bars[sk]);
             } else {  // Kitty mixed blocks (dense caches only)
                 const int64_t tk = mt.tok0 - sq.n_sink, page = tk >> p.g_shift, blk = tk >> 4;
                 if (i == 0) {
@@ -1693,8 +1694,7 @@ struct MiniWarp {
                 }
             }
         } else {
-            issue_copy(sV + i * kMiniRow, fresh ? p.v_new + (size_t)u * 128 : vrow16(p, sq, u, tl), 256,
-                       &bars[sk + 1]);
+            issue_copy(sV + i * kMiniRow, vrow16(p, sq, u, tl), 256, &bars[sk + 1]);
         }
     }
 

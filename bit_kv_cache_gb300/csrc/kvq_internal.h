@@ -108,13 +108,6 @@ struct PagedAppendParams {
     int B, H_kv, D, S, R;
 };
 
-// Up to three array copies in one launch (the host-buffer step's inputs).
-struct StageParams {
-    const void *src[3];
-    void *dst[3];
-    int64_t n[3];  // bytes, multiples of 16
-};
-
 // Writes lens[b] = {v0, v1, v2, v3} (prefill and release of a batch slot).
 struct SetLensParams {
     int32_t *lens;
@@ -196,7 +189,6 @@ cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st);
 cudaError_t launch_nvfp4(const QuantNvParams &p, bool values, cudaStream_t st);
 cudaError_t launch_copy_rows(const CopyRowsParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
-cudaError_t launch_stage_in(const StageParams &p, cudaStream_t st);
 cudaError_t launch_paged_append(const PagedAppendParams &p, cudaStream_t st);
 cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &p, bool fast, cudaStream_t st);

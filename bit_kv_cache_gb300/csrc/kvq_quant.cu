@@ -757,30 +757,6 @@ cudaError_t launch_set_lens(const SetLensParams &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// Copies up to three 16-byte-aligned arrays (n[i] bytes, multiples of 16) from src[i]
-// to dst[i]; the sources may be page-locked host memory mapped into the device's
-// address space (kvq_decode_step_host), read over the host link.
-__global__ void stage_in_kernel(StageParams p) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int64_t off = i;
-#pragma unroll
-    for (int a = 0; a < 3; a++) {
-        const int64_t n16 = p.n[a] / 16;
-        if (off < n16) {
-            reinterpret_cast<uint4 *>(p.dst[a])[off] = __ldcs(reinterpret_cast<const uint4 *>(p.src[a]) + off);
-            return;
-        }
-        off -= n16;
-    }
-}
-
-cudaError_t launch_stage_in(const StageParams &p, cudaStream_t st) {
-    const int64_t total = (p.n[0] + p.n[1] + p.n[2]) / 16;
-    if (total == 0) return cudaSuccess;
-    stage_in_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st) {
     int64_t total = (int64_t)p.U * (p.D / 8);
     append_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(p);

@@ -106,17 +106,27 @@ typedef struct {
 /* Caller-owned device buffers and host-side lengths of one layer's cache.
  * Layouts (U = B*H_kv sequences, fpi = 32/bits codes per int32 for keys and
  * 32/v_bits for values, element j of a word at bit bits*j, least significant first):
- *   k_codes  int32 [U][max_T/fpi][D]     keys packed along tokens: word (w, d) holds
- *                                        tokens fpi*w .. fpi*w+fpi-1 of channel d.
+ *   k_codes  int32 [U][max_T/fpi][D]     keys packed along tokens: row w holds the
+ *                                        words of tokens fpi*w .. fpi*w+fpi-1, one per
+ *                                        channel; the word of channel d sits at
+ *                                        position d ^ (4 * (r mod 8)), r = w mod (G/fpi)
+ *                                        its row within the page (16-byte chunks of a
+ *                                        row permuted, so that a decode tile of eight
+ *                                        rows is one contiguous copy whose tensor-core
+ *                                        reads avoid shared-memory bank conflicts).
  *                                        Kitty: the low 2-bit plane (fpi = 16).
  *   k_hi     int32 [U][max_T/16][n_boost] Kitty: high 2 bits of the boosted channels,
  *                                        slot order; NULL if n_boost == 0.
  *   k_bidx   uint8 [U][max_T/G][D]       Kitty: channel -> slot, n_boost+1 if not
  *                                        boosted; NULL in KIVI mode.
  *   k_meta   fp16  [U][max_T/G][D][2]    (scale, min) per channel per group.
- *   v_codes  int32 [U][max_T/G][D/fpi][G] values packed along channels; within a
- *                                        page of G tokens, word (m, t) holds channels
- *                                        fpi*m .. fpi*m+fpi-1 of token t.
+ *   v_codes  int32 [U][max_T/G][G/TV][D/fpi][TV]  values packed along channels: a
+ *                                        page of G tokens is G/TV tiles of TV tokens
+ *                                        (TV = 256/key bits -- 2 for Kitty -- when
+ *                                        that divides G, else G); in a tile, row m holds
+ *                                        the words of channels fpi*m .. fpi*m+fpi-1, and
+ *                                        token j's word sits at position j ^ (4*(m mod 8))
+ *                                        when TV is a multiple of 32, else at j.
  *   v_meta   fp16  [U][max_T][D/Gv][2]   (scale, min) per token per channel group.
  *   k_sink, v_sink  fp16 [U][S][D]       (NULL if S == 0)
  *   k_res    fp16  [U][cap_k][D]         cap_k = R (KIVI residual) or G (Kitty Q-buffer)
@@ -234,15 +244,16 @@ size_t kvq_step_io_bytes(const kvq_config *cfg);
 
 /* One whole decode step from host memory: the three stages of the decode pipeline in
  * order (Kitty Sec. 4.3), with the transfers in and out.
- *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) are brought
- *      into the device staging buffer io;
+ *   1. k_new, v_new (host fp16 [B][H_kv][D]) and q (host fp16 [B][H_q][D]) reach the
+ *      device;
  *   2. kvq_append_decode, then kvq_flush_group;
  *   3. the attention output reaches out (host fp16 [B][H_q][D]).
  * When all four host buffers are page-locked memory mapped into the device's address
  * space (cudaHostAlloc / cudaHostRegister; with unified addressing every page-locked
- * allocation is), one kernel reads the inputs over the host link into io and the
- * attention kernel writes its output straight into out.  Otherwise there is one
- * cudaMemcpyAsync per buffer in and out (asynchronous only for page-locked memory).
+ * allocation is), the kernels read the inputs and write the output in place over the
+ * host link (plain loads and stores) and io is not touched.  Otherwise there is one
+ * cudaMemcpyAsync per buffer through io, in and out (asynchronous only for page-locked
+ * memory).
  * Everything is enqueued on `stream` and nothing is synchronized: out holds the result
  * once the stream has passed this point (cudaStreamSynchronize or an event), and the
  * host inputs must stay unchanged until then.
@@ -251,7 +262,7 @@ size_t kvq_step_io_bytes(const kvq_config *cfg);
  * flushed_k, flushed_v as for kvq_flush_group.
  * Returns KVQ_OK or the status of the first stage that fails; the stages before it
  * have taken effect, as if called one by one (a refused append leaves the cache as it
- * was; only the transfers into io were enqueued). */
+ * was; only the copies into io, if the buffers are not mapped, were enqueued). */
 int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *q,
                          const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, void *io,
                          size_t io_bytes, void *ws, size_t ws_bytes, int *flushed_k,
@@ -260,9 +271,10 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
 /* Stages (1) and (2) together: kvq_append_token(k_new, v_new), then kvq_decode_attn(q,
  * out), with the same arguments, layouts, results and errors.  Where the token goes to
  * the key and value residuals of a KIVI cache (sink full) and the packed-tile path
- * serves the attention, both run in one launch: the 16-token tile holding the new
- * token reads its key and value rows straight from k_new and v_new, and the warp that
- * owns that tile also stores them into the residuals.  Otherwise the two calls run one
+ * serves the attention, both run in one launch: the warp that owns the 16-token tile
+ * holding the new token reads its key and value rows from k_new and v_new (plain loads)
+ * and stores them into the residuals, from where that tile's copies read them.  No other
+ * copy of the launch reads those rows.  Otherwise the two calls run one
  * after the other (then, if the attention stage fails, the append has taken effect).
  * *fused (may be NULL) receives 1 if one launch did both, else 0. */
 int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k_new,
@@ -308,9 +320,9 @@ int kvq_decode_attn_noalloc(const kvq_config *cfg, const kvq_cache *cache, const
  * Physical page p (0 <= p < n_pages) holds one group of G tokens of all H_kv heads of
  * one sequence.  The page pools use the page-major layouts of kvq_cache with the page
  * index (u * max_T/G + logical page) replaced by (p * H_kv + h):
- *   k_codes  int32 [n_pages][H_kv][G/fpi_k][D]
+ *   k_codes  int32 [n_pages][H_kv][G/fpi_k][D]        (rows arranged as in kvq_cache)
  *   k_meta   fp16  [n_pages][H_kv][D][2]
- *   v_codes  int32 [n_pages][H_kv][D/fpi_v][G]
+ *   v_codes  int32 [n_pages][H_kv][G/TV][D/fpi_v][TV]  (tiles arranged as in kvq_cache)
  *   v_meta   fp16  [n_pages][H_kv][G][D/Gv][2]
  * page_table int32 [B][max_T/G] (device) maps logical page j of sequence b to its
  * physical page.  The caller owns the pool and the table and chooses the pages: before

@@ -1,5 +1,5 @@
-"""kvq_decode_step_host (one decode step from host buffers: copies in, append,
-attend, flush, copy out) against the same steps through the device-buffer calls (bit
+"""kvq_decode_step_host (one decode step from host buffers: inputs in, append,
+attend, flush, output out) against the same steps through the device-buffer calls (bit
 for bit: decode is deterministic) and against the CPU oracle, over steps that cross a
 flush of the residual."""
 import numpy as np
@@ -38,9 +38,15 @@ def _cache(kvq, wl, K, V):
     return c
 
 
+@pytest.mark.parametrize("pinned", [True, False], ids=["mapped", "pageable"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_host_step_matches_device_steps(kvq, name):
+def test_host_step_matches_device_steps(kvq, name, pinned):
+    """Page-locked (mapped) host buffers are read and written by the kernels in place;
+    pageable ones go through copies into the staging buffer."""
     import torch
+
+    def host_mem(t):
+        return t.pin_memory() if pinned else t
     wl, L0 = CASES[name]
     K, V = kvq_synth.prefill_kv(wl, L0)
     kn, vn = kvq_synth.decode_tokens(wl, STEPS)
@@ -54,9 +60,9 @@ def test_host_step_matches_device_steps(kvq, name):
         dev.append_token(to_dev(kn[i], DEV), to_dev(vn[i], DEV))
         ref = dev.decode_attn(to_dev(qs[i], DEV))
         fd = dev.flush_group()
-        out = torch.full(tuple(qs[i].shape), float("nan"), dtype=torch.float16).pin_memory()
-        fh = host.step_host(torch.from_numpy(qs[i]).pin_memory(), torch.from_numpy(kn[i]).pin_memory(),
-                            torch.from_numpy(vn[i]).pin_memory(), out)
+        out = host_mem(torch.full(tuple(qs[i].shape), float("nan"), dtype=torch.float16))
+        fh = host.step_host(host_mem(torch.from_numpy(qs[i])), host_mem(torch.from_numpy(kn[i])),
+                            host_mem(torch.from_numpy(vn[i])), out)
         torch.cuda.synchronize()
         assert fh == fd
         flushes += fd[0] or fd[1]
