@@ -429,7 +429,7 @@ __device__ void combine_item(const DecodeParams &p, int u, int ns, int h, int d)
 #pragma unroll
         for (int j = 0; j < 8; j++) Mn = fmaxf(Mn, ml[j].x);
         if (Mn == -INFINITY) continue;
-        const float r = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float r = M == -INFINITY ? 0.f : ex2(M - Mn);
         L *= r;
         O.x *= r;
         O.y *= r;
@@ -438,7 +438,7 @@ __device__ void combine_item(const DecodeParams &p, int u, int ns, int h, int d)
         M = Mn;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            const float f = ml[j].x == -INFINITY ? 0.f : exp2f(ml[j].x - M);
+            const float f = ml[j].x == -INFINITY ? 0.f : ex2(ml[j].x - M);
             L = fmaf(ml[j].y, f, L);
             O.x = fmaf(v[j].x, f, O.x);
             O.y = fmaf(v[j].y, f, O.y);
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
                 if (s_seg[w][e] == u) {
                     const float *s = src_of(w, e) + h * R;
                     const float mw = s[D];
-                    const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                    const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
                     L = fmaf(s[D + 1], f, L);
                     const float4 v = *reinterpret_cast<const float4 *>(s + d);
                     acc.x = fmaf(v.x, f, acc.x);
