@@ -168,6 +168,20 @@ cudaError_t launch_values(const kvq_config *c, kvq_cache *k, const QuantVParams 
     return launch_nvfp4(q, true, st);
 }
 
+// Adds a row copy (same arguments as copy_rows) to the copies a quant launch carries.
+void add_rows(RowCopies &rc, const uint16_t *src, int64_t src_rows, int64_t src_r0, uint16_t *dst, int64_t dst_rows,
+              int64_t dst_r0, int64_t n) {
+    if (n <= 0) return;
+    RowCopy &r = rc.c[rc.n++];
+    r.src = src;
+    r.dst = dst;
+    r.src_rows = src_rows;
+    r.src_r0 = src_r0;
+    r.dst_rows = dst_rows;
+    r.dst_r0 = dst_r0;
+    r.n_rows = n;
+}
+
 cudaError_t copy_rows(const kvq_config *c, const uint16_t *src, int64_t src_rows, int64_t src_r0, uint16_t *dst,
                       int64_t dst_rows, int64_t dst_r0, int64_t n, cudaStream_t st) {
     CopyRowsParams p;
@@ -277,17 +291,29 @@ int kvq_quant_pack_k(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
     if (kres > cap_k(c)) return KVQ_ERR_CAPACITY;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t ce = cudaSuccess;
-    if (ns > 0) ce = copy_rows(c, src, L0, 0, k->k_sink, c->S, 0, ns, st);
-    if (ce == cudaSuccess && tk > 0) {
+    if (tk > 0 && !nvfp4(c)) {  // one launch: the pages, with the sink and residual rows
         QuantKParams p = qk_params(c, k);
         p.src = src;
         p.src_ustride = L0 * c->D;
         p.src_t0 = ns;
         p.n_pages = tk / c->G;
         p.pg0 = 0;
+        add_rows(p.rc, src, L0, 0, k->k_sink, c->S, 0, ns);
+        add_rows(p.rc, src, L0, ns + tk, k->k_res, cap_k(c), 0, kres);
         ce = launch_keys(c, k, p, st);
+    } else {
+        if (ns > 0) ce = copy_rows(c, src, L0, 0, k->k_sink, c->S, 0, ns, st);
+        if (ce == cudaSuccess && tk > 0) {
+            QuantKParams p = qk_params(c, k);
+            p.src = src;
+            p.src_ustride = L0 * c->D;
+            p.src_t0 = ns;
+            p.n_pages = tk / c->G;
+            p.pg0 = 0;
+            ce = launch_keys(c, k, p, st);
+        }
+        if (ce == cudaSuccess && kres > 0) ce = copy_rows(c, src, L0, ns + tk, k->k_res, cap_k(c), 0, kres, st);
     }
-    if (ce == cudaSuccess && kres > 0) ce = copy_rows(c, src, L0, ns + tk, k->k_res, cap_k(c), 0, kres, st);
     if (ce != cudaSuccess) return KVQ_ERR_CUDA;
     if (tk > 0) mark_fresh(k, 0, kNoFresh);
     k->n_sink = ns;
@@ -315,18 +341,31 @@ int kvq_quant_pack_v(const kvq_config *c, kvq_cache *k, const uint16_t *src, int
     if (vres > cap_v(c)) return KVQ_ERR_CAPACITY;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t ce = cudaSuccess;
-    if (ns > 0) ce = copy_rows(c, src, L0, 0, k->v_sink, c->S, 0, ns, st);
-    if (ce == cudaSuccess && tv > 0) {
+    if (tv > 0 && !nvfp4(c)) {  // one launch: the pages, with the sink, residual and window rows
         QuantVParams p = qv_params(c, k);
         p.src = src;
         p.src_ustride = L0 * c->D;
         p.src_t0 = ns;
         p.n_tok = tv;
         p.tok0 = 0;
+        add_rows(p.rc, src, L0, 0, k->v_sink, c->S, 0, ns);
+        add_rows(p.rc, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres);
+        add_rows(p.rc, src, L0, ns + older, k->v_local, c->R, 0, nl);
         ce = launch_values(c, k, p, st);
+    } else {
+        if (ns > 0) ce = copy_rows(c, src, L0, 0, k->v_sink, c->S, 0, ns, st);
+        if (ce == cudaSuccess && tv > 0) {
+            QuantVParams p = qv_params(c, k);
+            p.src = src;
+            p.src_ustride = L0 * c->D;
+            p.src_t0 = ns;
+            p.n_tok = tv;
+            p.tok0 = 0;
+            ce = launch_values(c, k, p, st);
+        }
+        if (ce == cudaSuccess && vres > 0) ce = copy_rows(c, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres, st);
+        if (ce == cudaSuccess && nl > 0) ce = copy_rows(c, src, L0, ns + older, k->v_local, c->R, 0, nl, st);
     }
-    if (ce == cudaSuccess && vres > 0) ce = copy_rows(c, src, L0, ns + tv, k->v_res, cap_v(c), 0, vres, st);
-    if (ce == cudaSuccess && nl > 0) ce = copy_rows(c, src, L0, ns + older, k->v_local, c->R, 0, nl, st);
     if (ce != cudaSuccess) return KVQ_ERR_CUDA;
     if (tv > 0) mark_fresh(k, kNoFresh, 0);
     k->n_sink = ns;

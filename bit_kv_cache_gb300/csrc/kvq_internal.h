@@ -43,6 +43,23 @@ struct PageMap {
     int32_t lp0[kMaxListSeq];
 };
 
+// fp16 rows copied by extra CTAs of a quant launch (the parts of a prefill that stay
+// fp16: sink, residual, local window), so that a prefill side is one launch.  Dense
+// caches only: row i of unit u goes from src[u * src_rows + src_r0 + i] to
+// dst[u * dst_rows + dst_r0 + i] (rows of D halves, 16-byte aligned).
+struct RowCopy {
+    const uint16_t *src;
+    uint16_t *dst;
+    int64_t src_rows, src_r0, dst_rows, dst_r0, n_rows;
+};
+constexpr int kMaxRowCopies = 3;
+struct RowCopies {
+    RowCopy c[kMaxRowCopies];
+    int n;                 // copies in c (0: none)
+    int cols;              // CTAs per unit that copy (set by the launcher)
+    int64_t x0;            // grid column of the first of them (set by the launcher)
+};
+
 struct QuantKParams {
     const uint16_t *src;   // fp16 [U][*][D]
     int64_t src_ustride;   // elements between sequences
@@ -55,6 +72,7 @@ struct QuantKParams {
     uint8_t *k_bidx;
     uint16_t *k_meta;
     int32_t *status;       // device status word (may be null)
+    RowCopies rc;
     PageMap pm;
 };
 
@@ -69,6 +87,7 @@ struct QuantVParams {
     int32_t *v_codes;
     uint16_t *v_meta;
     int32_t *status;       // device status word (may be null)
+    RowCopies rc;
     PageMap pm;
 };
 

@@ -151,6 +151,22 @@ __device__ __forceinline__ int64_t map_dst_page(const PageMap &m, int64_t max_T,
     return e * m.H_kv + h;
 }
 
+// The row copies of unit u carried by a quant launch: CTA `col` of the rc.cols copying
+// CTAs of that unit takes every rc.cols-th 16-byte chunk of each copy.
+__device__ __forceinline__ void row_copies(const RowCopies &rc, int D, int u, int64_t col) {
+    const int cpr = D >> 3;  // chunks per row
+#pragma unroll
+    for (int j = 0; j < kMaxRowCopies; j++) {
+        if (j >= rc.n) break;
+        const RowCopy &c = rc.c[j];
+        const int64_t total = c.n_rows * cpr;
+        const uint4 *s = reinterpret_cast<const uint4 *>(c.src + ((size_t)u * c.src_rows + c.src_r0) * D);
+        uint4 *d = reinterpret_cast<uint4 *>(c.dst + ((size_t)u * c.dst_rows + c.dst_r0) * D);
+        for (int64_t i = col * blockDim.x + threadIdx.x; i < total; i += (int64_t)rc.cols * blockDim.x)
+            d[i] = __ldg(s + i);
+    }
+}
+
 // ------------------------------------------------------------------------------
 // Keys: one CTA per page of G tokens.  Thread (pair pr, slice sl) holds channels
 // 2pr, 2pr+1 for TPS consecutive tokens in registers; min/max (and, for Kitty, the
@@ -168,6 +184,10 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
     unsigned long long *s_score =
         reinterpret_cast<unsigned long long *>(s_max + S * D);  // [S][D] (Kitty)
     int *s_slot = reinterpret_cast<int *>(s_score + (KITTY ? S * D : 0));  // [D]
+    if (blockIdx.x >= p.rc.x0) {
+        row_copies(p.rc, D, blockIdx.y, blockIdx.x - p.rc.x0);
+        return;
+    }
 
     const int tid = threadIdx.x, pr = tid % pairs, sl = tid / pairs;
     const bool active = sl < S;
@@ -300,6 +320,129 @@ __global__ void __launch_bounds__(256) quant_k_kernel(QuantKParams p) {
 }
 
 // ------------------------------------------------------------------------------
+// Keys, KIVI, D = G = 128: one CTA per page, 16 tokens per warp.  Lane l of warp w
+// holds channels 4 l .. 4 l + 3 of tokens 16 w .. 16 w + 15 (each warp load reads one
+// 256-byte token row).  Channel min / max reduce over the lane's tokens in registers
+// and over the warps in shared memory, where threads 0..127 form one channel's group
+// each.  Every lane then quantizes its 64 values with the fp32-pair quantizer and
+// packs its four channels' codes along tokens into whole words; each word row leaves
+// as one 16-byte store (four channels are one chunk of the kword_pos order).  A token
+// that came near a rounding tie has its four codes recomputed with quant_code.
+// (Measured against it: warps that own 16 channels of all 128 tokens, with no CTA
+// barrier, reading 32-byte sectors of 8 rows: 5% slower; a persistent CTA that
+// prefetches the next page with cp.async while it quantizes: 10% slower.)
+// ------------------------------------------------------------------------------
+__device__ __forceinline__ GroupQ group_from_meta(uint32_t m, int max_int) {
+    GroupQ g;
+    g.s16 = (uint16_t)(m & 0xffffu);
+    g.mn16 = (uint16_t)(m >> 16);
+    g.mn = h2f(g.mn16);
+    g.s = h2f(g.s16);
+    g.zero = (g.s == 0.0f);
+    g.inv = g.zero ? 0.0f : __frcp_rn(g.s);
+    g.maxf = (float)max_int;
+    return g;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(256, 4) quant_k_rows(QuantKParams p) {
+    constexpr int D = 128, FPI = 32 / BITS, NWR = 16 / FPI;  // word rows per warp
+    constexpr int MAXI = (1 << BITS) - 1;
+    __shared__ __align__(16) uint16_t s_lo[8][D], s_hi[8][D];  // per warp: channel min / max (fp16)
+    __shared__ __align__(16) float s_mn[D], s_inv[D];
+    __shared__ __align__(16) uint32_t s_meta[D];
+    if (blockIdx.x >= p.rc.x0) {
+        row_copies(p.rc, D, blockIdx.y, blockIdx.x - p.rc.x0);
+        return;
+    }
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int u = blockIdx.y;
+    const int64_t pg = blockIdx.x;
+    if (p.pm.lens && tid == 0 && pg == 0 && u % p.pm.H_kv == 0) {  // paged flush: commit the lengths
+        const int i = u / p.pm.H_kv;
+        int32_t *ln = p.pm.lens + 4 * (size_t)p.pm.seq[i];
+        ln[1] = (int32_t)((p.pm.lp0[i] + p.n_pages) * p.G);
+        ln[2] = 0;
+    }
+    const uint2 *src = reinterpret_cast<const uint2 *>(
+        p.src + (size_t)map_src_unit(p.pm, u) * p.src_ustride + (size_t)(p.src_t0 + pg * 128 + 16 * w) * D) + lane;
+    uint2 x[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) x[j] = __ldg(src + (size_t)j * (D / 4));
+    {
+        __half2 lo0 = *reinterpret_cast<const __half2 *>(&x[0].x), hi0 = lo0;
+        __half2 lo1 = *reinterpret_cast<const __half2 *>(&x[0].y), hi1 = lo1;
+#pragma unroll
+        for (int j = 1; j < 16; j++) {
+            const __half2 a = *reinterpret_cast<const __half2 *>(&x[j].x);
+            const __half2 b = *reinterpret_cast<const __half2 *>(&x[j].y);
+            lo0 = __hmin2(lo0, a);
+            hi0 = __hmax2(hi0, a);
+            lo1 = __hmin2(lo1, b);
+            hi1 = __hmax2(hi1, b);
+        }
+        reinterpret_cast<uint2 *>(&s_lo[w][0])[lane] =
+            make_uint2(*reinterpret_cast<uint32_t *>(&lo0), *reinterpret_cast<uint32_t *>(&lo1));
+        reinterpret_cast<uint2 *>(&s_hi[w][0])[lane] =
+            make_uint2(*reinterpret_cast<uint32_t *>(&hi0), *reinterpret_cast<uint32_t *>(&hi1));
+    }
+    __syncthreads();
+    const int64_t page = map_dst_page(p.pm, p.max_T, p.G, p.pg0, u, pg);
+    if (tid < D) {  // channel tid's group over the page
+        float mn = h2f(s_lo[0][tid]), mx = h2f(s_hi[0][tid]);
+#pragma unroll
+        for (int ww = 1; ww < 8; ww++) {
+            mn = fminf(mn, h2f(s_lo[ww][tid]));
+            mx = fmaxf(mx, h2f(s_hi[ww][tid]));
+        }
+        const GroupQ g = make_group(mn, mx, MAXI);
+        s_mn[tid] = g.mn;
+        s_inv[tid] = g.inv;
+        const uint32_t m = (uint32_t)g.s16 | ((uint32_t)g.mn16 << 16);
+        s_meta[tid] = m;
+        reinterpret_cast<uint32_t *>(p.k_meta + (size_t)page * D * 2)[tid] = m;
+    }
+    __syncthreads();
+    const float4 mn4 = reinterpret_cast<const float4 *>(s_mn)[lane];
+    const float4 in4 = reinterpret_cast<const float4 *>(s_inv)[lane];
+    const uint64_t mn01 = pk2(mn4.x, mn4.y), mn23 = pk2(mn4.z, mn4.w);
+    const uint64_t in01 = pk2(in4.x, in4.y), in23 = pk2(in4.z, in4.w);
+    constexpr uint32_t lim = kMagicBits + MAXI;
+    uint32_t wd[NWR][4];
+#pragma unroll
+    for (int r = 0; r < NWR; r++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) wd[r][c] = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        uint32_t a0, a1, a2, a3;
+        float em = 0.f;
+        qbits2(x[j].x, mn01, in01, lim, a0, a1, em);
+        qbits2(x[j].y, mn23, in23, lim, a2, a3, em);
+        if (em > kTieMargin) {  // near a half-integer: this token's exact quotients
+            const float2 f01 = unpack_half2(x[j].x), f23 = unpack_half2(x[j].y);
+            a0 = kMagicBits + quant_code(f01.x, group_from_meta(s_meta[4 * lane], MAXI));
+            a1 = kMagicBits + quant_code(f01.y, group_from_meta(s_meta[4 * lane + 1], MAXI));
+            a2 = kMagicBits + quant_code(f23.x, group_from_meta(s_meta[4 * lane + 2], MAXI));
+            a3 = kMagicBits + quant_code(f23.y, group_from_meta(s_meta[4 * lane + 3], MAXI));
+        }
+        const uint32_t m = 1u << (BITS * (j % FPI));
+        wd[j / FPI][0] += a0 * m;
+        wd[j / FPI][1] += a1 * m;
+        wd[j / FPI][2] += a2 * m;
+        wd[j / FPI][3] += a3 * m;
+    }
+    const int64_t row0 = page * (128 / FPI) + w * NWR;  // first word row of this warp
+#pragma unroll
+    for (int r = 0; r < NWR; r++) {
+        const uint32_t off = magic_sum(BITS, FPI);
+        const int R = w * NWR + r;
+        *reinterpret_cast<uint4 *>(p.k_codes + (size_t)(row0 + r) * D + kword_pos(4 * lane, R)) =
+            make_uint4(wd[r][0] - off, wd[r][1] - off, wd[r][2] - off, wd[r][3] - off);
+    }
+}
+
+// ------------------------------------------------------------------------------
 // Values: one thread per token; the whole row (ND x 8 halves) sits in registers.
 // ------------------------------------------------------------------------------
 template <int BITS, int ND, int GV>
@@ -307,6 +450,10 @@ __global__ void __launch_bounds__(128) quant_v_kernel(QuantVParams p) {
     constexpr int FPI = 32 / BITS, D = ND * 8, NWORD = D / FPI;
     static_assert(GV % FPI == 0 && D % GV == 0, "whole words per value group");
     const int u = blockIdx.y;
+    if (blockIdx.x >= p.rc.x0) {
+        row_copies(p.rc, D, u, blockIdx.x - p.rc.x0);
+        return;
+    }
     const int64_t tl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // token within call
     if (tl >= p.n_tok) return;
     const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -447,6 +594,10 @@ __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int6
 template <int BITS>
 __global__ void __launch_bounds__(256) quant_v_rows(QuantVParams p) {
     const int u = blockIdx.y;
+    if (blockIdx.x >= p.rc.x0) {
+        row_copies(p.rc, 128, u, blockIdx.x - p.rc.x0);
+        return;
+    }
     const int64_t tl0 = (int64_t)blockIdx.x * 128;
     quant_v_chunk<BITS>(p, u, tl0,
                         p.src + (size_t)map_src_unit(p.pm, u) * p.src_ustride + (size_t)(p.src_t0 + tl0) * 128);
@@ -656,9 +807,19 @@ __global__ void set_lens_kernel(SetLensParams p) {
 // ------------------------------------------------------------------------------
 // Launchers
 // ------------------------------------------------------------------------------
+// CTAs per unit for the row copies of a quant launch: about one 16-byte chunk per
+// thread of a 256-thread CTA, at most 64.
+static int row_copy_cols(const RowCopies &rc, int D) {
+    int64_t most = 0;
+    for (int j = 0; j < rc.n; j++) most = most > rc.c[j].n_rows ? most : rc.c[j].n_rows;
+    if (rc.n <= 0 || most <= 0) return 0;
+    const int64_t cols = (most * (D / 8) + 255) / 256;
+    return (int)(cols < 64 ? cols : 64);
+}
+
 template <int BITS, bool KITTY>
 static cudaError_t launch_qk_tps(const QuantKParams &p, int tps, size_t smem, cudaStream_t st) {
-    dim3 grid((unsigned)p.n_pages, (unsigned)p.U);
+    dim3 grid((unsigned)(p.n_pages + p.rc.cols), (unsigned)p.U);
     switch (tps) {
 #define KVQ_TPS(T)                                                                        \
     case T:                                                                               \
@@ -688,6 +849,16 @@ cudaError_t launch_quant_k(const QuantKParams &p_in, int bits, bool kitty, cudaS
     if (S == 0) return cudaErrorInvalidValue;
     const int tps = p.G / S;
     p.slices = S;
+    p.rc.x0 = p.n_pages;
+    p.rc.cols = row_copy_cols(p.rc, p.D);
+    if (!kitty && p.D == 128 && p.G == 128) {  // whole-word rows, fp32-pair quantizer
+        dim3 grid((unsigned)(p.n_pages + p.rc.cols), (unsigned)p.U);
+        if (bits == 2) quant_k_rows<2><<<grid, 256, 0, st>>>(p);
+        else if (bits == 4) quant_k_rows<4><<<grid, 256, 0, st>>>(p);
+        else if (bits == 8) quant_k_rows<8><<<grid, 256, 0, st>>>(p);
+        else return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     size_t smem = (size_t)S * p.D * 8 + (kitty ? (size_t)S * p.D * 8 + (size_t)p.D * 4 : 0);
     if (kitty) return launch_qk_tps<2, true>(p, tps, smem, st);
     if (bits == 2) return launch_qk_tps<2, false>(p, tps, smem, st);
@@ -696,17 +867,21 @@ cudaError_t launch_quant_k(const QuantKParams &p_in, int bits, bool kitty, cudaS
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_quant_v(const QuantVParams &p, int bits, cudaStream_t st) {
+cudaError_t launch_quant_v(const QuantVParams &p_in, int bits, cudaStream_t st) {
+    QuantVParams p = p_in;
     if (p.n_tok <= 0) return cudaSuccess;
+    p.rc.x0 = (p.n_tok + 127) / 128;
+    p.rc.cols = row_copy_cols(p.rc, p.D);
+    const unsigned gx = (unsigned)(p.rc.x0 + p.rc.cols);
     if ((bits == 2 || bits == 4) && p.D == 128 && p.Gv == 128 && p.G % 128 == 0 && p.n_tok % 128 == 0 &&
         p.tok0 % 128 == 0) {
-        dim3 grid((unsigned)(p.n_tok / 128), (unsigned)p.U);
+        dim3 grid(gx, (unsigned)p.U);
         if (bits == 2) quant_v_rows<2><<<grid, 256, 0, st>>>(p);
         else if (bits == 4) quant_v_rows<4><<<grid, 256, 0, st>>>(p);
         else return cudaErrorInvalidValue;
         return cudaGetLastError();
     }
-    dim3 grid((unsigned)((p.n_tok + 127) / 128), (unsigned)p.U);
+    dim3 grid(gx, (unsigned)p.U);
 #define KVQ_QV(B, N, GVV)                                          \
     if (bits == B && p.D == N * 8 && p.Gv == GVV) {                \
         quant_v_kernel<B, N, GVV><<<grid, 128, 0, st>>>(p);        \
