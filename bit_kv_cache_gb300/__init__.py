@@ -25,7 +25,7 @@ EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
            "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_step_io_bytes", "kvq_decode_step_host",
-           "kvq_append_decode",
+           "kvq_decode_step_host_wait", "kvq_append_decode",
            "kvq_paged_bytes", "kvq_paged_init",
            "kvq_paged_prefill", "kvq_paged_append", "kvq_paged_flush_plan", "kvq_paged_flush",
            "kvq_paged_release", "kvq_paged_workspace_bytes", "kvq_paged_decode_attn",
@@ -86,6 +86,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_step_io_bytes": ([CP], Sz),
         "kvq_append_decode": ([CP, KP, P, P, P, P, P, Sz, IP, P], I),
         "kvq_decode_step_host": ([CP, KP, P, P, P, P, P, Sz, P, Sz, IP, IP, P], I),
+        "kvq_decode_step_host_wait": ([CP, KP, P, P, P, P, P, P, Sz, IP, IP, P], I),
         "kvq_paged_bytes": ([CP, I64, I], Sz),
         "kvq_paged_init": ([CP, PP, P], I),
         "kvq_paged_prefill": ([CP, PP, I, P, P, I64, P], I),
@@ -158,6 +159,7 @@ class KVQCache:
         # staging of kvq_decode_step_host (q, k_new, v_new, out of one step)
         self.io = torch.empty(lib.kvq_step_io_bytes(ctypes.byref(self.cfg)), dtype=torch.uint8,
                               device=self.device)
+        self.done = None  # completion count of kvq_decode_step_host_wait (page-locked, made on first use)
 
     # -- helpers ------------------------------------------------------------- #
     @staticmethod
@@ -248,11 +250,13 @@ class KVQCache:
         self.flush_group()
         return out
 
-    def step_host(self, q, k_new, v_new, out):
+    def step_host(self, q, k_new, v_new, out, wait=False):
         """One decode step from host tensors (kvq_decode_step_host): q, out [B, H_q, D],
         k_new, v_new [B, H_kv, D], contiguous float16 on the CPU (page-locked for the
         copies to be asynchronous).  Enqueued on the current stream; out holds the
-        result once the stream is synchronized.  Returns (flushed_k, flushed_v)."""
+        result once the stream is synchronized.  wait (kvq_decode_step_host_wait; all
+        four tensors page-locked): returns once out holds the result.  Returns
+        (flushed_k, flushed_v)."""
         torch = self.torch
         for t, shp, what in ((q, (self.cfg.B, self.cfg.H_q, self.cfg.D), "q"),
                              (out, (self.cfg.B, self.cfg.H_q, self.cfg.D), "out"),
@@ -262,6 +266,17 @@ class KVQCache:
                     tuple(t.shape) != shp:
                 raise ValueError("%s must be a contiguous float16 CPU tensor of shape %s" % (what, shp))
         fk, fv = ctypes.c_int(0), ctypes.c_int(0)
+        if wait:
+            if self.done is None:
+                self.done = torch.zeros(1, dtype=torch.int32).pin_memory()
+            _check(lib.kvq_decode_step_host_wait(ctypes.byref(self.cfg), ctypes.byref(self.c),
+                                                 ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
+                                                 ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                                 ctypes.c_void_p(self.done.data_ptr()),
+                                                 ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+                                                 ctypes.byref(fk), ctypes.byref(fv), self._stream()),
+                   "kvq_decode_step_host_wait")
+            return bool(fk.value), bool(fv.value)
         _check(lib.kvq_decode_step_host(ctypes.byref(self.cfg), ctypes.byref(self.c),
                                         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_new.data_ptr()),
                                         ctypes.c_void_p(v_new.data_ptr()), ctypes.c_void_p(out.data_ptr()),

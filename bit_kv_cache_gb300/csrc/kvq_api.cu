@@ -3,6 +3,8 @@
 // Every entry point validates before it enqueues anything, returns a status, and
 // leaves the cache untouched on an argument error.
 #include <cuda_runtime.h>
+
+#include <chrono>
 #include <stdint.h>
 #include <string.h>
 
@@ -484,15 +486,18 @@ int kvq_workspace_init(void *ws, size_t ws_bytes, void *stream) {
 static constexpr int kDeclined = 1;
 static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
                        size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn,
-                       int32_t *status_word = nullptr);
+                       int32_t *status_word = nullptr, unsigned int *done = nullptr);
 
 int kvq_decode_attn(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
                     size_t ws_bytes, void *stream) {
     return decode_impl(c, k, q, out, ws, ws_bytes, stream, nullptr, nullptr);
 }
 
-int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, const uint16_t *vn,
-                      const uint16_t *q, uint16_t *out, void *ws, size_t ws_bytes, int *fused, void *stream) {
+// kvq_append_decode; done (device address, may be null): the decode kernel's
+// completion count (DecodeParams::done).
+static int append_decode_impl(const kvq_config *c, kvq_cache *k, const uint16_t *kn, const uint16_t *vn,
+                              const uint16_t *q, uint16_t *out, void *ws, size_t ws_bytes, int *fused,
+                              void *stream, unsigned int *done) {
     if (fused) *fused = 0;
     int e = kvq_config_check(c);
     if (e) return e;
@@ -505,7 +510,7 @@ int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, con
         kvq_cache nk = *k;
         nk.n_kres++;
         nk.n_vres++;
-        e = decode_impl(c, &nk, q, out, ws, ws_bytes, stream, kn, vn);
+        e = decode_impl(c, &nk, q, out, ws, ws_bytes, stream, kn, vn, nullptr, done);
         if (e != kDeclined) {
             if (e == KVQ_OK) {
                 *k = nk;
@@ -515,12 +520,17 @@ int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, con
         }
     }
     if ((e = kvq_append_token(c, k, kn, vn, stream))) return e;
-    return kvq_decode_attn(c, k, q, out, ws, ws_bytes, stream);
+    return decode_impl(c, k, q, out, ws, ws_bytes, stream, nullptr, nullptr, nullptr, done);
+}
+
+int kvq_append_decode(const kvq_config *c, kvq_cache *k, const uint16_t *kn, const uint16_t *vn,
+                      const uint16_t *q, uint16_t *out, void *ws, size_t ws_bytes, int *fused, void *stream) {
+    return append_decode_impl(c, k, kn, vn, q, out, ws, ws_bytes, fused, stream, nullptr);
 }
 
 static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *q, uint16_t *out, void *ws,
                        size_t ws_bytes, void *stream, const uint16_t *kn, const uint16_t *vn,
-                       int32_t *status_word) {
+                       int32_t *status_word, unsigned int *done) {
     int e = kvq::host::decode_check_args(c, k, q, out);
     if (e) return e;
     const int64_t L = k->n_sink + k->T_k + k->n_kres;
@@ -701,6 +711,8 @@ static int decode_impl(const kvq_config *c, const kvq_cache *k, const uint16_t *
     p.v_new = vn;
     char *w = static_cast<char *>(ws);
     p.status = status_word ? status_word : reinterpret_cast<int32_t *>(w + wl.status);
+    p.done = done;
+    p.done_ctr = reinterpret_cast<unsigned int *>(w + wl.status + 16);  // in the status block
     p.slot_ctr = nullptr;  // dense caches: a CTA's slot follows from the schedule
     {
         const int64_t fresh = take_fresh(k);
@@ -783,6 +795,37 @@ int kvq_decode_step_host(const kvq_config *c, kvq_cache *k, const uint16_t *q, c
     if ((e = kvq_append_decode(c, k, dk, dv, dq, dout, ws, ws_bytes, nullptr, stream))) return e;
     if ((e = kvq_flush_group(c, k, flushed_k, flushed_v, stream))) return e;
     if (!direct && cudaMemcpyAsync(out, dout, nq, cudaMemcpyDefault, st) != cudaSuccess) return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+int kvq_decode_step_host_wait(const kvq_config *c, kvq_cache *k, const uint16_t *q, const uint16_t *k_new,
+                              const uint16_t *v_new, uint16_t *out, unsigned int *done, void *ws, size_t ws_bytes,
+                              int *flushed_k, int *flushed_v, void *stream) {
+    int e = kvq_config_check(c);
+    if (e) return e;
+    if (!k || !q || !k_new || !v_new || !out || !done || ((uintptr_t)done & 3)) return KVQ_ERR_INVALID_ARG;
+    const void *mq = mapped_host(q), *mk = mapped_host(k_new), *mv = mapped_host(v_new);
+    void *mo = const_cast<void *>(mapped_host(out));
+    unsigned int *md = static_cast<unsigned int *>(const_cast<void *>(mapped_host(done)));
+    if (!mq || !mk || !mv || !mo || !md || !aligned16(mq) || !aligned16(mk) || !aligned16(mv) || !aligned16(mo))
+        return KVQ_ERR_INVALID_ARG;
+    __atomic_store_n(done, 0u, __ATOMIC_RELEASE);  // before the launch that counts into it
+    if ((e = append_decode_impl(c, k, static_cast<const uint16_t *>(mk), static_cast<const uint16_t *>(mv),
+                                static_cast<const uint16_t *>(mq), static_cast<uint16_t *>(mo), ws, ws_bytes,
+                                nullptr, stream, md)))
+        return e;
+    if ((e = kvq_flush_group(c, k, flushed_k, flushed_v, stream))) return e;
+    // Every sequence is combined by exactly one CTA, which counts it after its output
+    // stores; the last one releases U to *done.  Spin on it, then (past a bound) fall
+    // back to the stream.
+    const unsigned int want = (unsigned int)units(c);
+    const auto t0 = std::chrono::steady_clock::now();
+    for (uint32_t spins = 0; __atomic_load_n(done, __ATOMIC_ACQUIRE) < want; spins++) {
+        if ((spins & 1023u) == 1023u && std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(200)) {
+            if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KVQ_ERR_CUDA;
+            return __atomic_load_n(done, __ATOMIC_ACQUIRE) == want ? KVQ_OK : KVQ_ERR_DEVICE;
+        }
+    }
     return KVQ_OK;
 }
 

@@ -331,6 +331,18 @@ __device__ __forceinline__ int dense_slot(const DecodeParams &p, int u, bool til
     return (int)(nf + c - cta_of_item(p.W_m, p.N_m, (long long)u * p.n_mini, p.wpc));
 }
 
+// Completion count of a blocking host step (DecodeParams::done): one thread of a CTA
+// that combined n sequences, after the CTA's output stores were fenced at system
+// scope, adds n to the device counter; the CTA that brings it to U resets it and
+// releases U to the host word.
+__device__ __forceinline__ void count_done(const DecodeParams &p, unsigned int n) {
+    unsigned int before;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(before) : "l"(p.done_ctr), "r"(n) : "memory");
+    if (before + n == (unsigned int)p.U) {
+        *p.done_ctr = 0u;
+        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.done), "r"((unsigned int)p.U) : "memory");
+    }
+}
 __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long *ptr, unsigned long long v) {
     unsigned long long old;
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
@@ -471,10 +483,12 @@ static __device__ void publish_whole(const DecodeParams &p, int u, int cnt, int 
     const int ns = min((int)(before & 0xffffffffu) + 1, p.smax);
     const int D4 = p.D / 4;
     for (int i = lane; i < p.g * D4; i += 32) combine_item<true>(p, u, ns, i / D4, 4 * (i % D4));
+    if (p.done) __threadfence_system();
     __syncwarp();
     if (lane == 0) {
         p.slot_ctr[u] = 0;
         p.item_ctr[u] = 0;
+        if (p.done) count_done(p, 1u);
     }
 }
 
@@ -814,11 +828,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_kernel(const DecodeParams p
         const int lk = pi / g, h = pi - lk * g;
         combine_item<RG>(p, s_lu[lk], min(s_ns[lk], RG ? p.smax : p.max_slots), h, d);
     }
+    if (p.done) __threadfence_system();  // this thread's output stores, before the count
     __syncthreads();
     if (tid < nl) {
         if (RG) p.slot_ctr[s_lu[tid]] = 0;
         p.item_ctr[s_lu[tid]] = 0;
     }
+    if (p.done && tid == 0) count_done(p, (unsigned int)nl);
 }
 
 // ---------------------------------------------------------------------------------

@@ -171,6 +171,10 @@ struct DecodeParams {
     int32_t *slot_ctr;     // [U] slots taken (paged caches; zero between calls)
     unsigned long long *item_ctr;  // [U] items merged << 32 | CTAs arrived (zero between calls)
     int32_t *status;       // workspace status word
+    // blocking host step (null: none): done is a host word that receives U, at system
+    // scope, once every sequence's output is visible there; done_ctr counts the
+    // combined sequences (workspace, zero between calls)
+    unsigned int *done, *done_ctr;
     // schedule
     int U, wpc;            // sequences, warps per CTA
     int C_f, C_m, C_g;     // CTAs of the fast, mini and generic pools (grid: mini, fast; or generic)

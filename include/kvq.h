@@ -268,6 +268,26 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
                          size_t io_bytes, void *ws, size_t ws_bytes, int *flushed_k,
                          int *flushed_v, void *stream);
 
+/* kvq_decode_step_host for page-locked, mapped host buffers, returning once the
+ * output is in out: a blocking decode step (Kitty Sec. 4.3 stages 1-3 with the host
+ * transfers).
+ * done: a 4-byte-aligned unsigned int in page-locked host memory mapped into the
+ * device's address space, owned by the caller, used as a completion word: the call
+ * sets it to 0 before it launches; the decode kernel counts the sequences whose
+ * output stores it has made visible at system scope (in the workspace) and, when the
+ * count reaches B * H_kv, stores B * H_kv to *done (release, system scope); the call
+ * spins until it reads that value (after 200 ms it synchronizes the stream instead).
+ * When it returns KVQ_OK, out holds the result; a flush enqueued by the step may still
+ * be running on `stream`.
+ * KVQ_ERR_INVALID_ARG if any of q, k_new, v_new, out, done is missing or not mapped
+ * page-locked memory, or a buffer is not 16-byte aligned (done: 4); KVQ_ERR_DEVICE if
+ * the stream completed without *done reaching B * H_kv.  Other errors as for
+ * kvq_decode_step_host (no io buffer is needed). */
+int kvq_decode_step_host_wait(const kvq_config *cfg, kvq_cache *cache, const uint16_t *q,
+                              const uint16_t *k_new, const uint16_t *v_new, uint16_t *out,
+                              unsigned int *done, void *ws, size_t ws_bytes, int *flushed_k,
+                              int *flushed_v, void *stream);
+
 /* Stages (1) and (2) together: kvq_append_token(k_new, v_new), then kvq_decode_attn(q,
  * out), with the same arguments, layouts, results and errors.  Where the token goes to
  * the key and value residuals of a KIVI cache (sink full) and the packed-tile path

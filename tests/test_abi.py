@@ -196,3 +196,23 @@ def test_noalloc_refusals_before_any_launch(kvq):
     big = _cfg(kvq, B=512, H_q=32, H_kv=32, max_T=1024)
     assert kvq.lib.kvq_decode_attn_workspace_bytes(ctypes.byref(big)) > 16 * 1024 * 1024
     assert f(ctypes.byref(big), ctypes.byref(full), P(0x3000), P(0x4000), None) == -4
+
+
+def test_step_host_wait_refusals_before_any_launch(kvq):
+    """The blocking host step refuses missing, unaligned or unmapped buffers (fake
+    pointers, never dereferenced) before it writes the count or enqueues anything."""
+    P = ctypes.c_void_p
+    f = kvq.lib.kvq_decode_step_host_wait
+    c = _cfg(kvq)
+    cache = kvq.Cache()
+    done = ctypes.c_uint(7)
+
+    def call(q=P(0x1000), d=ctypes.cast(ctypes.byref(done), P), cfg=c):
+        return f(ctypes.byref(cfg), ctypes.byref(cache), q, P(0x1000), P(0x1000), P(0x1000), d, P(0x20000),
+                 1 << 20, None, None, None)
+    assert call(d=P(0)) == -1                         # no count word
+    assert call(d=P(0x1002)) == -1                    # count word not 4-byte aligned
+    assert call(q=P(0)) == -1                         # a missing host buffer
+    assert call() == -1                               # not page-locked mapped memory
+    assert call(cfg=_cfg(kvq, H_q=7)) == -1           # invalid configuration
+    assert done.value == 7                            # the count was never written

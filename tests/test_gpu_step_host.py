@@ -38,12 +38,14 @@ def _cache(kvq, wl, K, V):
     return c
 
 
-@pytest.mark.parametrize("pinned", [True, False], ids=["mapped", "pageable"])
+@pytest.mark.parametrize("mode", ["mapped", "pageable", "wait"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_host_step_matches_device_steps(kvq, name, pinned):
+def test_host_step_matches_device_steps(kvq, name, mode):
     """Page-locked (mapped) host buffers are read and written by the kernels in place;
-    pageable ones go through copies into the staging buffer."""
+    pageable ones go through copies into the staging buffer.  wait: the blocking entry
+    point, whose output is read as soon as the call returns (no synchronization)."""
     import torch
+    pinned, wait = mode != "pageable", mode == "wait"
 
     def host_mem(t):
         return t.pin_memory() if pinned else t
@@ -61,13 +63,17 @@ def test_host_step_matches_device_steps(kvq, name, pinned):
         ref = dev.decode_attn(to_dev(qs[i], DEV))
         fd = dev.flush_group()
         out = host_mem(torch.full(tuple(qs[i].shape), float("nan"), dtype=torch.float16))
+        ref_u16 = ref.cpu().numpy().view(np.uint16)     # the device path, synchronized
         fh = host.step_host(host_mem(torch.from_numpy(qs[i])), host_mem(torch.from_numpy(kn[i])),
-                            host_mem(torch.from_numpy(vn[i])), out)
+                            host_mem(torch.from_numpy(vn[i])), out, wait=wait)
+        if wait:
+            a = out.numpy().copy()                     # read before any synchronization
         torch.cuda.synchronize()
         assert fh == fd
         flushes += fd[0] or fd[1]
-        a = out.numpy()
-        assert np.array_equal(a.view(np.uint16), ref.cpu().numpy().view(np.uint16))
+        if not wait:
+            a = out.numpy()
+        assert np.array_equal(a.view(np.uint16), ref_u16)
         ora.append(kn[i], vn[i])
         assert_close(a, ora.attend(qs[i]), what="host step %d" % i)
         assert ora.flush() == fh
@@ -76,3 +82,22 @@ def test_host_step_matches_device_steps(kvq, name, pinned):
     for name_ in host.buf:                                # packed state and buffers: bit-exact
         assert torch.equal(host.buf[name_], dev.buf[name_]), name_
     assert host.read_status() == 0 and dev.read_status() == 0
+
+
+def test_host_step_wait_refuses_unmapped(kvq):
+    """The blocking entry point wants page-locked buffers and a page-locked count word;
+    otherwise it refuses before it enqueues anything (the cache is unchanged)."""
+    import torch
+    wl, L0 = CASES["tiny_kivi"]
+    K, V = kvq_synth.prefill_kv(wl, L0)
+    c = _cache(kvq, wl, K, V)
+    kn, vn = kvq_synth.decode_tokens(wl, 1)
+    q = kvq_synth.queries(wl, 1)[0]
+    out = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
+    before = c.lengths
+    with pytest.raises(kvq.KvqError):
+        c.step_host(torch.from_numpy(q), torch.from_numpy(kn[0]).pin_memory(),
+                    torch.from_numpy(vn[0]).pin_memory(), out, wait=True)   # q pageable
+    assert c.lengths == before
+    torch.cuda.synchronize()
+    assert c.read_status() == 0
