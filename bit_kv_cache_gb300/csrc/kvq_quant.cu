@@ -344,6 +344,15 @@ __device__ __forceinline__ GroupQ group_from_meta(uint32_t m, int max_int) {
     return g;
 }
 
+// The exact codes of one token's four channels (x: two half2 words; m: their
+// (scale, min) words).  Out of line: the rare near-tie path stays out of the unrolled
+// loop, whose code would otherwise outgrow the instruction cache.
+__device__ __noinline__ uint4 exact_codes4(uint2 x, uint4 m, int max_int) {
+    const float2 f01 = unpack_half2(x.x), f23 = unpack_half2(x.y);
+    return make_uint4(quant_code(f01.x, group_from_meta(m.x, max_int)), quant_code(f01.y, group_from_meta(m.y, max_int)),
+                      quant_code(f23.x, group_from_meta(m.z, max_int)), quant_code(f23.y, group_from_meta(m.w, max_int)));
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(256, 4) quant_k_rows(QuantKParams p) {
     constexpr int D = 128, FPI = 32 / BITS, NWR = 16 / FPI;  // word rows per warp
@@ -420,11 +429,11 @@ __global__ void __launch_bounds__(256, 4) quant_k_rows(QuantKParams p) {
         qbits2(x[j].x, mn01, in01, lim, a0, a1, em);
         qbits2(x[j].y, mn23, in23, lim, a2, a3, em);
         if (em > kTieMargin) {  // near a half-integer: this token's exact quotients
-            const float2 f01 = unpack_half2(x[j].x), f23 = unpack_half2(x[j].y);
-            a0 = kMagicBits + quant_code(f01.x, group_from_meta(s_meta[4 * lane], MAXI));
-            a1 = kMagicBits + quant_code(f01.y, group_from_meta(s_meta[4 * lane + 1], MAXI));
-            a2 = kMagicBits + quant_code(f23.x, group_from_meta(s_meta[4 * lane + 2], MAXI));
-            a3 = kMagicBits + quant_code(f23.y, group_from_meta(s_meta[4 * lane + 3], MAXI));
+            const uint4 e = exact_codes4(x[j], reinterpret_cast<const uint4 *>(s_meta)[lane], MAXI);
+            a0 = kMagicBits + e.x;
+            a1 = kMagicBits + e.y;
+            a2 = kMagicBits + e.z;
+            a3 = kMagicBits + e.w;
         }
         const uint32_t m = 1u << (BITS * (j % FPI));
         wd[j / FPI][0] += a0 * m;
