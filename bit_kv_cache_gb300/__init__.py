@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
 
 KVQ_MODE_KIVI, KVQ_MODE_KITTY, KVQ_MODE_NVFP4 = 0, 1, 2
+KVQ_DEV_TIMEOUT, KVQ_DEV_BAD_STATE = 1, 2  # device status-word bits
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
           -3: "capacity exceeded", -4: "workspace missing or too small", -5: "CUDA error",
           -6: "device-side error reported"}
@@ -25,7 +26,7 @@ EXPORTS = ("kvq_status_str", "kvq_config_check", "kvq_buffer_bytes", "kvq_quant_
            "kvq_quant_pack_v", "kvq_append_token", "kvq_flush_group",
            "kvq_decode_attn_workspace_bytes", "kvq_workspace_init", "kvq_decode_attn",
            "kvq_read_status", "kvq_decode_attn_noalloc", "kvq_step_io_bytes", "kvq_decode_step_host",
-           "kvq_decode_step_host_wait", "kvq_append_decode",
+           "kvq_decode_step_host_wait", "kvq_selftest_wait_timeout", "kvq_append_decode",
            "kvq_paged_bytes", "kvq_paged_init",
            "kvq_paged_prefill", "kvq_paged_append", "kvq_paged_flush_plan", "kvq_paged_flush",
            "kvq_paged_release", "kvq_paged_workspace_bytes", "kvq_paged_decode_attn",
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_append_decode": ([CP, KP, P, P, P, P, P, Sz, IP, P], I),
         "kvq_decode_step_host": ([CP, KP, P, P, P, P, P, Sz, P, Sz, IP, IP, P], I),
         "kvq_decode_step_host_wait": ([CP, KP, P, P, P, P, P, P, Sz, IP, IP, P], I),
+        "kvq_selftest_wait_timeout": ([P, P], I),
         "kvq_paged_bytes": ([CP, I64, I], Sz),
         "kvq_paged_init": ([CP, PP, P], I),
         "kvq_paged_prefill": ([CP, PP, I, P, P, I64, P], I),

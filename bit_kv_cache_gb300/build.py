@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_quant.cu", "kvq_decode.cu", "kvq_noalloc.cu", "kvq_paged.cu",
-           "kvq_decode_paged.cu", "kvq_decode_rope.cu", "kvq_decode_nvfp4.cu"]
+           "kvq_decode_paged.cu", "kvq_decode_rope.cu", "kvq_decode_nvfp4.cu", "kvq_selftest.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "kvq_decode_fast.cuh", "kvq_host.h",
            "kvq_decode.cuh"]
 

@@ -288,6 +288,14 @@ int kvq_decode_step_host_wait(const kvq_config *cfg, kvq_cache *cache, const uin
                               unsigned int *done, void *ws, size_t ws_bytes, int *flushed_k,
                               int *flushed_v, void *stream);
 
+/* Self-test of the kernels' bounded waits (no counterpart on the pages): one warp
+ * waits, through the same bounded mbarrier wait the decode kernels use, on a barrier
+ * that nothing completes.  At the kernels' bound (4e9 SM clock cycles, about 2 s at
+ * 2 GHz) the wait gives up, ORs KVQ_DEV_TIMEOUT into *status (device int32, 4-byte
+ * aligned) and the kernel returns; the context stays usable.  Enqueued on `stream`.
+ * KVQ_ERR_INVALID_ARG for a missing or misaligned status word. */
+int kvq_selftest_wait_timeout(int32_t *status, void *stream);
+
 /* Stages (1) and (2) together: kvq_append_token(k_new, v_new), then kvq_decode_attn(q,
  * out), with the same arguments, layouts, results and errors.  Where the token goes to
  * the key and value residuals of a KIVI cache (sink full) and the packed-tile path

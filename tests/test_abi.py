@@ -216,3 +216,12 @@ def test_step_host_wait_refusals_before_any_launch(kvq):
     assert call() == -1                               # not page-locked mapped memory
     assert call(cfg=_cfg(kvq, H_q=7)) == -1           # invalid configuration
     assert done.value == 7                            # the count was never written
+
+
+def test_selftest_wait_refusals(kvq):
+    """The bounded-wait self-test refuses a missing or misaligned status word before it
+    launches anything."""
+    P = ctypes.c_void_p
+    f = kvq.lib.kvq_selftest_wait_timeout
+    assert f(None, None) == -1
+    assert f(P(0x1002), None) == -1
