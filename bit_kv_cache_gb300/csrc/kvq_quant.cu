@@ -599,9 +599,10 @@ __device__ __forceinline__ void quant_v_chunk(const QuantVParams &p, int u, int6
             *reinterpret_cast<const uint4 *>(&s_meta[4 * tid]);
 }
 
-// One CTA per 128 value tokens, reading its rows straight from global memory.
+// One CTA per 128 value tokens, reading its rows straight from global memory; five
+// CTAs per SM (48 registers) hide more of the loads' latency than four.
 template <int BITS>
-__global__ void __launch_bounds__(256) quant_v_rows(QuantVParams p) {
+__global__ void __launch_bounds__(256, 5) quant_v_rows(QuantVParams p) {
     const int u = blockIdx.y;
     if (blockIdx.x >= p.rc.x0) {
         row_copies(p.rc, 128, u, blockIdx.x - p.rc.x0);
